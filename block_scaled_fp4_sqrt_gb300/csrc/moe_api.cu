@@ -1,0 +1,468 @@
+// Host side of the C ABI declared in include/moe.h: argument checks, handles, the workspace
+// carve-up, TMA tensor-map encoding and the launch sequence of one layer forward.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <string>
+
+#include "moe.h"
+#include "moe_internal.h"
+#include "moe_testing.h"
+
+using namespace moe;
+
+struct moe_experts_s {
+  moe_config_t cfg;
+  int n = 0;  // experts in this set
+  const uint8_t* w13 = nullptr;
+  const uint8_t* w2 = nullptr;
+  uint8_t* sf13 = nullptr;  // owned: scale atoms [n, 2f/128, d/128, 512]
+  uint8_t* sf2 = nullptr;   // owned: [n, d/128, f/128, 512]
+  CUtensorMap tm13;
+  CUtensorMap tm2;
+  const int32_t* hash_table = nullptr;
+  int32_t hash_V = 0;
+  void* ws_base = nullptr;
+  size_t ws_bytes = 0;
+  int32_t ws_max_T = 0;
+  Workspace ws{};
+  int* status = nullptr;  // owned: device status word
+  uint64_t budget_ns = 2000000000ull;
+  int num_sms = 0;
+  int device = 0;
+  int32_t last_T = 0;
+  int stall_loads = 0;
+};
+
+namespace {
+
+thread_local std::string g_last_error;
+
+moe_status_t fail(moe_status_t st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+
+moe_status_t cuda_fail(cudaError_t e, const char* what) {
+  return fail(MOE_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+#define MOE_CUDA(call, what)                       \
+  do {                                             \
+    cudaError_t e_ = (call);                       \
+    if (e_ != cudaSuccess) return cuda_fail(e_, what); \
+  } while (0)
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// 2-D K-major tensor map: inner dimension K (elements), outer `rows`, box {128, box_rows}, 128-byte swizzle.
+moe_status_t make_map(CUtensorMap* m, const void* base, bool fp4, uint64_t K, uint64_t rows, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  cuuint64_t gdim[2] = {K, rows};
+  cuuint64_t gstride[1] = {fp4 ? K / 2 : K};
+  cuuint32_t box[2] = {128u, box_rows};
+  cuuint32_t estr[2] = {1u, 1u};
+  CUresult r = fn(m, fp4 ? CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+                  const_cast<void*>(base), gdim, gstride, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return MOE_OK;
+}
+
+moe_status_t check_cfg(const moe_config_t* c) {
+  if (!c) return fail(MOE_ERR_INVALID_ARG, "config is NULL");
+  if (c->d_model <= 0 || c->d_ff <= 0 || c->d_model % 128 || c->d_ff % 128)
+    return fail(MOE_ERR_UNSUPPORTED, "d_model (%d) and d_ff (%d) must be positive multiples of 128", c->d_model,
+                c->d_ff);
+  if (c->d_model > 65536 || c->d_ff > 65536) return fail(MOE_ERR_UNSUPPORTED, "d_model / d_ff above 65536");
+  if (c->n_experts < 1 || c->n_experts > 1024)
+    return fail(MOE_ERR_UNSUPPORTED, "n_experts (%d) must be in [1, 1024]", c->n_experts);
+  if (c->top_k < 1 || c->top_k > 16 || c->top_k > c->n_experts)
+    return fail(MOE_ERR_UNSUPPORTED, "top_k (%d) must be in [1, min(16, n_experts)]", c->top_k);
+  if (!(c->route_scale == c->route_scale) || !(c->swiglu_limit > 0.f))
+    return fail(MOE_ERR_INVALID_ARG, "route_scale must be a number and swiglu_limit positive");
+  return MOE_OK;
+}
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+int max_ksplit_rows(int max_T, int E, int d) {
+  // largest ksplit * T over 1 <= T <= max_T, for the router partial sums: ksplit only changes with
+  // ceil(T / 64), so each 64-row bucket peaks at its last T
+  int best = 0;
+  for (int b = 1; (b - 1) * 64 < max_T; ++b) {
+    const int T = std::min(64 * b, max_T);
+    best = std::max(best, router_ksplit(T, E, d) * T);
+  }
+  return best;
+}
+
+struct Dims {
+  int rows;       // max rows incl. shared
+  int G;          // max groups
+  int n_chunks;
+  int max_tiles;
+};
+
+Dims dims_for(int max_T, int E, int k) {
+  Dims dm;
+  dm.rows = max_T * (k + 1);
+  dm.G = E + 1;
+  dm.n_chunks = (max_T + 31) / 32;
+  dm.max_tiles = (dm.rows + kDecodeBN - 1) / kDecodeBN + dm.G;
+  return dm;
+}
+
+}  // namespace
+
+namespace moe {
+
+size_t workspace_layout(int max_T, int d, int f, int E, int k, Workspace* ws, void* base) {
+  const Dims dm = dims_for(max_T, E, k);
+  size_t off = 0;
+  auto take = [&](size_t bytes) -> void* {
+    off = align_up(off, 256);
+    void* p = base ? static_cast<uint8_t*>(base) + off : nullptr;
+    off += bytes;
+    return p;
+  };
+  Workspace w{};
+  w.topk_ids = (int32_t*)take((size_t)max_T * k * 4);
+  w.topk_w = (float*)take((size_t)max_T * k * 4);
+  w.logits = (float*)take((size_t)max_ksplit_rows(max_T, E, d) * E * 4);
+  w.chunk_hist = (int32_t*)take((size_t)dm.n_chunks * dm.G * 4);
+  w.counts = (int32_t*)take((size_t)dm.G * 4);
+  w.offsets = (int32_t*)take((size_t)(dm.G + 1) * 4);
+  w.tile_off = (int32_t*)take((size_t)(dm.G + 1) * 4);
+  w.n_tiles = (int32_t*)take(4);
+  w.tiles = (RowTile*)take((size_t)dm.max_tiles * sizeof(RowTile));
+  w.perm_tok = (int32_t*)take((size_t)dm.rows * 4);
+  w.inv_pos = (int32_t*)take((size_t)max_T * k * 4);
+  w.row_w = (float*)take((size_t)dm.rows * 4);
+  w.a_q = (uint8_t*)take((size_t)dm.rows * d);
+  w.a_sf = (uint8_t*)take((size_t)dm.max_tiles * (d / 128) * kSfAtomBytes);
+  w.h_q = (uint8_t*)take((size_t)dm.rows * f);
+  w.h_sf = (uint8_t*)take((size_t)dm.max_tiles * (f / 128) * kSfAtomBytes);
+  w.y_rows = (__nv_bfloat16*)take((size_t)dm.rows * d * 2);
+  if (ws) *ws = w;
+  return align_up(off, 256);
+}
+
+}  // namespace moe
+
+extern "C" {
+
+const char* moe_last_error(void) { return g_last_error.c_str(); }
+
+const char* moe_status_string(moe_status_t s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported shape or device";
+    case MOE_ERR_WORKSPACE: return "workspace missing or too small";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_DEVICE_CHECK: return "device-side range check failed";
+    case MOE_ERR_TIMEOUT: return "device wait timed out";
+  }
+  return "unknown status";
+}
+
+size_t moe_workspace_size(const moe_config_t* cfg, int32_t max_T) {
+  if (check_cfg(cfg) != MOE_OK || max_T < 1) return 0;
+  return workspace_layout(max_T, cfg->d_model, cfg->d_ff, cfg->n_experts, cfg->top_k, nullptr, nullptr);
+}
+
+moe_status_t moe_experts_create(const moe_config_t* cfg, int32_t n, const uint8_t* w13_fp4, const uint8_t* w13_e8m0,
+                                const uint8_t* w2_fp4, const uint8_t* w2_e8m0, moe_stream_t stream,
+                                moe_experts_t* out) {
+  if (!out) return fail(MOE_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  moe_status_t st = check_cfg(cfg);
+  if (st != MOE_OK) return st;
+  if (n < 1 || n > 1024) return fail(MOE_ERR_INVALID_ARG, "expert count %d outside [1, 1024]", n);
+  if (!w13_fp4 || !w13_e8m0 || !w2_fp4 || !w2_e8m0) return fail(MOE_ERR_INVALID_ARG, "weight pointer is NULL");
+  if (!aligned(w13_fp4, 32) || !aligned(w2_fp4, 32))
+    return fail(MOE_ERR_INVALID_ARG, "FP4 weight buffers must be 32-byte aligned");
+  if (!aligned(w13_e8m0, 4) || !aligned(w2_e8m0, 4))
+    return fail(MOE_ERR_INVALID_ARG, "scale buffers must be 4-byte aligned");
+  int dev = 0;
+  MOE_CUDA(cudaGetDevice(&dev), "cudaGetDevice");
+  int major = 0, minor = 0, sms = 0;
+  MOE_CUDA(cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev), "cudaDeviceGetAttribute");
+  MOE_CUDA(cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev), "cudaDeviceGetAttribute");
+  MOE_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev), "cudaDeviceGetAttribute");
+  if (major != 10 || minor != 3)
+    return fail(MOE_ERR_UNSUPPORTED, "libmoe is built for sm_103a; device %d is sm_%d%d", dev, major, minor);
+  const int d = cfg->d_model, f = cfg->d_ff;
+  moe_experts_s* h = new (std::nothrow) moe_experts_s();
+  if (!h) return fail(MOE_ERR_CUDA, "host allocation failed");
+  h->cfg = *cfg;
+  h->n = n;
+  h->w13 = w13_fp4;
+  h->w2 = w2_fp4;
+  h->num_sms = sms;
+  h->device = dev;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const size_t sf13_bytes = (size_t)n * 2 * f * (d / 32), sf2_bytes = (size_t)n * d * (f / 32);
+  cudaError_t e = cudaMalloc(&h->sf13, sf13_bytes);
+  if (e == cudaSuccess) e = cudaMalloc(&h->sf2, sf2_bytes);
+  if (e == cudaSuccess) e = cudaMalloc(&h->status, sizeof(int));
+  if (e == cudaSuccess) e = cudaMemsetAsync(h->status, 0, sizeof(int), s);
+  if (e == cudaSuccess) e = launch_pack_weight_sf(w13_e8m0, n, 2 * f, d, h->sf13, s);
+  if (e == cudaSuccess) e = launch_pack_weight_sf(w2_e8m0, n, d, f, h->sf2, s);
+  if (e != cudaSuccess) {
+    moe_experts_destroy(h);
+    return cuda_fail(e, "moe_experts_create");
+  }
+  st = make_map(&h->tm13, w13_fp4, true, (uint64_t)d, (uint64_t)n * 2 * f, 128);
+  if (st == MOE_OK) st = make_map(&h->tm2, w2_fp4, true, (uint64_t)f, (uint64_t)n * d, 128);
+  if (st != MOE_OK) {
+    moe_experts_destroy(h);
+    return st;
+  }
+  *out = h;
+  return MOE_OK;
+}
+
+void moe_experts_destroy(moe_experts_t h) {
+  if (!h) return;
+  if (h->sf13) cudaFree(h->sf13);
+  if (h->sf2) cudaFree(h->sf2);
+  if (h->status) cudaFree(h->status);
+  delete h;
+}
+
+moe_status_t moe_experts_set_hash_table(moe_experts_t h, const int32_t* table, int32_t V) {
+  if (!h) return fail(MOE_ERR_INVALID_ARG, "handle is NULL");
+  if (table && V < 1) return fail(MOE_ERR_INVALID_ARG, "hash table needs V >= 1");
+  h->hash_table = table;
+  h->hash_V = table ? V : 0;
+  return MOE_OK;
+}
+
+moe_status_t moe_set_workspace(moe_experts_t h, void* ws, size_t bytes, int32_t max_T) {
+  if (!h) return fail(MOE_ERR_INVALID_ARG, "handle is NULL");
+  if (!ws || max_T < 1) return fail(MOE_ERR_INVALID_ARG, "workspace pointer NULL or max_T < 1");
+  if (!aligned(ws, 256)) return fail(MOE_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  const size_t need = workspace_layout(max_T, h->cfg.d_model, h->cfg.d_ff, h->cfg.n_experts, h->cfg.top_k, nullptr,
+                                       nullptr);
+  if (bytes < need) return fail(MOE_ERR_WORKSPACE, "workspace of %zu bytes, %zu needed for max_T %d", bytes, need, max_T);
+  workspace_layout(max_T, h->cfg.d_model, h->cfg.d_ff, h->cfg.n_experts, h->cfg.top_k, &h->ws, ws);
+  h->ws_base = ws;
+  h->ws_bytes = bytes;
+  h->ws_max_T = max_T;
+  return MOE_OK;
+}
+
+moe_status_t moe_set_wait_budget(moe_experts_t h, uint64_t budget_ns) {
+  if (!h || budget_ns == 0) return fail(MOE_ERR_INVALID_ARG, "handle NULL or zero budget");
+  h->budget_ns = budget_ns;
+  return MOE_OK;
+}
+
+static moe_status_t check_input(const moe_experts_s* h, const moe_input_t* x) {
+  if (!h) return fail(MOE_ERR_INVALID_ARG, "handle is NULL");
+  if (!x) return fail(MOE_ERR_INVALID_ARG, "input is NULL");
+  if (x->T < 0) return fail(MOE_ERR_INVALID_ARG, "T = %d is negative", x->T);
+  if (x->T > 0 && !x->x_bf16) return fail(MOE_ERR_INVALID_ARG, "x is NULL");
+  if (x->x_bf16 && !aligned(x->x_bf16, 16)) return fail(MOE_ERR_INVALID_ARG, "x must be 16-byte aligned");
+  if (!h->ws_base) return fail(MOE_ERR_WORKSPACE, "no workspace attached (moe_set_workspace)");
+  if (x->T > h->ws_max_T) return fail(MOE_ERR_WORKSPACE, "T = %d above the workspace's max_T = %d", x->T, h->ws_max_T);
+  return MOE_OK;
+}
+
+static moe_status_t route_into(moe_experts_s* h, const moe_input_t* x, const float* router_w, const float* router_bias,
+                               int32_t* ids, float* wts, cudaStream_t s) {
+  const int T = x->T, E = h->cfg.n_experts, k = h->cfg.top_k, d = h->cfg.d_model;
+  if (h->hash_table) {
+    if (router_w || router_bias) return fail(MOE_ERR_INVALID_ARG, "hash layer: router_w and router_bias must be NULL");
+    if (!x->token_ids) return fail(MOE_ERR_INVALID_ARG, "hash layer: token_ids is NULL");
+    if (T == 0) return MOE_OK;
+    MOE_CUDA(launch_hash_route(x->token_ids, h->hash_table, h->hash_V, T, E, k, h->cfg.route_scale, ids, wts, h->status,
+                               s),
+             "hash route");
+    return MOE_OK;
+  }
+  if (!router_w || !router_bias) return fail(MOE_ERR_INVALID_ARG, "router_w / router_bias is NULL");
+  if (x->token_ids) return fail(MOE_ERR_INVALID_ARG, "token_ids given but no hash table is set");
+  if (E > 512) return fail(MOE_ERR_UNSUPPORTED, "the learned router supports up to 512 experts");
+  if (!aligned(router_w, 16)) return fail(MOE_ERR_INVALID_ARG, "router_w must be 16-byte aligned");
+  if (T == 0) return MOE_OK;
+  const int ks = router_ksplit(T, E, d);
+  MOE_CUDA(launch_router_logits(static_cast<const __nv_bfloat16*>(x->x_bf16), router_w, T, d, E, ks, h->ws.logits, s),
+           "router logits");
+  MOE_CUDA(launch_router_topk(h->ws.logits, ks, router_bias, T, E, k, h->cfg.route_scale, ids, wts, s), "router top-k");
+  return MOE_OK;
+}
+
+moe_status_t moe_route(moe_experts_t h, const moe_input_t* x, const float* router_w, const float* router_bias,
+                       int32_t* topk_ids, float* topk_w, moe_stream_t stream) {
+  moe_status_t st = check_input(h, x);
+  if (st != MOE_OK) return st;
+  if (x->T > 0 && (!topk_ids || !topk_w)) return fail(MOE_ERR_INVALID_ARG, "topk_ids / topk_w is NULL");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  st = route_into(h, x, router_w, router_bias, topk_ids, topk_w, s);
+  if (st == MOE_OK) h->last_T = x->T;
+  return st;
+}
+
+moe_status_t moe_permute(moe_experts_t h, const moe_input_t* x, const int32_t* topk_ids, int32_t* counts,
+                         int32_t* offsets, int32_t* perm_tok, int32_t* inv_pos, uint8_t* a_q, uint8_t* a_s,
+                         moe_stream_t stream) {
+  moe_status_t st = check_input(h, x);
+  if (st != MOE_OK) return st;
+  if (!counts || !offsets || !perm_tok || !inv_pos) return fail(MOE_ERR_INVALID_ARG, "an output pointer is NULL");
+  if (x->T > 0 && !topk_ids) return fail(MOE_ERR_INVALID_ARG, "topk_ids is NULL");
+  if ((a_q && !aligned(a_q, 16)) || (a_s && !aligned(a_s, 4)))
+    return fail(MOE_ERR_INVALID_ARG, "a_q must be 16-byte and a_s 4-byte aligned");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int T = x->T, E = h->cfg.n_experts, k = h->cfg.top_k, d = h->cfg.d_model;
+  const Dims dm = dims_for(h->ws_max_T, E, k);
+  const int n_chunks = (T + 31) / 32;
+  if (T == 0) {
+    MOE_CUDA(cudaMemsetAsync(counts, 0, sizeof(int32_t) * E, s), "memset");
+    MOE_CUDA(cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (E + 1), s), "memset");
+    return MOE_OK;
+  }
+  MOE_CUDA(launch_histogram(topk_ids, T, k, E, E, h->ws.chunk_hist, h->status, s), "histogram");
+  MOE_CUDA(launch_scan(h->ws.chunk_hist, n_chunks, T, E, E, 0, kDecodeBN, dm.max_tiles, counts, offsets,
+                       h->ws.tile_off, h->ws.n_tiles, h->ws.tiles, h->status, s),
+           "scan");
+  uint8_t* q = a_q ? a_q : h->ws.a_q;
+  MOE_CUDA(launch_gather(static_cast<const __nv_bfloat16*>(x->x_bf16), topk_ids, nullptr, h->ws.chunk_hist, offsets,
+                         h->ws.tile_off, T, d, k, E, E, 0, kDecodeBN, q, nullptr, a_s, perm_tok, inv_pos, nullptr, s),
+           "gather");
+  return MOE_OK;
+}
+
+static moe_status_t run_ffn(moe_experts_s* h, moe_experts_s* sh, int rows, int E_groups_shared_index,
+                            const uint8_t* a_q, const uint8_t* a_sf_atoms, const float* row_w, __nv_bfloat16* y,
+                            int max_tiles, cudaStream_t s) {
+  const int d = h->cfg.d_model, f = h->cfg.d_ff;
+  CUtensorMap tm_a, tm_h;
+  moe_status_t st = make_map(&tm_a, a_q, false, (uint64_t)d, (uint64_t)rows, kDecodeBN);
+  if (st == MOE_OK) st = make_map(&tm_h, h->ws.h_q, false, (uint64_t)f, (uint64_t)rows, kDecodeBN);
+  if (st != MOE_OK) return st;
+  const moe_experts_s* shx = sh ? sh : h;
+  MOE_CUDA(launch_gemm_gate_up(h->tm13, shx->tm13, h->sf13, shx->sf13, tm_a, a_sf_atoms, h->ws.tiles, h->ws.n_tiles,
+                               max_tiles, E_groups_shared_index, d, f, h->cfg.swiglu_limit, h->ws.h_q, h->ws.h_sf,
+                               h->status, h->budget_ns, h->stall_loads, h->num_sms, s),
+           "gate-up GEMM");
+  MOE_CUDA(launch_gemm_down(h->tm2, shx->tm2, h->sf2, shx->sf2, tm_h, h->ws.h_sf, h->ws.tiles, h->ws.n_tiles, max_tiles,
+                            E_groups_shared_index, d, f, row_w, y, h->status, h->budget_ns, h->stall_loads,
+                            h->num_sms, s),
+           "down GEMM");
+  return MOE_OK;
+}
+
+moe_status_t moe_expert_ffn(moe_experts_t h, int32_t n_rows, const int32_t* offsets, const uint8_t* a_q,
+                            const uint8_t* a_s, const float* row_w, void* y_bf16, moe_stream_t stream) {
+  if (!h) return fail(MOE_ERR_INVALID_ARG, "handle is NULL");
+  if (n_rows < 0) return fail(MOE_ERR_INVALID_ARG, "n_rows is negative");
+  if (!h->ws_base) return fail(MOE_ERR_WORKSPACE, "no workspace attached (moe_set_workspace)");
+  const Dims dm = dims_for(h->ws_max_T, h->cfg.n_experts, h->cfg.top_k);
+  if (n_rows > dm.rows) return fail(MOE_ERR_WORKSPACE, "n_rows = %d above the workspace capacity %d", n_rows, dm.rows);
+  if (h->n + 1 > dm.G) return fail(MOE_ERR_WORKSPACE, "expert set larger than the workspace's group capacity");
+  if (n_rows == 0) return MOE_OK;
+  if (!a_q || !a_s || !y_bf16) return fail(MOE_ERR_INVALID_ARG, "a_q / a_s / y is NULL");
+  if (!aligned(a_q, 16) || !aligned(a_s, 4) || !aligned(y_bf16, 16))
+    return fail(MOE_ERR_INVALID_ARG, "a_q and y must be 16-byte aligned, a_s 4-byte aligned");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  MOE_CUDA(launch_tiles_from_offsets(offsets, offsets ? h->n : 1, n_rows, kDecodeBN, dm.max_tiles, h->ws.tile_off,
+                                     h->ws.n_tiles, h->ws.tiles, h->status, s),
+           "tile list");
+  MOE_CUDA(launch_rows_sf_to_atoms(a_s, h->ws.tiles, h->ws.n_tiles, h->cfg.d_model, dm.max_tiles, h->ws.a_sf, s),
+           "scale atoms");
+  return run_ffn(h, nullptr, n_rows, h->n, a_q, h->ws.a_sf, row_w, static_cast<__nv_bfloat16*>(y_bf16), dm.max_tiles,
+                 s);
+}
+
+moe_status_t moe_forward(const moe_input_t* x, const float* router_w, const float* router_bias, moe_experts_t h,
+                         moe_experts_t sh, void* out_bf16, moe_stream_t stream) {
+  moe_status_t st = check_input(h, x);
+  if (st != MOE_OK) return st;
+  if (h->n != h->cfg.n_experts) return fail(MOE_ERR_INVALID_ARG, "routed set must hold cfg.n_experts experts");
+  if (sh) {
+    if (sh->n != 1) return fail(MOE_ERR_INVALID_ARG, "shared set must hold exactly one expert");
+    if (sh->cfg.d_model != h->cfg.d_model || sh->cfg.d_ff != h->cfg.d_ff)
+      return fail(MOE_ERR_INVALID_ARG, "shared expert shape differs from the routed experts");
+  }
+  if (x->T > 0 && !out_bf16) return fail(MOE_ERR_INVALID_ARG, "out is NULL");
+  if (out_bf16 && !aligned(out_bf16, 16)) return fail(MOE_ERR_INVALID_ARG, "out must be 16-byte aligned");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int T = x->T, E = h->cfg.n_experts, k = h->cfg.top_k, d = h->cfg.d_model;
+  st = route_into(h, x, router_w, router_bias, h->ws.topk_ids, h->ws.topk_w, s);
+  if (st != MOE_OK) return st;
+  h->last_T = T;
+  if (T == 0) return MOE_OK;
+  const int has_shared = sh ? 1 : 0;
+  const int G = E + has_shared;
+  const int R = T * k;
+  const int rows = R + (has_shared ? T : 0);
+  const Dims dm = dims_for(h->ws_max_T, E, k);
+  const int n_chunks = (T + 31) / 32;
+  MOE_CUDA(launch_histogram(h->ws.topk_ids, T, k, E, G, h->ws.chunk_hist, h->status, s), "histogram");
+  MOE_CUDA(launch_scan(h->ws.chunk_hist, n_chunks, T, E, G, has_shared, kDecodeBN, dm.max_tiles, h->ws.counts,
+                       h->ws.offsets, h->ws.tile_off, h->ws.n_tiles, h->ws.tiles, h->status, s),
+           "scan");
+  MOE_CUDA(launch_gather(static_cast<const __nv_bfloat16*>(x->x_bf16), h->ws.topk_ids, h->ws.topk_w, h->ws.chunk_hist,
+                         h->ws.offsets, h->ws.tile_off, T, d, k, E, G, has_shared, kDecodeBN, h->ws.a_q, h->ws.a_sf,
+                         nullptr, h->ws.perm_tok, h->ws.inv_pos, h->ws.row_w, s),
+           "gather");
+  st = run_ffn(h, sh, rows, E, h->ws.a_q, h->ws.a_sf, h->ws.row_w, h->ws.y_rows, dm.max_tiles, s);
+  if (st != MOE_OK) return st;
+  MOE_CUDA(launch_combine(h->ws.y_rows, h->ws.inv_pos, T, d, k, R, has_shared, static_cast<__nv_bfloat16*>(out_bf16), s),
+           "combine");
+  return MOE_OK;
+}
+
+moe_status_t moe_get_routing(moe_experts_t h, const int32_t** ids, const float** w, int32_t* T) {
+  if (!h || !ids || !w || !T) return fail(MOE_ERR_INVALID_ARG, "NULL argument");
+  if (!h->ws_base) return fail(MOE_ERR_WORKSPACE, "no workspace attached");
+  *ids = h->ws.topk_ids;
+  *w = h->ws.topk_w;
+  *T = h->last_T;
+  return MOE_OK;
+}
+
+moe_status_t moe_testing_stall_loads(moe_experts_t h, int32_t enable) {
+  if (!h) return fail(MOE_ERR_INVALID_ARG, "handle is NULL");
+  h->stall_loads = enable ? 1 : 0;
+  return MOE_OK;
+}
+
+moe_status_t moe_check(moe_experts_t h, moe_stream_t stream) {
+  if (!h) return fail(MOE_ERR_INVALID_ARG, "handle is NULL");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  MOE_CUDA(cudaStreamSynchronize(s), "stream synchronize");
+  int v = 0;
+  MOE_CUDA(cudaMemcpy(&v, h->status, sizeof(int), cudaMemcpyDeviceToHost), "status read");
+  if (v == 0) return MOE_OK;
+  MOE_CUDA(cudaMemset(h->status, 0, sizeof(int)), "status clear");
+  if (v & DEV_TIMEOUT) return fail(MOE_ERR_TIMEOUT, "a device wait expired (status 0x%x)", v);
+  return fail(MOE_ERR_DEVICE_CHECK, "device range check failed (status 0x%x)", v);
+}
+
+}  // extern "C"

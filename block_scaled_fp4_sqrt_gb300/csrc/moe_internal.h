@@ -1,0 +1,114 @@
+// Internal declarations shared by the C-ABI host code and the kernel translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace moe {
+
+// Device status bits (sticky, OR-ed into the handle's status word).
+enum : int {
+  DEV_BAD_EXPERT_ID = 1,   // an expert id outside [0, E) reached the permutation
+  DEV_BAD_TOKEN_ID = 2,    // a token id outside [0, V) reached the hash router
+  DEV_TIMEOUT = 4,         // a bounded mbarrier wait ran out
+  DEV_BAD_WORK = 8,        // a work list larger than the workspace capacity
+};
+
+constexpr int kMmaM = 128;         // weight rows per MMA tile (tcgen05 M)
+constexpr int kKGroup = 128;       // K elements per pipeline stage (one 128-byte swizzle row of FP8)
+constexpr int kSfAtomBytes = 512;  // scale-factor atom: 128 rows x 4 K-blocks of 32
+constexpr int kDecodeBN = 32;      // token rows per MMA tile (tcgen05 N) in the grouped GEMMs
+
+// One row tile of the grouped GEMMs: rows [row0, row0 + nrows) of group `group`.
+struct RowTile {
+  int group;
+  int row0;
+  int nrows;
+  int pad;
+};
+
+// Geometry of one forward call, fixed on the host from (config, T).
+struct Geometry {
+  int T, d, f, E, k;
+  int G;            // groups: E routed + 1 shared (or E when there is no shared expert)
+  int R;            // routed rows T*k
+  int rows;         // R + T (shared rows follow the routed ones) or R
+  int n_chunks;     // ceil(T / 32) histogram chunks
+  int max_tiles;    // capacity of the row-tile list
+  int bn;           // rows per tile
+};
+
+// Workspace carve-up (device pointers), see moe_workspace_layout().
+struct Workspace {
+  int32_t* topk_ids;    // [T, k]
+  float* topk_w;        // [T, k]
+  float* logits;        // [ksplit, T, E] router partial sums
+  int32_t* chunk_hist;  // [n_chunks, G]
+  int32_t* counts;      // [G]
+  int32_t* offsets;     // [G + 1]
+  int32_t* tile_off;    // [G + 1] first row tile of each group
+  int32_t* n_tiles;     // [1]
+  RowTile* tiles;       // [max_tiles]
+  int32_t* perm_tok;    // [rows]
+  int32_t* inv_pos;     // [T, k]
+  float* row_w;         // [rows]
+  uint8_t* a_q;         // [rows, d]
+  uint8_t* a_sf;        // [max_tiles, d/128, 512]
+  uint8_t* h_q;         // [rows, f]
+  uint8_t* h_sf;        // [max_tiles, f/128, 512]
+  __nv_bfloat16* y_rows;  // [rows, d]
+};
+
+size_t workspace_layout(int max_T, int d, int f, int E, int k, Workspace* ws, void* base);
+
+// ------------------------------------------------------------------ launchers (return cudaError_t)
+constexpr int kRouterKSplitMax = 8;
+int router_ksplit(int T, int E, int d);
+cudaError_t launch_router_logits(const __nv_bfloat16* x, const float* w, int T, int d, int E, int ksplit,
+                                 float* partial, cudaStream_t s);
+cudaError_t launch_router_topk(const float* partial, int ksplit, const float* bias, int T, int E, int k,
+                               float route_scale, int32_t* ids, float* wts, cudaStream_t s);
+cudaError_t launch_hash_route(const int32_t* tok, const int32_t* table, int V, int T, int E, int k, float route_scale,
+                              int32_t* ids, float* wts, int* status, cudaStream_t s);
+
+cudaError_t launch_histogram(const int32_t* ids, int T, int k, int E, int G, int32_t* chunk_hist, int* status,
+                             cudaStream_t s);
+cudaError_t launch_scan(int32_t* chunk_hist, int n_chunks, int T, int E, int G, int has_shared, int bn, int max_tiles,
+                        int32_t* counts, int32_t* offsets, int32_t* tile_off, int32_t* n_tiles, RowTile* tiles,
+                        int* status, cudaStream_t s);
+// Quantise x to MXFP8 and scatter each token row to its k routed rows (+ its shared row).
+// a_sf_atoms / a_s_rows may each be null (kernel-layout scale atoms / canonical [rows, d/32]).
+cudaError_t launch_gather(const __nv_bfloat16* x, const int32_t* ids, const float* wts, const int32_t* chunk_hist,
+                          const int32_t* offsets, const int32_t* tile_off, int T, int d, int k, int E, int G,
+                          int has_shared, int bn, uint8_t* a_q, uint8_t* a_sf_atoms, uint8_t* a_s_rows,
+                          int32_t* perm_tok, int32_t* inv_pos, float* row_w, cudaStream_t s);
+// Canonical [rows, d/32] scales -> per-tile atoms (for moe_expert_ffn on caller buffers).
+cudaError_t launch_rows_sf_to_atoms(const uint8_t* a_s_rows, const RowTile* tiles, const int32_t* n_tiles, int d,
+                                    int max_tiles, uint8_t* atoms, cudaStream_t s);
+cudaError_t launch_tiles_from_offsets(const int32_t* offsets, int G, int n_rows, int bn, int max_tiles,
+                                      int32_t* tile_off, int32_t* n_tiles, RowTile* tiles, int* status,
+                                      cudaStream_t s);
+
+// Per-expert weight scale atoms: canonical [n, rows, K/32] -> [n, rows/128, K/128, 512].
+cudaError_t launch_pack_weight_sf(const uint8_t* s, int n, int rows, int K, uint8_t* atoms, cudaStream_t s_);
+
+cudaError_t launch_gemm_gate_up(const CUtensorMap& w_routed, const CUtensorMap& w_shared, const uint8_t* sf_routed,
+                                const uint8_t* sf_shared, const CUtensorMap& act, const uint8_t* act_sf,
+                                const RowTile* tiles, const int32_t* n_tiles, int max_tiles, int E, int d, int f,
+                                float limit,
+                                uint8_t* h_q, uint8_t* h_sf, int* status, uint64_t wait_budget_ns, int stall_loads,
+                                int num_sms, cudaStream_t s);
+cudaError_t launch_gemm_down(const CUtensorMap& w_routed, const CUtensorMap& w_shared, const uint8_t* sf_routed,
+                             const uint8_t* sf_shared, const CUtensorMap& act, const uint8_t* act_sf,
+                             const RowTile* tiles, const int32_t* n_tiles, int max_tiles, int E, int d, int f,
+                             const float* row_w,
+                             __nv_bfloat16* y, int* status, uint64_t wait_budget_ns, int stall_loads, int num_sms,
+                             cudaStream_t s);
+
+cudaError_t launch_combine(const __nv_bfloat16* y_rows, const int32_t* inv_pos, int T, int d, int k, int R,
+                           int has_shared, __nv_bfloat16* out, cudaStream_t s);
+
+}  // namespace moe

@@ -1,0 +1,180 @@
+/*
+ * moe.h -- C ABI of libmoe, the GB300 (sm_103a) forward pass of a DeepSeek-V4-Flash-style
+ * Mixture-of-Experts layer over a speculative-decode verify batch.
+ *
+ * The layer (DeepSeek-V4-Flash pages):
+ *   - "sqrt-softplus MoE routing with hash layers" (TensorSharp DeepSeek V4 Flash page, section
+ *     "How TensorSharp runs it"), top-k = 6 of 256 routed experts plus one always-on shared expert,
+ *     route_scale = 1.5, swiglu_limit = 10 (FaStar model card, "Speeds, Sizes, Times" and "Model
+ *     Architecture and Objective");
+ *   - expert weights in MXFP4: E2M1 values with one E8M0 scale per 32 (model card "Preprocessing";
+ *     TensorSharp page, "Getting a drafter"), gate / up / down = w1 / w3 / w2 (ds4 issue, "Loader
+ *     spec -- mtp.* tensor map");
+ *   - gate -> top-6 -> dispatch -> routed + shared expert FFNs -> combine (pypto page, "MoE and
+ *     output stages"), the weighted sum being the moe_scatter_add epilogue (TensorSharp page, "DSpark
+ *     and MoE CPU offload together").
+ * Activations enter the expert GEMMs as MXFP8 (E4M3, one E8M0 scale per 32 along the reduction
+ * dimension), as do the SwiGLU outputs before the down projection.
+ *
+ * Conventions for every call:
+ *   - All tensor pointers are DEVICE pointers unless stated otherwise; row-major; the caller owns
+ *     them.  bf16 tensors are passed as void*.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy default stream).  The
+ *     returned status covers host-side argument checks and launch errors only.  Conditions found on
+ *     the device (an out-of-range expert or token id, a bounded wait that ran out) are recorded in a
+ *     sticky per-handle status word and reported by moe_check().
+ *   - No call allocates device memory except moe_experts_create (its scale-factor copy); per-call
+ *     scratch lives in a caller-provided workspace (moe_workspace_size / moe_set_workspace).
+ *   - Shapes: d_model and d_ff multiples of 128; n_experts in [1, 1024]; top_k in [1, min(16,
+ *     n_experts)]; n_experts <= 512 for the learned router (hash routing has no such limit).
+ *   - Nothing is thread-safe per handle: calls on one handle must be ordered by the caller (one
+ *     stream, or explicit events).  Two handles may be used concurrently.
+ */
+#ifndef MOE_H_
+#define MOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* moe_stream_t; /* identical to cudaStream_t */
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1, /* null pointer, bad size, misaligned pointer, wrong mode */
+  MOE_ERR_UNSUPPORTED = 2, /* shape outside the supported set, or no sm_100-family GPU */
+  MOE_ERR_WORKSPACE = 3,   /* workspace missing or smaller than the call needs */
+  MOE_ERR_CUDA = 4,        /* a CUDA runtime / driver call failed (text in moe_last_error()) */
+  MOE_ERR_DEVICE_CHECK = 5, /* moe_check: a device-side range check failed */
+  MOE_ERR_TIMEOUT = 6      /* moe_check: a bounded device wait expired */
+} moe_status_t;
+
+typedef struct {
+  int32_t d_model;    /* hidden size d (4096 in the pages' model) */
+  int32_t d_ff;       /* expert FFN width f (2048) */
+  int32_t n_experts;  /* routed experts E (256); 1 for a shared-expert handle */
+  int32_t top_k;      /* experts per token k (6) */
+  float route_scale;  /* routed weights sum to this (1.5) */
+  float swiglu_limit; /* SwiGLU clamp L (10): h = silu(min(gate, L)) * clamp(up, -L, L) */
+} moe_config_t;
+
+typedef struct moe_experts_s* moe_experts_t;
+
+/* One batch of token rows. */
+typedef struct {
+  const void* x_bf16;       /* [T, d_model] bf16, 16-byte aligned */
+  int32_t T;                /* rows (tokens) in the batch, >= 0 */
+  const int32_t* token_ids; /* [T] token ids, hash-routed layers only (else NULL) */
+} moe_input_t;
+
+/*
+ * Create an expert set of `n` experts in the canonical MXFP4 layout:
+ *   w13_fp4 [n, 2*d_ff, d_model/2]  gate rows 0..d_ff-1 (w1) then up rows d_ff..2*d_ff-1 (w3); element
+ *                                    2i of a row is the low nibble of byte i; E2M1 code = sign bit 3,
+ *                                    exponent bits 2..1, mantissa bit 0;
+ *   w13_e8m0 [n, 2*d_ff, d_model/32] one E8M0 scale byte (2^(b-127)) per 32 consecutive elements;
+ *   w2_fp4  [n, d_model, d_ff/2], w2_e8m0 [n, d_model, d_ff/32]  the down projection (w2).
+ * The FP4 code buffers are BORROWED: they must stay alive and unchanged until
+ * moe_experts_destroy (the kernels stream them directly; 32-byte alignment required).  The scale
+ * bytes are copied into a handle-owned, kernel-ordered buffer (enqueued on `stream`; the scale
+ * inputs may be released once `stream` has passed this call).  A routed set uses
+ * n = cfg->n_experts; a shared expert is a set with n = 1.
+ * Errors: MOE_ERR_INVALID_ARG (null / misaligned / n < 1), MOE_ERR_UNSUPPORTED (shape or GPU),
+ * MOE_ERR_CUDA.  *out is NULL on error.
+ */
+MOE_API moe_status_t moe_experts_create(const moe_config_t* cfg, int32_t n, const uint8_t* w13_fp4, const uint8_t* w13_e8m0,
+                                const uint8_t* w2_fp4, const uint8_t* w2_e8m0, moe_stream_t stream,
+                                moe_experts_t* out);
+
+/*
+ * Turn a routed set into a hash-routed layer: table [V, top_k] int32 (device, borrowed) maps a
+ * token id to its experts ("hash routing over the first 3 layers", model card "Speeds, Sizes,
+ * Times"; the .fst.tid2eid sidecar).  Routing weights are route_scale / top_k.  Pass table = NULL to
+ * return to learned routing.  Token ids outside [0, V) or table entries outside [0, n_experts) are
+ * reported by moe_check (MOE_ERR_DEVICE_CHECK) and replaced by valid ids.
+ */
+MOE_API moe_status_t moe_experts_set_hash_table(moe_experts_t experts, const int32_t* table, int32_t V);
+
+/* Bytes of workspace a routed set needs for batches of up to max_T rows (with a shared expert). */
+MOE_API size_t moe_workspace_size(const moe_config_t* cfg, int32_t max_T);
+
+/* Attach caller-owned device workspace (256-byte aligned) sized for up to max_T rows. */
+MOE_API moe_status_t moe_set_workspace(moe_experts_t experts, void* workspace, size_t bytes, int32_t max_T);
+
+/*
+ * Router.  Learned: logits l = x . router_w^T in fp32 (router_w fp32 [E, d_model]), score
+ * s = sqrt(softplus(l)), the top_k experts by s + router_bias (fp32 [E]; ties to the lower id),
+ * weights route_scale * s_j / sum of the selected s (the bias steers selection only).
+ * Hash layer (a table is set): router_w and router_bias must be NULL, x->token_ids non-NULL.
+ * Outputs: topk_ids int32 [T, top_k] ascending per row, topk_w fp32 [T, top_k].
+ * Uses the workspace.  Errors: MOE_ERR_INVALID_ARG, MOE_ERR_WORKSPACE, MOE_ERR_CUDA.
+ */
+MOE_API moe_status_t moe_route(moe_experts_t experts, const moe_input_t* x, const float* router_w, const float* router_bias,
+                       int32_t* topk_ids, float* topk_w, moe_stream_t stream);
+
+/*
+ * Token -> expert permutation and MXFP8 activation quantisation (the dispatch step).
+ * Inputs: x, topk_ids [T, top_k] (each row's ids distinct).  Outputs (R = T * top_k):
+ *   counts [E]       rows per expert;      offsets [E+1]  exclusive prefix sums (offsets[E] = R);
+ *   perm_tok [R]     token of each row, rows expert-major with tokens ascending inside an expert;
+ *   inv_pos [T, top_k]  row of (t, topk_ids[t, j]);
+ *   a_q [R, d_model] E4M3 codes of x[perm_tok[r]] (round-to-nearest-even, saturating at +-448),
+ *   a_s [R, d_model/32] E8M0 bytes, exponent floor(log2(amax of the 32-block)) - 8 (0 for a zero block).
+ * a_q / a_s may be NULL (not written).  Uses the workspace.  Ids outside [0, E) are reported by
+ * moe_check and treated as expert 0.
+ */
+MOE_API moe_status_t moe_permute(moe_experts_t experts, const moe_input_t* x, const int32_t* topk_ids, int32_t* counts,
+                         int32_t* offsets, int32_t* perm_tok, int32_t* inv_pos, uint8_t* a_q, uint8_t* a_s,
+                         moe_stream_t stream);
+
+/*
+ * Grouped expert FFN over n_rows MXFP8 rows a_q [n_rows, d_model] / a_s [n_rows, d_model/32]
+ * (the layout moe_permute writes): row r belongs to expert g when offsets[g] <= r < offsets[g+1]
+ * (offsets int32 [n+1] of the handle's n experts, offsets[0] = 0, offsets[n] = n_rows; NULL = every
+ * row uses expert 0).  y[r] = row_w[r] * W2_g . q8(silu(min(W1_g a_r, L)) * clamp(W3_g a_r, -L, L)),
+ * with q8 the MXFP8 quantisation along d_ff; row_w fp32 [n_rows] or NULL (= 1); y bf16
+ * [n_rows, d_model].  Uses the workspace of the handle (n_rows <= max_T * (top_k + 1)).
+ */
+MOE_API moe_status_t moe_expert_ffn(moe_experts_t experts, int32_t n_rows, const int32_t* offsets, const uint8_t* a_q,
+                            const uint8_t* a_s, const float* row_w, void* y_bf16, moe_stream_t stream);
+
+/*
+ * The whole layer: out[t] = sum_j w_tj * FFN_{e_tj}(x_t) + FFN_shared(x_t), bf16 [T, d_model]
+ * (fp32 sums, one rounding to bf16).  `shared` may be NULL (no shared expert).  Routing as in
+ * moe_route (hash layers: router_w = router_bias = NULL).  The routing of the last call stays in
+ * the workspace (moe_get_routing).  Everything stays on the device: the call never waits for the
+ * GPU and copies nothing to or from the host.
+ */
+MOE_API moe_status_t moe_forward(const moe_input_t* x, const float* router_w, const float* router_bias,
+                         moe_experts_t experts, moe_experts_t shared, void* out_bf16, moe_stream_t stream);
+
+/* Device pointers to the routing of the last moe_route / moe_forward on this handle (valid until
+ * the next call): ids int32 [T, top_k], weights fp32 [T, top_k]. */
+MOE_API moe_status_t moe_get_routing(moe_experts_t experts, const int32_t** topk_ids, const float** topk_w, int32_t* T);
+
+/* Synchronise `stream`, then return and clear the handle's sticky device status:
+ * MOE_OK, MOE_ERR_DEVICE_CHECK (range check) or MOE_ERR_TIMEOUT (bounded wait expired). */
+MOE_API moe_status_t moe_check(moe_experts_t experts, moe_stream_t stream);
+
+/* Upper bound, in nanoseconds, of every device-side wait (default 2 s). */
+MOE_API moe_status_t moe_set_wait_budget(moe_experts_t experts, uint64_t budget_ns);
+
+MOE_API void moe_experts_destroy(moe_experts_t experts);
+MOE_API const char* moe_status_string(moe_status_t status);
+/* Text of the last host-side error on this thread ("" if none). */
+MOE_API const char* moe_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H_ */

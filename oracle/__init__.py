@@ -263,11 +263,16 @@ def route_inputs(inp: "synth.LayerInputs"):
 
 
 def margin_filtered_layer(wl: "synth.Workload", seed: int = 0, threshold: float = MARGIN_MIN,
-                          with_shared: bool = True):
+                          with_shared: bool = True, adjust=None, x_scale: float = 1.0):
     """Generate a layer and redraw (per row, up to 255 times) every x row whose top-k selection gap is
     below ``threshold``, so that the selection does not depend on the precision it is computed in.
-    Returns (inputs, ids, wts, margin)."""
+    ``adjust(inputs)`` may edit the generated inputs (e.g. the router bias) before routing; x rows are
+    drawn with standard deviation ``x_scale``.  Returns (inputs, ids, wts, margin)."""
     inp = synth.gen_layer(wl, seed, with_shared=with_shared)
+    if x_scale != 1.0:
+        inp.x = synth.gen_x(seed, wl.T, wl.d, scale=x_scale)
+    if adjust is not None:
+        adjust(inp)
     ids, wts, margin = route_inputs(inp)
     if wl.hashed:
         return inp, ids, wts, margin
@@ -277,7 +282,7 @@ def margin_filtered_layer(wl: "synth.Workload", seed: int = 0, threshold: float 
         if low.size == 0:
             break
         attempts[low] += 1
-        xs = synth.gen_x(seed, wl.T, wl.d, attempts)
+        xs = synth.gen_x(seed, wl.T, wl.d, attempts, scale=x_scale)
         inp.x[low] = xs[low]
         ids_l, wts_l, m_l = route(inp.x[low], inp.router_w, inp.router_bias, wl.k, wl.route_scale)
         ids[low], wts[low], margin[low] = ids_l, wts_l, m_l

@@ -1,0 +1,65 @@
+"""Shared set-up of the GPU parity tests: seeded, margin-filtered layers on the device next to the
+oracle's routing, and the parity tolerances."""
+from __future__ import annotations
+
+import functools
+
+import numpy as np
+import torch
+
+import oracle
+import synth
+
+# Layer output (floating point), from the layer's contract: max |y - y_ref| <= 2e-2 rms(y_ref) and
+# sum |y - y_ref| / sum |y_ref| <= 5e-3.
+TOL_MAX_RMS = 2e-2
+TOL_MEAN_REL = 5e-3
+# Routing weights: fp32 logits are dot products of length d; their error is a few units of
+# 2^-24 * sqrt(d) * sum_i |x_i w_i| (~1e-5 of the score for d = 4096), so 1e-4 relative bounds the
+# weights with margin.
+TOL_WEIGHT_REL = 1e-4
+
+# A mid-size layer that the oracle evaluates in seconds but that still spans several output tiles
+# (f/128 = 4 gate-up, d/128 = 8 down), several K stages per tile, more work items than SMs and
+# expert groups longer than one 32-row tile.
+MEDIUM = synth.Workload("medium", 512, 1024, 512, 16, 4, description="T=512, d=1024, f=512, 16 experts top-4")
+
+WORKLOADS = dict(synth.WORKLOADS, medium=MEDIUM)
+
+
+def device():
+    return torch.device("cuda:0")
+
+
+def x_to_device(x_bits: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(x_bits).view(np.int16)).to(device()).view(torch.bfloat16)
+
+
+@functools.lru_cache(maxsize=1)
+def case(name: str, T: int | None = None, seed: int = 0):
+    """(workload, inputs, oracle ids, oracle weights, device layer) for a named workload."""
+    from block_scaled_fp4_sqrt_gb300 import MoELayer
+    wl = WORKLOADS[name]
+    if T is not None:
+        wl = wl.with_T(T)
+    inp, ids, wts, _ = oracle.margin_filtered_layer(wl, seed)
+    layer = MoELayer.from_host(inp, device=device(), max_T=max(wl.T, 1))
+    return wl, inp, ids, wts, layer
+
+
+def compare_outputs(y: np.ndarray, y_ref: np.ndarray):
+    rms = float(np.sqrt(np.mean(y_ref ** 2)))
+    max_err = float(np.max(np.abs(y - y_ref))) if y.size else 0.0
+    mean_rel = float(np.sum(np.abs(y - y_ref)) / max(np.sum(np.abs(y_ref)), 1e-300)) if y.size else 0.0
+    return max_err, rms, mean_rel
+
+
+def assert_close(y: np.ndarray, y_ref: np.ndarray, what: str = "output"):
+    max_err, rms, mean_rel = compare_outputs(y, y_ref)
+    assert max_err <= TOL_MAX_RMS * rms, f"{what}: max |dy| {max_err:.4e} > {TOL_MAX_RMS} rms ({rms:.4e})"
+    assert mean_rel <= TOL_MEAN_REL, f"{what}: mean relative error {mean_rel:.4e} > {TOL_MEAN_REL}"
+    return max_err / max(rms, 1e-300), mean_rel
+
+
+def bf16_to_f64(t: torch.Tensor) -> np.ndarray:
+    return t.float().cpu().numpy().astype(np.float64)
