@@ -1,0 +1,388 @@
+#!/usr/bin/env python3
+"""Benchmark of the MoE-layer forward on GB300: tokens/s at a verify batch, with the roofline of the
+dominant kernel, an end-to-end leg through host buffers, and the fp64 oracle timed on the host cores.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload verify512] [--impl ours|reference]
+
+One step = one moe_forward (route -> dispatch -> gate-up GEMM -> down GEMM -> combine) over one batch of
+synthetic token rows; the expert weights (3.44 GB for verify512) are resident in HBM and larger than L2,
+so no flush is needed between steps.  Under torchrun every rank runs its own replica on its own batch
+(weak scaling, no data-path collective); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE layer tokens/sec at T=512 verify; achieved HBM GB/s / tensor-pipe %"
+
+
+def parse_args():
+    p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=30)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--workload", default="verify512")
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--seed", type=int, default=0)
+    p.add_argument("--cpu-seconds", type=float, default=10.0, help="target CPU time of the oracle baseline sample")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+def dist_env():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")), int(os.environ.get("WORLD_SIZE", "1"))
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            m = json.load(fh)
+        return {"hbm_gbs": m["hbm_gbs"], "bf16_tflops": m["bf16_tflops"],
+                "bf16_tflops_sustained": m.get("bf16_tflops_sustained", m["bf16_tflops"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def expert_bytes(wl):
+    """MXFP4 bytes of one expert: gate + up + down codes (0.5 B each) plus one E8M0 byte per 32."""
+    n = 3 * wl.d * wl.f
+    return n // 2 + n // 32
+
+
+def stage_bytes(wl, touched, rows):
+    """Algorithmic HBM bytes per launch of each stage (touched = experts read, including the shared one)."""
+    d, f, T, k, E = wl.d, wl.f, wl.T, wl.k, wl.E
+    gate_up_w = 2 * f * d // 2 + 2 * f * d // 32
+    down_w = d * f // 2 + d * f // 32
+    router = (0 if wl.hashed else E * d * 4 + E * 4) + T * d * 2 + T * k * 8
+    return {
+        "route": router,
+        "dispatch": T * d * 2 + rows * (d + d // 32),
+        "gemm_gate_up": touched * gate_up_w + rows * (d + d // 32) + rows * (f + f // 32),
+        "gemm_down": touched * down_w + rows * (f + f // 32) + rows * d * 4,
+        "combine": rows * d * 4 + T * d * 2,
+    }
+
+
+def layer_bytes(wl, touched):
+    b = touched * expert_bytes(wl) + 2 * wl.T * wl.d * 2
+    if wl.hashed:
+        b += wl.T * 4 + wl.T * wl.k * 4
+    else:
+        b += wl.E * wl.d * 4 + wl.E * 4
+    return b
+
+
+def gemm_flops(wl, rows):
+    return {"gemm_gate_up": 2 * rows * 2 * wl.f * wl.d, "gemm_down": 2 * rows * wl.d * wl.f}
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.fh,
+                                         stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as fh:
+            for line in fh:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for name, val in zip(names, parts[5:9]):
+                    if val.lower().startswith("active"):
+                        reasons.add(name)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def kernel_source_digest():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "block_scaled_fp4_sqrt_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as fh:
+            h.update(name.encode())
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu capture, only if the kernels have not changed since."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as fh:
+        rec = json.load(fh)
+    if rec.get("kernel_source_digest") != kernel_source_digest():
+        return None
+    return rec.get("per_launch_bytes", {}).get(workload, {}).get(kernel)
+
+
+def oracle_tokens_per_s(inp, wl, n_tokens: int, seed: int):
+    """Time the fp64 oracle (routing + layer) on n_tokens sampled token rows."""
+    import numpy as np
+
+    import oracle
+    rng = np.random.default_rng(seed)
+    toks = np.sort(rng.choice(wl.T, size=min(n_tokens, wl.T), replace=False)).astype(np.int32)
+    t0 = time.perf_counter()
+    if wl.hashed:
+        ids, wts = oracle.hash_route(inp.token_ids[toks], inp.hash_table, wl.k, wl.route_scale)
+    else:
+        ids, wts, _ = oracle.route(inp.x[toks], inp.router_w, inp.router_bias, wl.k, wl.route_scale)
+    oracle.layer(inp.x[toks], ids, wts, inp.experts, inp.shared, wl.swiglu_limit)
+    dt = time.perf_counter() - t0
+    return len(toks), dt
+
+
+def cpu_baseline(inp, wl, target_s: float, seed: int):
+    import oracle
+    n0 = 4
+    _, t0 = oracle_tokens_per_s(inp, wl, n0, seed)
+    n = int(max(n0, min(wl.T, round(target_s / max(t0 / n0, 1e-9)))))
+    n, dt = oracle_tokens_per_s(inp, wl, n, seed + 1)
+    return {"value": n / dt, "unit": "tokens/s", "cores": oracle.threads(), "kind": "oracle",
+            "sample": f"{n} of the {wl.T} token rows of {wl.name} (routing + all expert rows + combine), fp64, {dt:.1f} s"}
+
+
+def run_reference(args, wl):
+    """Reference arm: the fp64 oracle as it stands, on the host cores, same workload and metric."""
+    import synth
+    rank, _, world = dist_env()
+    if rank != 0:
+        return
+    inp = synth.gen_layer(wl, args.seed)
+    import oracle
+    per_step = max(1, min(wl.T, 4 if wl.d >= 4096 else 16))
+    for i in range(args.warmup):
+        oracle_tokens_per_s(inp, wl, per_step, 1000 + i)
+    total_tok, total_s = 0, 0.0
+    for i in range(args.steps):
+        n, dt = oracle_tokens_per_s(inp, wl, per_step, 2000 + i)
+        total_tok += n
+        total_s += dt
+    value = total_tok / total_s
+    cores = oracle.threads()
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": workload_config(wl),
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": f"{per_step} token rows of {wl.name} per step"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(wl):
+    return {"workload": wl.name, "T": wl.T, "d_model": wl.d, "d_ff": wl.f, "routed_experts": wl.E, "top_k": wl.k,
+            "shared_experts": 1, "routing": "hash table" if wl.hashed else "sqrt-softplus",
+            "weights": "MXFP4 (E2M1 + E8M0/32), resident in HBM",
+            "l2": "no flush: expert weights read per step exceed the 129 MB L2"}
+
+
+def run_ours(args, wl):
+    import numpy as np
+    import torch
+
+    import __graft_entry__ as g
+    import synth
+
+    rank, local_rank, world = dist_env()
+    g.build()
+    import block_scaled_fp4_sqrt_gb300 as moe
+
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+
+    inp = synth.gen_layer(wl, args.seed)
+    if world > 1:  # each replica gets its own batch of token rows
+        inp.x = synth.gen_x(args.seed + 7919 * rank, wl.T, wl.d)
+    layer = moe.MoELayer.from_host(inp, device=dev, max_T=wl.T)
+    x = torch.from_numpy(inp.x.view(np.int16)).to(dev).view(torch.bfloat16)
+    out = torch.empty((wl.T, wl.d), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        layer.forward(x, out=out)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    layer.check()
+    ids, _ = layer.last_routing()
+    touched = int(torch.unique(ids).numel()) + 1  # + shared expert
+    rows = wl.T * wl.k + wl.T
+
+    # ---- device-timed steps, with per-stage events on the launching stream
+    n_ev = moe.MOE_N_STAGES + 1
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(args.steps)]
+    cvd = [v for v in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if v.strip()]
+    clocks = ClockSampler(cvd[local_rank] if local_rank < len(cvd) else local_rank)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    t_begin = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    keep = []
+    t_begin.record(stream)
+    for i in range(args.steps):
+        keep.append(moe.moe_set_stage_events(layer.h, events[i]))
+        step()
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    moe.moe_set_stage_events(layer.h, None)
+    layer.check()
+    ms = t_begin.elapsed_time(t_end) / args.steps
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    stage_ms = {name: statistics.mean(ev[i].elapsed_time(ev[i + 1]) for ev in events)
+                for i, name in enumerate(moe.STAGE_NAMES)}
+
+    # ---- end to end: pinned host x in, bf16 out back to the host, every step
+    x_host = torch.from_numpy(inp.x.view(np.int16)).view(torch.bfloat16).pin_memory()
+    out_host = torch.empty((wl.T, wl.d), dtype=torch.bfloat16).pin_memory()
+    x_e2e = torch.empty_like(x)
+    tok_dev = layer.token_ids
+    tok_host = None if tok_dev is None else tok_dev.cpu().pin_memory()
+
+    def e2e_step():
+        x_e2e.copy_(x_host, non_blocking=True)
+        if tok_host is not None:
+            tok_dev.copy_(tok_host, non_blocking=True)
+        layer.forward(x_e2e, out=out)
+        out_host.copy_(out, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms_e2e = e0.elapsed_time(e1) / args.steps
+    if world > 1:
+        t = torch.tensor([ms_e2e], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_e2e = float(t.item())
+
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+
+    pk = peaks()
+    dom = max(stage_ms, key=stage_ms.get)
+    sb = stage_bytes(wl, touched, rows)
+    fl = gemm_flops(wl, rows)
+    # verify shapes stream the expert weights (HBM bound); with >= 64 rows per expert (the prefill
+    # chunk) the grouped GEMMs are dense block-scaled contractions (tensor bound)
+    compute_bound = dom in fl and wl.T * wl.k / wl.E >= 64
+    if compute_bound:
+        achieved = fl[dom] / (stage_ms[dom] * 1e-3) / 1e12
+        peak = 2 * pk["bf16_tflops_sustained"]  # FP8-class block-scaled MMA: nominal 2x the bf16 rate
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                "traffic": measured_traffic(dom, wl.name), "kernel": dom,
+                "peak_source": f"{pk['source']} bf16 sustained x 2 (nominal FP8/BF16 ratio)",
+                "algorithmic_flops_per_launch": fl[dom]}
+    else:
+        achieved = sb[dom] / (stage_ms[dom] * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / pk["hbm_gbs"], "traffic": measured_traffic(dom, wl.name), "kernel": dom,
+                "peak_source": f"{pk['source']} HBM copy bandwidth", "algorithmic_bytes_per_launch": sb[dom]}
+    lb = layer_bytes(wl, touched)
+    kernels_per_step = (1 if wl.hashed else 2) + 3 + 2 + 1
+    line = {
+        "metric": METRIC, "value": world * wl.T / (ms * 1e-3), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "mxfp4 x mxfp8 -> f32", "data": "synthetic",
+        "config": dict(workload_config(wl), touched_experts=touched, parallelism=f"replicas x{world}"),
+        "roofline": roof,
+        "layer_roofline": {"bound": "hbm", "algorithmic_bytes": lb, "achieved": lb / (ms * 1e-3) / 1e9,
+                           "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": lb / (ms * 1e-3) / 1e9 / pk["hbm_gbs"]},
+        "stage_ms": stage_ms,
+        "e2e": {"value": world * wl.T / (ms_e2e * 1e-3), "unit": "tokens/s",
+                "h2d_bytes_per_step": wl.T * wl.d * 2 + (wl.T * 4 if wl.hashed else 0),
+                "d2h_bytes_per_step": wl.T * wl.d * 2},
+        "gpu_launches": kernels_per_step * args.steps,
+        "clocks": clk,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(inp, wl, args.cpu_seconds, args.seed)
+    layer.close()
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def main():
+    args = parse_args()
+    import synth
+    if args.workload not in synth.WORKLOADS:
+        raise SystemExit(f"unknown workload {args.workload}; choose from {sorted(synth.WORKLOADS)}")
+    wl = synth.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        import __graft_entry__ as g
+        g.build_cpu()
+        run_reference(args, wl)
+    else:
+        run_ours(args, wl)
+
+
+if __name__ == "__main__":
+    main()

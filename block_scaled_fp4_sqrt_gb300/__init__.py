@@ -25,7 +25,10 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
 EXPORTED = ("moe_experts_create", "moe_experts_set_hash_table", "moe_workspace_size", "moe_set_workspace",
             "moe_route", "moe_permute", "moe_expert_ffn", "moe_forward", "moe_get_routing", "moe_check",
             "moe_set_wait_budget", "moe_experts_destroy", "moe_status_string", "moe_last_error",
-            "moe_testing_stall_loads")
+            "moe_testing_stall_loads", "moe_set_stage_events")
+
+MOE_N_STAGES = 5
+STAGE_NAMES = ("route", "dispatch", "gemm_gate_up", "gemm_down", "combine")
 
 
 class MoEError(RuntimeError):
@@ -65,6 +68,7 @@ def lib() -> ctypes.CDLL:
         L.moe_check.argtypes = [vp, vp]
         L.moe_set_wait_budget.argtypes = [vp, u64]
         L.moe_testing_stall_loads.argtypes = [vp, i32]
+        L.moe_set_stage_events.argtypes = [vp, ctypes.POINTER(vp), i32]
         L.moe_experts_destroy.argtypes = [vp]
         L.moe_experts_destroy.restype = None
         L.moe_status_string.argtypes = [st]
@@ -163,6 +167,17 @@ def moe_testing_stall_loads(h, enable: bool) -> None:
     _ok("moe_testing_stall_loads", lib().moe_testing_stall_loads(h, 1 if enable else 0))
 
 
+def moe_set_stage_events(h, events) -> object:
+    """events: MOE_N_STAGES + 1 torch.cuda.Event(enable_timing=True) (or None to stop).  Returns the
+    ctypes array the library reads; keep it alive while recording."""
+    if events is None:
+        _ok("moe_set_stage_events", lib().moe_set_stage_events(h, None, 0))
+        return None
+    arr = (ctypes.c_void_p * len(events))(*[ctypes.c_void_p(e.cuda_event) for e in events])
+    _ok("moe_set_stage_events", lib().moe_set_stage_events(h, arr, len(events)))
+    return arr
+
+
 def moe_experts_destroy(h) -> None:
     if h:
         lib().moe_experts_destroy(h)
@@ -172,7 +187,7 @@ class _DeviceView:
     """__cuda_array_interface__ over library-owned device memory (read through torch.as_tensor)."""
 
     def __init__(self, ptr: int, shape, typestr: str, owner):
-        self.__cuda_array_interface__ = {"data": (ptr, True), "shape": tuple(shape), "typestr": typestr,
+        self.__cuda_array_interface__ = {"data": (ptr, False), "shape": tuple(shape), "typestr": typestr,
                                          "version": 3, "strides": None}
         self._owner = owner
 
@@ -267,8 +282,15 @@ class MoELayer:
         return out
 
     def expert_ffn(self, a_q, a_s, offsets=None, row_w=None, shared: bool = False) -> torch.Tensor:
+        h = self.h
+        if shared:
+            h = self.h_shared
+            if getattr(self, "_shared_ws", None) is None:  # the shared handle gets a workspace on first use
+                self._shared_ws = torch.empty(moe_workspace_size(self.cfg, self.max_T), dtype=torch.uint8,
+                                              device=self.device)
+                moe_set_workspace(h, self._shared_ws, self.max_T)
         y = torch.empty((a_q.shape[0], self.d), dtype=torch.bfloat16, device=self.device)
-        moe_expert_ffn(self.h_shared if shared else self.h, int(a_q.shape[0]), offsets, a_q, a_s, row_w, y)
+        moe_expert_ffn(h, int(a_q.shape[0]), offsets, a_q, a_s, row_w, y)
         return y
 
     def last_routing(self):

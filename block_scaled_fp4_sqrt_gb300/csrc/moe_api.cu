@@ -36,6 +36,7 @@ struct moe_experts_s {
   int device = 0;
   int32_t last_T = 0;
   int stall_loads = 0;
+  void* const* stage_events = nullptr;  // MOE_N_STAGES + 1 caller-owned cudaEvent_t, or null
 };
 
 namespace {
@@ -165,7 +166,7 @@ size_t workspace_layout(int max_T, int d, int f, int E, int k, Workspace* ws, vo
   w.a_sf = (uint8_t*)take((size_t)dm.max_tiles * (d / 128) * kSfAtomBytes);
   w.h_q = (uint8_t*)take((size_t)dm.rows * f);
   w.h_sf = (uint8_t*)take((size_t)dm.max_tiles * (f / 128) * kSfAtomBytes);
-  w.y_rows = (__nv_bfloat16*)take((size_t)dm.rows * d * 2);
+  w.y_rows = (float*)take((size_t)dm.rows * d * 4);
   if (ws) *ws = w;
   return align_up(off, 256);
 }
@@ -357,9 +358,13 @@ moe_status_t moe_permute(moe_experts_t h, const moe_input_t* x, const int32_t* t
   return MOE_OK;
 }
 
+static void mark_stage(const moe_experts_s* h, int i, cudaStream_t s) {
+  if (h->stage_events) cudaEventRecord(static_cast<cudaEvent_t>(h->stage_events[i]), s);
+}
+
 static moe_status_t run_ffn(moe_experts_s* h, moe_experts_s* sh, int rows, int E_groups_shared_index,
-                            const uint8_t* a_q, const uint8_t* a_sf_atoms, const float* row_w, __nv_bfloat16* y,
-                            int max_tiles, cudaStream_t s) {
+                            const uint8_t* a_q, const uint8_t* a_sf_atoms, const float* row_w, float* y_f32,
+                            __nv_bfloat16* y_bf16, int max_tiles, bool timed, cudaStream_t s) {
   const int d = h->cfg.d_model, f = h->cfg.d_ff;
   CUtensorMap tm_a, tm_h;
   moe_status_t st = make_map(&tm_a, a_q, false, (uint64_t)d, (uint64_t)rows, kDecodeBN);
@@ -370,9 +375,10 @@ static moe_status_t run_ffn(moe_experts_s* h, moe_experts_s* sh, int rows, int E
                                max_tiles, E_groups_shared_index, d, f, h->cfg.swiglu_limit, h->ws.h_q, h->ws.h_sf,
                                h->status, h->budget_ns, h->stall_loads, h->num_sms, s),
            "gate-up GEMM");
+  if (timed) mark_stage(h, 3, s);
   MOE_CUDA(launch_gemm_down(h->tm2, shx->tm2, h->sf2, shx->sf2, tm_h, h->ws.h_sf, h->ws.tiles, h->ws.n_tiles, max_tiles,
-                            E_groups_shared_index, d, f, row_w, y, h->status, h->budget_ns, h->stall_loads,
-                            h->num_sms, s),
+                            E_groups_shared_index, d, f, row_w, y_f32, y_bf16, h->status, h->budget_ns,
+                            h->stall_loads, h->num_sms, s),
            "down GEMM");
   return MOE_OK;
 }
@@ -395,8 +401,18 @@ moe_status_t moe_expert_ffn(moe_experts_t h, int32_t n_rows, const int32_t* offs
            "tile list");
   MOE_CUDA(launch_rows_sf_to_atoms(a_s, h->ws.tiles, h->ws.n_tiles, h->cfg.d_model, dm.max_tiles, h->ws.a_sf, s),
            "scale atoms");
-  return run_ffn(h, nullptr, n_rows, h->n, a_q, h->ws.a_sf, row_w, static_cast<__nv_bfloat16*>(y_bf16), dm.max_tiles,
-                 s);
+  return run_ffn(h, nullptr, n_rows, h->n, a_q, h->ws.a_sf, row_w, nullptr, static_cast<__nv_bfloat16*>(y_bf16),
+                 dm.max_tiles, false, s);
+}
+
+moe_status_t moe_set_stage_events(moe_experts_t h, void* const* events, int32_t n) {
+  if (!h) return fail(MOE_ERR_INVALID_ARG, "handle is NULL");
+  if (events && n < MOE_N_STAGES + 1) return fail(MOE_ERR_INVALID_ARG, "need %d events", MOE_N_STAGES + 1);
+  if (events)
+    for (int i = 0; i <= MOE_N_STAGES; ++i)
+      if (!events[i]) return fail(MOE_ERR_INVALID_ARG, "event %d is NULL", i);
+  h->stage_events = events;
+  return MOE_OK;
 }
 
 moe_status_t moe_forward(const moe_input_t* x, const float* router_w, const float* router_bias, moe_experts_t h,
@@ -413,10 +429,15 @@ moe_status_t moe_forward(const moe_input_t* x, const float* router_w, const floa
   if (out_bf16 && !aligned(out_bf16, 16)) return fail(MOE_ERR_INVALID_ARG, "out must be 16-byte aligned");
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const int T = x->T, E = h->cfg.n_experts, k = h->cfg.top_k, d = h->cfg.d_model;
+  mark_stage(h, 0, s);
   st = route_into(h, x, router_w, router_bias, h->ws.topk_ids, h->ws.topk_w, s);
   if (st != MOE_OK) return st;
   h->last_T = T;
-  if (T == 0) return MOE_OK;
+  mark_stage(h, 1, s);
+  if (T == 0) {
+    for (int i = 2; i <= MOE_N_STAGES; ++i) mark_stage(h, i, s);
+    return MOE_OK;
+  }
   const int has_shared = sh ? 1 : 0;
   const int G = E + has_shared;
   const int R = T * k;
@@ -431,10 +452,13 @@ moe_status_t moe_forward(const moe_input_t* x, const float* router_w, const floa
                          h->ws.offsets, h->ws.tile_off, T, d, k, E, G, has_shared, kDecodeBN, h->ws.a_q, h->ws.a_sf,
                          nullptr, h->ws.perm_tok, h->ws.inv_pos, h->ws.row_w, s),
            "gather");
-  st = run_ffn(h, sh, rows, E, h->ws.a_q, h->ws.a_sf, h->ws.row_w, h->ws.y_rows, dm.max_tiles, s);
+  mark_stage(h, 2, s);
+  st = run_ffn(h, sh, rows, E, h->ws.a_q, h->ws.a_sf, h->ws.row_w, h->ws.y_rows, nullptr, dm.max_tiles, true, s);
   if (st != MOE_OK) return st;
+  mark_stage(h, 4, s);
   MOE_CUDA(launch_combine(h->ws.y_rows, h->ws.inv_pos, T, d, k, R, has_shared, static_cast<__nv_bfloat16*>(out_bf16), s),
            "combine");
+  mark_stage(h, 5, s);
   return MOE_OK;
 }
 

@@ -290,9 +290,9 @@ __global__ void pack_weight_sf_kernel(const uint8_t* __restrict__ s, int n, int 
   }
 }
 
-// out[t, c] = bf16( sum_j Yr[inv_pos[t, j], c] + Yr[R + t, c] ), 8 columns per thread
-__global__ void combine_kernel(const __nv_bfloat16* __restrict__ y_rows, const int32_t* __restrict__ inv_pos, int T,
-                               int d, int k, int R, int has_shared, __nv_bfloat16* __restrict__ out) {
+// out[t, c] = bf16( sum_j Yr[inv_pos[t, j], c] + Yr[R + t, c] ), fp32 rows, 8 columns per thread
+__global__ void combine_kernel(const float* __restrict__ y_rows, const int32_t* __restrict__ inv_pos, int T, int d,
+                               int k, int R, int has_shared, __nv_bfloat16* __restrict__ out) {
   const int vec_per_row = d / 8;
   const size_t total = (size_t)T * vec_per_row;
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
@@ -300,19 +300,14 @@ __global__ void combine_kernel(const __nv_bfloat16* __restrict__ y_rows, const i
     float acc[8];
 #pragma unroll
     for (int q = 0; q < 8; ++q) acc[q] = 0.f;
-    for (int j = 0; j < k; ++j) {
-      const int r = __ldg(&inv_pos[(size_t)t * k + j]);
-      uint4 raw = __ldg(reinterpret_cast<const uint4*>(y_rows + (size_t)r * d) + c8);
-      const __nv_bfloat16* hv = reinterpret_cast<const __nv_bfloat16*>(&raw);
-#pragma unroll
-      for (int q = 0; q < 8; ++q) acc[q] += __bfloat162float(hv[q]);
-    }
-    if (has_shared) {
-      uint4 raw = __ldg(reinterpret_cast<const uint4*>(y_rows + (size_t)(R + t) * d) + c8);
-      const __nv_bfloat16* hv = reinterpret_cast<const __nv_bfloat16*>(&raw);
-#pragma unroll
-      for (int q = 0; q < 8; ++q) acc[q] += __bfloat162float(hv[q]);
-    }
+    auto add_row = [&](int r) {
+      const float4* src = reinterpret_cast<const float4*>(y_rows + (size_t)r * d) + 2 * c8;
+      const float4 a = __ldg(src), b = __ldg(src + 1);
+      acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
+      acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+    };
+    for (int j = 0; j < k; ++j) add_row(__ldg(&inv_pos[(size_t)t * k + j]));
+    if (has_shared) add_row(R + t);
     uint4 o;
     __nv_bfloat16* ov = reinterpret_cast<__nv_bfloat16*>(&o);
 #pragma unroll
@@ -374,7 +369,7 @@ cudaError_t launch_pack_weight_sf(const uint8_t* sc, int n, int rows, int K, uin
   return cudaGetLastError();
 }
 
-cudaError_t launch_combine(const __nv_bfloat16* y_rows, const int32_t* inv_pos, int T, int d, int k, int R,
+cudaError_t launch_combine(const float* y_rows, const int32_t* inv_pos, int T, int d, int k, int R,
                            int has_shared, __nv_bfloat16* out, cudaStream_t s) {
   const size_t total = (size_t)T * (d / 8);
   int blocks = (int)((total + 255) / 256);

@@ -5,8 +5,9 @@
 //    clamp(U, -L, L) (Ops.SiLUMulClamp, swiglu_limit = 10), re-quantised to MXFP8 along the FFN
 //    dimension ("expert FFN (fused dequant + GEMM)", FaStar README "Features"; TensorSharp page
 //    "How TensorSharp runs it").
-//  * down:     Y = w_row * (H . W2^T), stored bf16 per permuted row, summed by the combine kernel
-//    (the weighted-sum epilogue moe_scatter_add of the TensorSharp page, "DSpark and MoE CPU offload").
+//  * down:     Y = w_row * (H . W2^T) per permuted row, fp32 (summed by the combine kernel, the
+//    weighted-sum epilogue moe_scatter_add of the TensorSharp page, "DSpark and MoE CPU offload") or
+//    bf16 (the standalone grouped FFN call).
 //
 // Tile shape ("swap-AB"): the 128 weight rows of one output tile are the MMA's M side, the token
 // rows of one expert group (up to 32) are its N side, so a verify batch with ~12 rows per expert
@@ -62,9 +63,10 @@ struct GemmArgs {
   uint8_t* h_q;
   uint8_t* h_sf;
   int f;
-  // down epilogue
+  // down epilogue: exactly one of y_f32 / y_bf16 is set
   const float* row_w;
-  __nv_bfloat16* y;
+  float* y_f32;
+  __nv_bfloat16* y_bf16;
   int d;
   int* status;
   uint64_t budget_ns;
@@ -283,7 +285,10 @@ __global__ void __launch_bounds__(192, 1)
           if (n < rt.nrows) {
             const int r = rt.row0 + n;
             const float wr = a.row_w ? __ldg(&a.row_w[r]) : 1.0f;
-            a.y[(size_t)r * a.d + dcol] = __float2bfloat16_rn(g[n] * wr);
+            if (a.y_f32)
+              a.y_f32[(size_t)r * a.d + dcol] = g[n] * wr;
+            else
+              a.y_bf16[(size_t)r * a.d + dcol] = __float2bfloat16_rn(g[n] * wr);
           }
         }
       }
@@ -347,8 +352,8 @@ cudaError_t launch_gemm_gate_up(const CUtensorMap& w_routed, const CUtensorMap& 
 cudaError_t launch_gemm_down(const CUtensorMap& w_routed, const CUtensorMap& w_shared, const uint8_t* sf_routed,
                              const uint8_t* sf_shared, const CUtensorMap& act, const uint8_t* act_sf,
                              const RowTile* tiles, const int32_t* n_tiles, int max_tiles, int E, int d, int f,
-                             const float* row_w, __nv_bfloat16* y, int* status, uint64_t wait_budget_ns,
-                             int stall_loads, int num_sms, cudaStream_t s) {
+                             const float* row_w, float* y_f32, __nv_bfloat16* y_bf16, int* status,
+                             uint64_t wait_budget_ns, int stall_loads, int num_sms, cudaStream_t s) {
   GemmArgs a{};
   a.sf_routed = sf_routed;
   a.sf_shared = sf_shared ? sf_shared : sf_routed;
@@ -363,7 +368,8 @@ cudaError_t launch_gemm_down(const CUtensorMap& w_routed, const CUtensorMap& w_s
   a.up_row_offset = 0;
   a.w_mblocks = d / kMmaM;
   a.row_w = row_w;
-  a.y = y;
+  a.y_f32 = y_f32;
+  a.y_bf16 = y_bf16;
   a.d = d;
   a.status = status;
   a.budget_ns = wait_budget_ns;

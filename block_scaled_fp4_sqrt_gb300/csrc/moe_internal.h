@@ -59,7 +59,7 @@ struct Workspace {
   uint8_t* a_sf;        // [max_tiles, d/128, 512]
   uint8_t* h_q;         // [rows, f]
   uint8_t* h_sf;        // [max_tiles, f/128, 512]
-  __nv_bfloat16* y_rows;  // [rows, d]
+  float* y_rows;         // [rows, d] weighted expert outputs (fp32)
 };
 
 size_t workspace_layout(int max_T, int d, int f, int E, int k, Workspace* ws, void* base);
@@ -104,11 +104,10 @@ cudaError_t launch_gemm_gate_up(const CUtensorMap& w_routed, const CUtensorMap& 
 cudaError_t launch_gemm_down(const CUtensorMap& w_routed, const CUtensorMap& w_shared, const uint8_t* sf_routed,
                              const uint8_t* sf_shared, const CUtensorMap& act, const uint8_t* act_sf,
                              const RowTile* tiles, const int32_t* n_tiles, int max_tiles, int E, int d, int f,
-                             const float* row_w,
-                             __nv_bfloat16* y, int* status, uint64_t wait_budget_ns, int stall_loads, int num_sms,
-                             cudaStream_t s);
+                             const float* row_w, float* y_f32, __nv_bfloat16* y_bf16, int* status,
+                             uint64_t wait_budget_ns, int stall_loads, int num_sms, cudaStream_t s);
 
-cudaError_t launch_combine(const __nv_bfloat16* y_rows, const int32_t* inv_pos, int T, int d, int k, int R,
+cudaError_t launch_combine(const float* y_rows, const int32_t* inv_pos, int T, int d, int k, int R,
                            int has_shared, __nv_bfloat16* out, cudaStream_t s);
 
 }  // namespace moe

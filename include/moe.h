@@ -161,6 +161,17 @@ MOE_API moe_status_t moe_forward(const moe_input_t* x, const float* router_w, co
  * the next call): ids int32 [T, top_k], weights fp32 [T, top_k]. */
 MOE_API moe_status_t moe_get_routing(moe_experts_t experts, const int32_t** topk_ids, const float** topk_w, int32_t* T);
 
+/*
+ * Stage timing (the per-stage timing the TensorSharp page exposes as TS_DSV4_PERF = 2).  events holds
+ * n >= MOE_N_STAGES + 1 cudaEvent_t handles created by the caller; every later moe_forward on this
+ * handle records events[i] on its stream before stage i and events[MOE_N_STAGES] after the last one.
+ * Stages: 0 route, 1 dispatch (histogram, scan, quantise + gather), 2 gate-up GEMM, 3 down GEMM,
+ * 4 combine.  The handle keeps the pointer array (not a copy) until it is replaced; events = NULL
+ * switches the recording off.
+ */
+#define MOE_N_STAGES 5
+MOE_API moe_status_t moe_set_stage_events(moe_experts_t experts, void* const* events, int32_t n);
+
 /* Synchronise `stream`, then return and clear the handle's sticky device status:
  * MOE_OK, MOE_ERR_DEVICE_CHECK (range check) or MOE_ERR_TIMEOUT (bounded wait expired). */
 MOE_API moe_status_t moe_check(moe_experts_t experts, moe_stream_t stream);
