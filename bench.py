@@ -37,6 +37,9 @@ def parse_args():
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--cpu-seconds", type=float, default=10.0, help="target CPU time of the oracle baseline sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--experts", type=int, default=0,
+                   help="override the routed-expert count (small cases for profiling; not a benchmark line)")
+    p.add_argument("--tokens", type=int, default=0, help="override T (small cases for profiling)")
     return p.parse_args()
 
 
@@ -263,6 +266,9 @@ def run_ours(args, wl):
     # ---- device-timed steps, with per-stage events on the launching stream
     n_ev = moe.MOE_N_STAGES + 1
     events = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(args.steps)]
+    for ev in events:  # create the events before the timed region
+        for e in ev:
+            e.record(stream)
     cvd = [v for v in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if v.strip()]
     clocks = ClockSampler(cvd[local_rank] if local_rank < len(cvd) else local_rank)
     if world > 1:
@@ -376,6 +382,11 @@ def main():
     if args.workload not in synth.WORKLOADS:
         raise SystemExit(f"unknown workload {args.workload}; choose from {sorted(synth.WORKLOADS)}")
     wl = synth.WORKLOADS[args.workload]
+    if args.experts or args.tokens:
+        import dataclasses
+        E = args.experts or wl.E
+        T = args.tokens or wl.T
+        wl = dataclasses.replace(wl, name=f"{wl.name}-E{E}-T{T}", E=E, T=T)
     if args.impl == "reference":
         import __graft_entry__ as g
         g.build_cpu()

@@ -173,6 +173,9 @@ def moe_set_stage_events(h, events) -> object:
     if events is None:
         _ok("moe_set_stage_events", lib().moe_set_stage_events(h, None, 0))
         return None
+    for e in events:  # torch creates the underlying event on first record
+        if not e.cuda_event:
+            e.record()
     arr = (ctypes.c_void_p * len(events))(*[ctypes.c_void_p(e.cuda_event) for e in events])
     _ok("moe_set_stage_events", lib().moe_set_stage_events(h, arr, len(events)))
     return arr
