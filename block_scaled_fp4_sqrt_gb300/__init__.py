@@ -25,7 +25,7 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
 EXPORTED = ("moe_experts_create", "moe_experts_set_hash_table", "moe_workspace_size", "moe_set_workspace",
             "moe_route", "moe_permute", "moe_expert_ffn", "moe_forward", "moe_get_routing", "moe_check",
             "moe_set_wait_budget", "moe_experts_destroy", "moe_status_string", "moe_last_error",
-            "moe_testing_stall_loads", "moe_set_stage_events")
+            "moe_testing_stall_loads", "moe_set_stage_events", "moe_route_noalloc")
 
 MOE_N_STAGES = 5
 STAGE_NAMES = ("route", "dispatch", "gemm_gate_up", "gemm_down", "combine")
@@ -69,6 +69,7 @@ def lib() -> ctypes.CDLL:
         L.moe_set_wait_budget.argtypes = [vp, u64]
         L.moe_testing_stall_loads.argtypes = [vp, i32]
         L.moe_set_stage_events.argtypes = [vp, ctypes.POINTER(vp), i32]
+        L.moe_route_noalloc.argtypes = [cfgp, inp, vp, vp, vp, vp, vp]
         L.moe_experts_destroy.argtypes = [vp]
         L.moe_experts_destroy.restype = None
         L.moe_status_string.argtypes = [st]
@@ -179,6 +180,12 @@ def moe_set_stage_events(h, events) -> object:
     arr = (ctypes.c_void_p * len(events))(*[ctypes.c_void_p(e.cuda_event) for e in events])
     _ok("moe_set_stage_events", lib().moe_set_stage_events(h, arr, len(events)))
     return arr
+
+
+def moe_route_noalloc(cfg: moe_config_t, x, router_w, router_bias, topk_ids, topk_w, stream=None) -> None:
+    """Learned router without a handle or workspace (fixed library scratch; see include/moe.h)."""
+    _ok("moe_route_noalloc", lib().moe_route_noalloc(ctypes.byref(cfg), ctypes.byref(_input(x)), _p(router_w),
+                                                     _p(router_bias), _p(topk_ids), _p(topk_w), _stream(stream)))
 
 
 def moe_experts_destroy(h) -> None:

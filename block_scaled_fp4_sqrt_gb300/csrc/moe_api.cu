@@ -140,6 +140,8 @@ Dims dims_for(int max_T, int E, int k) {
 
 namespace moe {
 
+void set_last_error(const char* msg) { g_last_error = msg ? msg : ""; }
+
 size_t workspace_layout(int max_T, int d, int f, int E, int k, Workspace* ws, void* base) {
   const Dims dm = dims_for(max_T, E, k);
   size_t off = 0;

@@ -62,6 +62,9 @@ struct Workspace {
   float* y_rows;         // [rows, d] weighted expert outputs (fp32)
 };
 
+// Text returned by moe_last_error() on this thread.
+void set_last_error(const char* msg);
+
 size_t workspace_layout(int max_T, int d, int f, int E, int k, Workspace* ws, void* base);
 
 // ------------------------------------------------------------------ launchers (return cudaError_t)

@@ -179,6 +179,26 @@ MOE_API moe_status_t moe_check(moe_experts_t experts, moe_stream_t stream);
 /* Upper bound, in nanoseconds, of every device-side wait (default 2 s). */
 MOE_API moe_status_t moe_set_wait_budget(moe_experts_t experts, uint64_t budget_ns);
 
+/*
+ * Learned router that allocates nothing -- for callers that can't call cudaMalloc: code running
+ * while a stream is captured into a CUDA graph (allocation is not allowed there in the default capture
+ * mode), plug-ins whose host framework owns all device memory, and latency-critical paths that must
+ * not enter an allocator.  It needs no expert handle and no workspace.  (The pages have no
+ * counterpart; it is the same router as moe_route.)
+ * Computes exactly what moe_route computes for a learned (not hash) layer: cfg gives d_model,
+ * n_experts (<= 512), top_k and route_scale; x, router_w, router_bias, topk_ids, topk_w as there.
+ * Its split-K partial sums live in one fixed 4 MiB array of library device memory (1,048,576 fp32),
+ * which every GPU that loads the library holds until the process exits; batches with
+ * T * n_experts > 1,048,576 (T > 4096 at 256 experts) are rejected with MOE_ERR_WORKSPACE.
+ * The first call on a device looks up that array's device address (with that device current); make
+ * that first call before any stream capture.  All calls share the array and it keeps the last call's
+ * contents (every call overwrites what it reads), so calls that overlap on the GPU -- on different
+ * streams, or from several host threads -- race: order them.
+ */
+MOE_API moe_status_t moe_route_noalloc(const moe_config_t* cfg, const moe_input_t* x, const float* router_w,
+                                       const float* router_bias, int32_t* topk_ids, float* topk_w,
+                                       moe_stream_t stream);
+
 MOE_API void moe_experts_destroy(moe_experts_t experts);
 MOE_API const char* moe_status_string(moe_status_t status);
 /* Text of the last host-side error on this thread ("" if none). */
