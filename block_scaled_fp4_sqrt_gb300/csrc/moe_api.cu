@@ -17,11 +17,11 @@ using namespace moe;
 
 struct moe_experts_s {
   moe_config_t cfg;
-  int n = 0;  // experts in this set
-  const uint8_t* w13 = nullptr;
-  const uint8_t* w2 = nullptr;
-  uint8_t* sf13 = nullptr;  // owned: scale atoms [n, 2f/128, d/128, 512]
-  uint8_t* sf2 = nullptr;   // owned: [n, d/128, f/128, 512]
+  int n = 0;                // experts in this set
+  uint8_t* w13 = nullptr;   // owned: packed gate-up codes [n, f/128, d/128, 256, 64]
+  uint8_t* w2 = nullptr;    // owned: packed down codes [n, d/256, f/128, 256, 64]
+  uint8_t* sf13 = nullptr;  // owned: scale atoms [n, f/128, d/128, 2, 512]
+  uint8_t* sf2 = nullptr;   // owned: [n, d/256, f/128, 2, 512]
   CUtensorMap tm13;
   CUtensorMap tm2;
   const int32_t* hash_table = nullptr;
@@ -78,6 +78,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // 2-D K-major tensor map: inner dimension K (elements), outer `rows`, box {128, box_rows}, 128-byte swizzle.
+// FP4 maps expand each 16-element chunk to 16 bytes in shared memory (the operand form of the MMA).
 moe_status_t make_map(CUtensorMap* m, const void* base, bool fp4, uint64_t K, uint64_t rows, uint32_t box_rows) {
   auto fn = encode_fn();
   if (!fn) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
@@ -94,9 +95,9 @@ moe_status_t make_map(CUtensorMap* m, const void* base, bool fp4, uint64_t K, ui
 
 moe_status_t check_cfg(const moe_config_t* c) {
   if (!c) return fail(MOE_ERR_INVALID_ARG, "config is NULL");
-  if (c->d_model <= 0 || c->d_ff <= 0 || c->d_model % 128 || c->d_ff % 128)
-    return fail(MOE_ERR_UNSUPPORTED, "d_model (%d) and d_ff (%d) must be positive multiples of 128", c->d_model,
-                c->d_ff);
+  if (c->d_model <= 0 || c->d_ff <= 0 || c->d_model % 256 || c->d_ff % 128)
+    return fail(MOE_ERR_UNSUPPORTED, "d_model (%d) must be a positive multiple of 256 and d_ff (%d) of 128",
+                c->d_model, c->d_ff);
   if (c->d_model > 65536 || c->d_ff > 65536) return fail(MOE_ERR_UNSUPPORTED, "d_model / d_ff above 65536");
   if (c->n_experts < 1 || c->n_experts > 1024)
     return fail(MOE_ERR_UNSUPPORTED, "n_experts (%d) must be in [1, 1024]", c->n_experts);
@@ -132,7 +133,7 @@ Dims dims_for(int max_T, int E, int k) {
   dm.rows = max_T * (k + 1);
   dm.G = E + 1;
   dm.n_chunks = (max_T + 31) / 32;
-  dm.max_tiles = (dm.rows + kDecodeBN - 1) / kDecodeBN + dm.G;
+  dm.max_tiles = (dm.rows + kTileRows - 1) / kTileRows + dm.G;
   return dm;
 }
 
@@ -206,8 +207,8 @@ moe_status_t moe_experts_create(const moe_config_t* cfg, int32_t n, const uint8_
   if (st != MOE_OK) return st;
   if (n < 1 || n > 1024) return fail(MOE_ERR_INVALID_ARG, "expert count %d outside [1, 1024]", n);
   if (!w13_fp4 || !w13_e8m0 || !w2_fp4 || !w2_e8m0) return fail(MOE_ERR_INVALID_ARG, "weight pointer is NULL");
-  if (!aligned(w13_fp4, 32) || !aligned(w2_fp4, 32))
-    return fail(MOE_ERR_INVALID_ARG, "FP4 weight buffers must be 32-byte aligned");
+  if (!aligned(w13_fp4, 16) || !aligned(w2_fp4, 16))
+    return fail(MOE_ERR_INVALID_ARG, "FP4 weight buffers must be 16-byte aligned");
   if (!aligned(w13_e8m0, 4) || !aligned(w2_e8m0, 4))
     return fail(MOE_ERR_INVALID_ARG, "scale buffers must be 4-byte aligned");
   int dev = 0;
@@ -223,24 +224,28 @@ moe_status_t moe_experts_create(const moe_config_t* cfg, int32_t n, const uint8_
   if (!h) return fail(MOE_ERR_CUDA, "host allocation failed");
   h->cfg = *cfg;
   h->n = n;
-  h->w13 = w13_fp4;
-  h->w2 = w2_fp4;
   h->num_sms = sms;
   h->device = dev;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const size_t w13_bytes = (size_t)n * 2 * f * (d / 2), w2_bytes = (size_t)n * d * (f / 2);
   const size_t sf13_bytes = (size_t)n * 2 * f * (d / 32), sf2_bytes = (size_t)n * d * (f / 32);
-  cudaError_t e = cudaMalloc(&h->sf13, sf13_bytes);
+  cudaError_t e = cudaMalloc(&h->w13, w13_bytes);
+  if (e == cudaSuccess) e = cudaMalloc(&h->w2, w2_bytes);
+  if (e == cudaSuccess) e = cudaMalloc(&h->sf13, sf13_bytes);
   if (e == cudaSuccess) e = cudaMalloc(&h->sf2, sf2_bytes);
   if (e == cudaSuccess) e = cudaMalloc(&h->status, sizeof(int));
   if (e == cudaSuccess) e = cudaMemsetAsync(h->status, 0, sizeof(int), s);
-  if (e == cudaSuccess) e = launch_pack_weight_sf(w13_e8m0, n, 2 * f, d, h->sf13, s);
-  if (e == cudaSuccess) e = launch_pack_weight_sf(w2_e8m0, n, d, f, h->sf2, s);
+  if (e == cudaSuccess) e = launch_pack_weights(w13_fp4, n, 2 * f, d, 0, h->w13, s);
+  if (e == cudaSuccess) e = launch_pack_weights(w2_fp4, n, d, f, 1, h->w2, s);
+  if (e == cudaSuccess) e = launch_pack_weight_sf(w13_e8m0, n, 2 * f, d, 0, h->sf13, s);
+  if (e == cudaSuccess) e = launch_pack_weight_sf(w2_e8m0, n, d, f, 1, h->sf2, s);
   if (e != cudaSuccess) {
     moe_experts_destroy(h);
     return cuda_fail(e, "moe_experts_create");
   }
-  st = make_map(&h->tm13, w13_fp4, true, (uint64_t)d, (uint64_t)n * 2 * f, 128);
-  if (st == MOE_OK) st = make_map(&h->tm2, w2_fp4, true, (uint64_t)f, (uint64_t)n * d, 128);
+  // packed codes as [slabs * 256 rows, 128 FP4]: one 256-row box per (output tile, K group)
+  st = make_map(&h->tm13, h->w13, true, 128, (uint64_t)n * 2 * f * (d / 128), 256);
+  if (st == MOE_OK) st = make_map(&h->tm2, h->w2, true, 128, (uint64_t)n * d * (f / 128), 256);
   if (st != MOE_OK) {
     moe_experts_destroy(h);
     return st;
@@ -251,6 +256,8 @@ moe_status_t moe_experts_create(const moe_config_t* cfg, int32_t n, const uint8_
 
 void moe_experts_destroy(moe_experts_t h) {
   if (!h) return;
+  if (h->w13) cudaFree(h->w13);
+  if (h->w2) cudaFree(h->w2);
   if (h->sf13) cudaFree(h->sf13);
   if (h->sf2) cudaFree(h->sf2);
   if (h->status) cudaFree(h->status);
@@ -350,12 +357,12 @@ moe_status_t moe_permute(moe_experts_t h, const moe_input_t* x, const int32_t* t
     return MOE_OK;
   }
   MOE_CUDA(launch_histogram(topk_ids, T, k, E, E, h->ws.chunk_hist, h->status, s), "histogram");
-  MOE_CUDA(launch_scan(h->ws.chunk_hist, n_chunks, T, E, E, 0, kDecodeBN, dm.max_tiles, counts, offsets,
+  MOE_CUDA(launch_scan(h->ws.chunk_hist, n_chunks, T, E, E, 0, kTileRows, dm.max_tiles, counts, offsets,
                        h->ws.tile_off, h->ws.n_tiles, h->ws.tiles, h->status, s),
            "scan");
   uint8_t* q = a_q ? a_q : h->ws.a_q;
   MOE_CUDA(launch_gather(static_cast<const __nv_bfloat16*>(x->x_bf16), topk_ids, nullptr, h->ws.chunk_hist, offsets,
-                         h->ws.tile_off, T, d, k, E, E, 0, kDecodeBN, q, nullptr, a_s, perm_tok, inv_pos, nullptr, s),
+                         h->ws.tile_off, T, d, k, E, E, 0, kTileRows, q, nullptr, a_s, perm_tok, inv_pos, nullptr, s),
            "gather");
   return MOE_OK;
 }
@@ -368,17 +375,19 @@ static moe_status_t run_ffn(moe_experts_s* h, moe_experts_s* sh, int rows, int E
                             const uint8_t* a_q, const uint8_t* a_sf_atoms, const float* row_w, float* y_f32,
                             __nv_bfloat16* y_bf16, int max_tiles, bool timed, cudaStream_t s) {
   const int d = h->cfg.d_model, f = h->cfg.d_ff;
-  CUtensorMap tm_a, tm_h;
-  moe_status_t st = make_map(&tm_a, a_q, false, (uint64_t)d, (uint64_t)rows, kDecodeBN);
-  if (st == MOE_OK) st = make_map(&tm_h, h->ws.h_q, false, (uint64_t)f, (uint64_t)rows, kDecodeBN);
+  CUtensorMap tm_a, tm_a32, tm_h, tm_h32;
+  moe_status_t st = make_map(&tm_a, a_q, false, (uint64_t)d, (uint64_t)rows, kTileRows);
+  if (st == MOE_OK) st = make_map(&tm_a32, a_q, false, (uint64_t)d, (uint64_t)rows, 32);
+  if (st == MOE_OK) st = make_map(&tm_h, h->ws.h_q, false, (uint64_t)f, (uint64_t)rows, kTileRows);
+  if (st == MOE_OK) st = make_map(&tm_h32, h->ws.h_q, false, (uint64_t)f, (uint64_t)rows, 32);
   if (st != MOE_OK) return st;
   const moe_experts_s* shx = sh ? sh : h;
-  MOE_CUDA(launch_gemm_gate_up(h->tm13, shx->tm13, h->sf13, shx->sf13, tm_a, a_sf_atoms, h->ws.tiles, h->ws.n_tiles,
+  MOE_CUDA(launch_gemm_gate_up(h->tm13, shx->tm13, h->sf13, shx->sf13, tm_a, tm_a32, a_sf_atoms, h->ws.tiles, h->ws.n_tiles,
                                max_tiles, E_groups_shared_index, d, f, h->cfg.swiglu_limit, h->ws.h_q, h->ws.h_sf,
                                h->status, h->budget_ns, h->stall_loads, h->num_sms, s),
            "gate-up GEMM");
   if (timed) mark_stage(h, 3, s);
-  MOE_CUDA(launch_gemm_down(h->tm2, shx->tm2, h->sf2, shx->sf2, tm_h, h->ws.h_sf, h->ws.tiles, h->ws.n_tiles, max_tiles,
+  MOE_CUDA(launch_gemm_down(h->tm2, shx->tm2, h->sf2, shx->sf2, tm_h, tm_h32, h->ws.h_sf, h->ws.tiles, h->ws.n_tiles, max_tiles,
                             E_groups_shared_index, d, f, row_w, y_f32, y_bf16, h->status, h->budget_ns,
                             h->stall_loads, h->num_sms, s),
            "down GEMM");
@@ -398,7 +407,7 @@ moe_status_t moe_expert_ffn(moe_experts_t h, int32_t n_rows, const int32_t* offs
   if (!aligned(a_q, 16) || !aligned(a_s, 4) || !aligned(y_bf16, 16))
     return fail(MOE_ERR_INVALID_ARG, "a_q and y must be 16-byte aligned, a_s 4-byte aligned");
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  MOE_CUDA(launch_tiles_from_offsets(offsets, offsets ? h->n : 1, n_rows, kDecodeBN, dm.max_tiles, h->ws.tile_off,
+  MOE_CUDA(launch_tiles_from_offsets(offsets, offsets ? h->n : 1, n_rows, kTileRows, dm.max_tiles, h->ws.tile_off,
                                      h->ws.n_tiles, h->ws.tiles, h->status, s),
            "tile list");
   MOE_CUDA(launch_rows_sf_to_atoms(a_s, h->ws.tiles, h->ws.n_tiles, h->cfg.d_model, dm.max_tiles, h->ws.a_sf, s),
@@ -447,11 +456,11 @@ moe_status_t moe_forward(const moe_input_t* x, const float* router_w, const floa
   const Dims dm = dims_for(h->ws_max_T, E, k);
   const int n_chunks = (T + 31) / 32;
   MOE_CUDA(launch_histogram(h->ws.topk_ids, T, k, E, G, h->ws.chunk_hist, h->status, s), "histogram");
-  MOE_CUDA(launch_scan(h->ws.chunk_hist, n_chunks, T, E, G, has_shared, kDecodeBN, dm.max_tiles, h->ws.counts,
+  MOE_CUDA(launch_scan(h->ws.chunk_hist, n_chunks, T, E, G, has_shared, kTileRows, dm.max_tiles, h->ws.counts,
                        h->ws.offsets, h->ws.tile_off, h->ws.n_tiles, h->ws.tiles, h->status, s),
            "scan");
   MOE_CUDA(launch_gather(static_cast<const __nv_bfloat16*>(x->x_bf16), h->ws.topk_ids, h->ws.topk_w, h->ws.chunk_hist,
-                         h->ws.offsets, h->ws.tile_off, T, d, k, E, G, has_shared, kDecodeBN, h->ws.a_q, h->ws.a_sf,
+                         h->ws.offsets, h->ws.tile_off, T, d, k, E, G, has_shared, kTileRows, h->ws.a_q, h->ws.a_sf,
                          nullptr, h->ws.perm_tok, h->ws.inv_pos, h->ws.row_w, s),
            "gather");
   mark_stage(h, 2, s);

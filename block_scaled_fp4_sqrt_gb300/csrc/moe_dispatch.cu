@@ -11,6 +11,8 @@
 //  * combine:    out[t] = sum_j Yr[inv_pos[t, j]] + Yr[R + t] in fp32, in the fixed order j = 0..k-1
 //                then the shared row, rounded once to bf16 (the weighted-sum epilogue; the routing
 //                weight was applied in the down GEMM).
+#include <algorithm>
+
 #include "moe_device.cuh"
 
 namespace moe {
@@ -275,18 +277,57 @@ __global__ void rows_sf_to_atoms_kernel(const uint8_t* __restrict__ a_s_rows, co
   }
 }
 
-// weight scales [n, rows, K/32] -> atoms [n, rows/128, K/128, 512]
-__global__ void pack_weight_sf_kernel(const uint8_t* __restrict__ s, int n, int rows, int K, uint8_t* __restrict__ atoms) {
-  const int groups = K / kKGroup;
+// Output tile and row inside its 256-row slab of canonical weight row `row` (see launch_pack_weights).
+__device__ __forceinline__ void slab_of_row(int row, int rows, int mode, int* tile, int* rr) {
+  if (mode == 0) {
+    const int f = rows / 2;
+    const bool up = row >= f;
+    const int fr = up ? row - f : row;
+    *tile = fr >> 7;
+    *rr = (up ? 128 : 0) + (fr & 127);
+  } else {
+    *tile = row >> 8;
+    *rr = row & 255;
+  }
+}
+
+// codes [n, rows, K/2] -> packed [n, rows/256, K/128, 256, 64]; one 16-byte chunk per thread step
+__global__ void pack_weights_kernel(const uint8_t* __restrict__ src, int n, int rows, int K, int mode,
+                                    uint8_t* __restrict__ dst) {
+  const int KG = K / kKGroup, MT = rows / 256;
+  const size_t total = (size_t)n * rows * (K / 2) / 16;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
+    const int c16 = (int)(i & 3);
+    const int rr = (int)((i >> 2) & 255);
+    const size_t rest = i >> 10;  // (e * MT + mt) * KG + kg
+    const int kg = (int)(rest % KG);
+    const size_t emt = rest / KG;
+    const int mt = (int)(emt % MT);
+    const size_t e = emt / MT;
+    int row;
+    if (mode == 0) row = rr < 128 ? mt * 128 + rr : rows / 2 + mt * 128 + (rr - 128);
+    else row = mt * 256 + rr;
+    const uint4 v = *reinterpret_cast<const uint4*>(src + (e * rows + row) * (size_t)(K / 2) + kg * 64 + c16 * 16);
+    reinterpret_cast<uint4*>(dst)[i] = v;
+  }
+}
+
+// scales [n, rows, K/32] -> atoms [n, rows/256, K/128, 2, 512]
+__global__ void pack_weight_sf_kernel(const uint8_t* __restrict__ s, int n, int rows, int K, int mode,
+                                      uint8_t* __restrict__ atoms) {
+  const int groups = K / kKGroup, MT = rows / 256;
   const size_t total = (size_t)n * rows * groups;
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
     const int grp = (int)(i % groups);
     const size_t er = i / groups;  // e * rows + r
     const int r = (int)(er % rows);
     const size_t e = er / rows;
+    int tile, rr;
+    slab_of_row(r, rows, mode, &tile, &rr);
+    const int half = rr >> 7, lr = rr & 127;
     const uint32_t word = *reinterpret_cast<const uint32_t*>(s + er * (K / 32) + grp * 4);
-    const size_t blk = (e * (rows / kMmaM) + r / kMmaM) * groups + grp;
-    *reinterpret_cast<uint32_t*>(atoms + blk * kSfAtomBytes + (r & 31) * 16 + ((r & 127) >> 5) * 4) = word;
+    const size_t blk = (((e * MT + tile) * groups + grp) * 2 + half);
+    *reinterpret_cast<uint32_t*>(atoms + blk * kSfAtomBytes + (lr & 31) * 16 + (lr >> 5) * 4) = word;
   }
 }
 
@@ -362,10 +403,19 @@ cudaError_t launch_rows_sf_to_atoms(const uint8_t* a_s_rows, const RowTile* tile
   return cudaGetLastError();
 }
 
-cudaError_t launch_pack_weight_sf(const uint8_t* sc, int n, int rows, int K, uint8_t* atoms, cudaStream_t s) {
+cudaError_t launch_pack_weights(const uint8_t* codes, int n, int rows, int K, int mode, uint8_t* packed,
+                                cudaStream_t s) {
+  const size_t total = (size_t)n * rows * (K / 2) / 16;
+  const int blocks = (int)std::min<size_t>((total + 255) / 256, 152 * 32);
+  pack_weights_kernel<<<blocks > 0 ? blocks : 1, 256, 0, s>>>(codes, n, rows, K, mode, packed);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pack_weight_sf(const uint8_t* sc, int n, int rows, int K, int mode, uint8_t* atoms,
+                                  cudaStream_t s) {
   const size_t total = (size_t)n * rows * (K / kKGroup);
-  const int blocks = (int)((total + 255) / 256 < 4096 ? (total + 255) / 256 : 4096);
-  pack_weight_sf_kernel<<<blocks > 0 ? blocks : 1, 256, 0, s>>>(sc, n, rows, K, atoms);
+  const int blocks = (int)std::min<size_t>((total + 255) / 256, 4096);
+  pack_weight_sf_kernel<<<blocks > 0 ? blocks : 1, 256, 0, s>>>(sc, n, rows, K, mode, atoms);
   return cudaGetLastError();
 }
 

@@ -1,5 +1,5 @@
 // Grouped expert GEMMs on 5th-generation tensor cores (tcgen05, kind::mxf8f6f4 with E8M0 block
-// scales): MXFP4 expert weights x MXFP8 activations, fp32 accumulation in tensor memory.
+// scales): MXFP8 activations x MXFP4 expert weights, fp32 accumulation in tensor memory.
 //
 //  * gate-up:  G = A . W1^T, U = A . W3^T per expert group; epilogue h = silu(min(G, L)) *
 //    clamp(U, -L, L) (Ops.SiLUMulClamp, swiglu_limit = 10), re-quantised to MXFP8 along the FFN
@@ -9,55 +9,58 @@
 //    weighted-sum epilogue moe_scatter_add of the TensorSharp page, "DSpark and MoE CPU offload") or
 //    bf16 (the standalone grouped FFN call).
 //
-// Tile shape ("swap-AB"): the 128 weight rows of one output tile are the MMA's M side, the token
-// rows of one expert group (up to 32) are its N side, so a verify batch with ~12 rows per expert
-// streams each weight byte from HBM exactly once.  One persistent CTA per SM walks a device-built
-// list of (row tile, output tile) work items.  Warp roles: warp 0 issues TMA loads, warp 1 issues
-// tcgen05 copies/MMAs, warps 2..5 drain the TMEM accumulators (double buffered) and run the
-// epilogue.  Every wait is bounded; on timeout the kernel records DEV_TIMEOUT and unwinds.
+// Tile shape.  One MMA (M = 128, N <= 256, K = 32) takes the same time for any N, so the weights sit
+// on the N side: 256 weight rows per MMA (gate 128 + up 128 of one 128-wide FFN slice, or 256 rows of
+// the down projection), the token rows of one expert group (up to 128) on the M side.  Each MMA then
+// consumes 4 KB of MXFP4 weights, enough to stream HBM at full rate even for a handful of tokens.
+// The weights are stored tile-contiguous (see moe_api.cu), so every pipeline stage is one contiguous
+// 16 KB TMA box.
+//
+// One persistent CTA per SM walks a device-built list of (row tile, output tile) work items.  Warp 0
+// issues TMA loads, warp 1 the tcgen05 scale copies and MMAs, warps 2..17 drain the accumulator:
+// four warps per 32-lane TMEM quadrant, each owning a quarter of the 256 columns, so one thread holds
+// one token row of one MX block and needs no shuffles.  The accumulator is released as soon as it is
+// in registers.  Every wait is bounded; on timeout the kernel records DEV_TIMEOUT and unwinds.
 #include "moe_device.cuh"
 
 namespace moe {
 
 namespace {
 
-constexpr int kBN = kDecodeBN;  // token rows per MMA (tcgen05 N)
+constexpr int kN = 256;         // weight rows per MMA (tcgen05 N)
+constexpr int kBM = kTileRows;  // token rows per MMA (tcgen05 M) = 128
+constexpr int kSmallRows = 32;  // groups this small load a 32-row activation box
+constexpr int kEpiWarps = 16;
+constexpr int kThreads = 64 + 32 * kEpiWarps;
 
-__host__ __device__ constexpr int pow2_at_least(int v) {
-  int p = 32;
-  while (p < v) p <<= 1;
-  return p;
-}
-
-template <int NMAT, int STAGES>
+template <int STAGES>
 struct Cfg {
-  static constexpr int kATile = kMmaM * 128;       // one 128 x 128 weight tile, FP4 padded to bytes in smem
-  static constexpr int kBTile = kBN * 128;         // 32 token rows x 128 FP8
-  static constexpr int kSfBytes = (NMAT + 1) * kSfAtomBytes;
-  static constexpr int kStageRaw = NMAT * kATile + kBTile + kSfBytes;
+  static constexpr int kATile = kBM * 128;           // 128 token rows x 128 FP8
+  static constexpr int kBTile = kN * 128;            // 256 weight rows x 128 FP4, padded to bytes
+  static constexpr int kSfBytes = 3 * kSfAtomBytes;  // activation atom + two weight atoms
+  static constexpr int kStageRaw = kATile + kBTile + kSfBytes;
   static constexpr int kStage = (kStageRaw + 1023) / 1024 * 1024;
-  static constexpr int kBarBytes = (2 * STAGES + 5) * 8;
+  static constexpr int kBarBytes = (2 * STAGES + 3) * 8;
   static constexpr int kSmem = STAGES * kStage + 1024 + kBarBytes;
-  // bytes delivered per stage: packed FP4 boxes count 64 bytes per row
-  static constexpr uint32_t kTx = NMAT * (kMmaM * 64) + kBTile + kSfBytes;
-  static constexpr int kAccCols = 2 * NMAT * kBN;  // two accumulator buffers
-  static constexpr int kSfCols = (NMAT + 1) * 4;   // per stage
-  static constexpr int kTmemCols = pow2_at_least(kAccCols + STAGES * kSfCols);
+  static constexpr uint32_t kTxB = kN * 64 + 2 * kSfAtomBytes;  // packed FP4 box (64 B per row) + weight atoms
+  static constexpr int kAccCols = kN;                           // one fp32 accumulator [128 x 256]
+  static constexpr int kSfCols = 12;                            // per stage: A atom 4 columns, B atoms 8
+  static constexpr int kTmemCols = 512;
+  static_assert(kAccCols + STAGES * kSfCols <= kTmemCols, "TMEM budget");
+  static_assert(kSmem <= 232448, "shared memory budget");
 };
 
 struct GemmArgs {
-  const uint8_t* sf_routed;  // weight scale atoms [E, w_mblocks, KG, 512]
-  const uint8_t* sf_shared;  // [1, w_mblocks, KG, 512]
+  const uint8_t* sf_routed;  // weight scale atoms [E, m_tiles, KG, 2, 512]
+  const uint8_t* sf_shared;  // [1, m_tiles, KG, 2, 512]
   const uint8_t* act_sf;     // activation scale atoms [tile, KG, 512]
   const RowTile* tiles;
   const int32_t* n_tiles;
   int max_tiles;
-  int E;                // group E is the shared expert
-  int KG;               // K / 128
-  int m_tiles;          // output tiles of 128 per row tile
-  int rows_per_expert;  // weight rows per expert in the tensor map
-  int up_row_offset;    // gate-up: rows f .. 2f-1 are the up projection
-  int w_mblocks;        // rows_per_expert / 128
+  int E;        // group E is the shared expert
+  int KG;       // K / 128
+  int m_tiles;  // 256-wide output tiles per row tile (f/128 gate-up slices, or d/256)
+  int gate_up;  // 1: SwiGLU + MXFP8 epilogue; 0: weighted fp32 / bf16 rows
   // gate-up epilogue
   float limit;
   uint8_t* h_q;
@@ -75,18 +78,19 @@ struct GemmArgs {
 
 __device__ __forceinline__ float silu_f(float z) { return z / (1.0f + expf(-z)); }
 
-template <int NMAT, int STAGES>
-__global__ void __launch_bounds__(192, 1)
+template <int STAGES>
+__global__ void __launch_bounds__(kThreads, 1)
     grouped_mx_gemm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_w_shared,
-                           const __grid_constant__ CUtensorMap tm_act, const GemmArgs a) {
-  using C = Cfg<NMAT, STAGES>;
+                           const __grid_constant__ CUtensorMap tm_act, const __grid_constant__ CUtensorMap tm_act_small,
+                           const GemmArgs a) {
+  using C = Cfg<STAGES>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * C::kStage);
   uint64_t* empty = full + STAGES;
-  uint64_t* acc_full = empty + STAGES;  // [2]
-  uint64_t* acc_empty = acc_full + 2;   // [2]
-  uint64_t* drain = acc_empty + 2;      // [1]
+  uint64_t* acc_full = empty + STAGES;
+  uint64_t* acc_empty = acc_full + 1;
+  uint64_t* drain = acc_empty + 1;
   __shared__ uint32_t tmem_slot;
   __shared__ volatile int abort_flag;
 
@@ -100,10 +104,8 @@ __global__ void __launch_bounds__(192, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&acc_full[b], 1);
-      mbar_init(&acc_empty[b], 4);
-    }
+    mbar_init(acc_full, 1);
+    mbar_init(acc_empty, kEpiWarps);
     mbar_init(drain, 1);
     abort_flag = 0;
     mbar_fence_init();
@@ -112,6 +114,7 @@ __global__ void __launch_bounds__(192, 1)
     prefetch_tensormap(&tm_w);
     prefetch_tensormap(&tm_w_shared);
     prefetch_tensormap(&tm_act);
+    prefetch_tensormap(&tm_act_small);
   }
   if (warp == 1) tmem_alloc(&tmem_slot, C::kTmemCols);
   tc_fence_before();
@@ -122,7 +125,7 @@ __global__ void __launch_bounds__(192, 1)
   if (warp == 0) {
     if (lane == 0) {
       // ---------------------------------------------------------------- TMA producer
-      const uint64_t pol_w = l2_policy_evict_first();  // weights: streamed once
+      const uint64_t pol_w = l2_policy_evict_first();  // weights: streamed once per row tile
       const uint64_t pol_a = l2_policy_evict_last();   // activations: re-read by every output tile
       int stage = 0;
       uint32_t phase = 0;
@@ -134,25 +137,25 @@ __global__ void __launch_bounds__(192, 1)
         const bool sh = rt.group == a.E;
         const CUtensorMap* tw = sh ? &tm_w_shared : &tm_w;
         const int e = sh ? 0 : rt.group;
-        const int wrow = e * a.rows_per_expert + mt * kMmaM;
-        const uint8_t* sfw = (sh ? a.sf_shared : a.sf_routed) + (size_t)e * a.w_mblocks * a.KG * kSfAtomBytes;
-        const uint8_t* sf_gate = sfw + (size_t)mt * a.KG * kSfAtomBytes;
-        const uint8_t* sf_up = sfw + (size_t)(a.up_row_offset / kMmaM + mt) * a.KG * kSfAtomBytes;
-        const uint8_t* sf_act = a.act_sf + (size_t)ti * a.KG * kSfAtomBytes;
+        const bool small = rt.nrows <= kSmallRows;
+        const CUtensorMap* ta = small ? &tm_act_small : &tm_act;
+        const uint32_t tx = C::kTxB + (small ? kSmallRows : kBM) * 128 + kSfAtomBytes;
+        const int wrow0 = (e * a.m_tiles + mt) * a.KG * kN;  // first packed row of this output tile
+        const uint8_t* sfw =
+            (sh ? a.sf_shared : a.sf_routed) + ((size_t)e * a.m_tiles + mt) * a.KG * 2 * kSfAtomBytes;
+        const uint8_t* sfa = a.act_sf + (size_t)ti * a.KG * kSfAtomBytes;
         for (int kg = 0; kg < a.KG; ++kg) {
           if (abort_flag || !mbar_wait(&empty[stage], phase ^ 1u, a.budget_ns)) {
             ok = false;
             break;
           }
           uint8_t* st = smem + stage * C::kStage;
-          mbar_arrive_expect_tx(&full[stage], C::kTx);
-          tma_load_2d(st, tw, kg * kKGroup, wrow, &full[stage], pol_w);
-          if (NMAT == 2) tma_load_2d(st + C::kATile, tw, kg * kKGroup, wrow + a.up_row_offset, &full[stage], pol_w);
-          tma_load_2d(st + NMAT * C::kATile, &tm_act, kg * kKGroup, rt.row0, &full[stage], pol_a);
-          uint8_t* sf = st + NMAT * C::kATile + C::kBTile;
-          bulk_load(sf, sf_gate + kg * kSfAtomBytes, kSfAtomBytes, &full[stage]);
-          if (NMAT == 2) bulk_load(sf + kSfAtomBytes, sf_up + kg * kSfAtomBytes, kSfAtomBytes, &full[stage]);
-          bulk_load(sf + NMAT * kSfAtomBytes, sf_act + kg * kSfAtomBytes, kSfAtomBytes, &full[stage]);
+          mbar_arrive_expect_tx(&full[stage], tx);
+          tma_load_2d(st + C::kATile, tw, 0, wrow0 + kg * kN, &full[stage], pol_w);
+          tma_load_2d(st, ta, kg * kKGroup, rt.row0, &full[stage], pol_a);
+          uint8_t* sf = st + C::kATile + C::kBTile;
+          bulk_load(sf, sfa + kg * kSfAtomBytes, kSfAtomBytes, &full[stage]);
+          bulk_load(sf + kSfAtomBytes, sfw + kg * 2 * kSfAtomBytes, 2 * kSfAtomBytes, &full[stage]);
           issued |= 1u << stage;
           last_par = (last_par & ~(1u << stage)) | (phase << stage);
           if (++stage == STAGES) {
@@ -172,21 +175,19 @@ __global__ void __launch_bounds__(192, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------------------------------------------------------- MMA issuer
-      const uint32_t idesc_k[4] = {mma_idesc(5, 0, kMmaM, kBN, 0, 0), mma_idesc(5, 0, kMmaM, kBN, 1, 1),
-                                   mma_idesc(5, 0, kMmaM, kBN, 2, 2), mma_idesc(5, 0, kMmaM, kBN, 3, 3)};
+      // A = activations (E4M3), B = weights (E2M1); the sf id picks the 32-element block of the group
+      const uint32_t idesc_k[4] = {mma_idesc(0, 5, kBM, kN, 0, 0), mma_idesc(0, 5, kBM, kN, 1, 1),
+                                   mma_idesc(0, 5, kBM, kN, 2, 2), mma_idesc(0, 5, kBM, kN, 3, 3)};
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true, any = false;
       int it = 0;
       for (int w = blockIdx.x; w < total && ok; w += gridDim.x, ++it) {
-        const int acc = it & 1;
-        const uint32_t acc_par = (uint32_t)(it >> 1) & 1u;
-        if (abort_flag || !mbar_wait(&acc_empty[acc], acc_par ^ 1u, a.budget_ns)) {
+        if (abort_flag || !mbar_wait(acc_empty, ((uint32_t)it & 1u) ^ 1u, a.budget_ns)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t d0 = tbase + (uint32_t)(acc * NMAT * kBN);
         for (int kg = 0; kg < a.KG; ++kg) {
           if (abort_flag || !mbar_wait(&full[stage], phase, a.budget_ns)) {
             ok = false;
@@ -194,22 +195,16 @@ __global__ void __launch_bounds__(192, 1)
           }
           tc_fence_after();
           uint8_t* st = smem + stage * C::kStage;
-          const uint8_t* sf = st + NMAT * C::kATile + C::kBTile;
+          const uint8_t* sf = st + C::kATile + C::kBTile;
           const uint32_t sf_t = tbase + (uint32_t)(C::kAccCols + stage * C::kSfCols);
 #pragma unroll
-          for (int m = 0; m <= NMAT; ++m)
+          for (int m = 0; m < 3; ++m)
             tc_copy_sf(sf_t + 4 * m, smem_desc(smem_addr(sf + m * kSfAtomBytes), 128, 128, 0));
-          const uint32_t a_addr = smem_addr(st), b_addr = smem_addr(st + NMAT * C::kATile);
+          const uint32_t a_addr = smem_addr(st), b_addr = smem_addr(st + C::kATile);
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const uint64_t bdesc = smem_desc(b_addr + k * 32, 16, 1024, 2);
-            const uint32_t accumulate = (kg | k) ? 1u : 0u;
-            tc_mma_mx(d0, smem_desc(a_addr + k * 32, 16, 1024, 2), bdesc, idesc_k[k], sf_t, sf_t + 4 * NMAT,
-                      accumulate);
-            if (NMAT == 2)
-              tc_mma_mx(d0 + kBN, smem_desc(a_addr + C::kATile + k * 32, 16, 1024, 2), bdesc, idesc_k[k], sf_t + 4,
-                        sf_t + 4 * NMAT, accumulate);
-          }
+          for (int k = 0; k < 4; ++k)
+            tc_mma_mx(tbase, smem_desc(a_addr + k * 32, 16, 1024, 2), smem_desc(b_addr + k * 32, 16, 1024, 2),
+                      idesc_k[k], sf_t, sf_t + 4, (kg | k) ? 1u : 0u);
           any = true;
           tc_commit(&empty[stage]);
           if (++stage == STAGES) {
@@ -218,7 +213,7 @@ __global__ void __launch_bounds__(192, 1)
           }
         }
         if (!ok) break;
-        tc_commit(&acc_full[acc]);
+        tc_commit(acc_full);
       }
       if (!ok) {
         set_status(a.status, DEV_TIMEOUT);
@@ -230,14 +225,13 @@ __global__ void __launch_bounds__(192, 1)
       }
     }
   } else {
-    // ------------------------------------------------------------------ epilogue (warps 2..5)
-    const int q = warp & 3;  // TMEM lane quadrant this warp may access
-    const int m = q * 32 + lane;
+    // ------------------------------------------------------------------ epilogue (warps 2..17)
+    const int q = warp & 3;         // TMEM lane quadrant: token rows 32q .. 32q+31
+    const int c = (warp - 2) >> 2;  // column quarter
+    const int lr = q * 32 + lane;   // token row inside the tile
     int it = 0;
     for (int w = blockIdx.x; w < total; w += gridDim.x, ++it) {
-      const int acc = it & 1;
-      const uint32_t acc_par = (uint32_t)(it >> 1) & 1u;
-      bool got = !abort_flag && mbar_wait(&acc_full[acc], acc_par, a.budget_ns);
+      bool got = !abort_flag && mbar_wait(acc_full, (uint32_t)it & 1u, a.budget_ns);
       got = __all_sync(0xFFFFFFFFu, got);
       if (!got) {
         if (lane == 0) {
@@ -249,46 +243,65 @@ __global__ void __launch_bounds__(192, 1)
       tc_fence_after();
       const int ti = w / a.m_tiles, mt = w - ti * a.m_tiles;
       const RowTile rt = a.tiles[ti];
-      const uint32_t tl = tbase + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * NMAT * kBN);
-      float g[kBN];
-      tmem_ld32(tl, g);
-      if (NMAT == 2) {
-        float u[kBN];
-        tmem_ld32(tl + kBN, u);
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&acc_empty[acc]);
+      const bool active = q * 32 < rt.nrows;  // warp-uniform
+      const uint32_t tl = tbase + ((uint32_t)(q * 32) << 16);
+      float v0[32], v1[32];
+      if (active) {
+        // gate-up: gate columns 32c.., up columns 128+32c..; down: columns 64c .. 64c+63
+        tmem_ld32(tl + (uint32_t)(a.gate_up ? 32 * c : 64 * c), v0);
+        tmem_ld32(tl + (uint32_t)(a.gate_up ? 128 + 32 * c : 64 * c + 32), v1);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acc_empty);
+      if (!active || lr >= rt.nrows) continue;
+      const int r = rt.row0 + lr;
+      if (a.gate_up) {
         const float L = a.limit;
-        const int fcol = mt * kMmaM + m;
-        uint8_t* hq_base = a.h_q + fcol;
-        uint8_t* hsf_base = a.h_sf + ((size_t)ti * (a.f / kKGroup) + mt) * kSfAtomBytes + q;
+        float* h = v0;  // h overwrites the gate values in place
+        float amax = 0.f;
 #pragma unroll
-        for (int n = 0; n < kBN; ++n) {
-          const float gc = fminf(g[n], L);
-          const float uc = fminf(fmaxf(u[n], -L), L);
-          const float h = silu_f(gc) * uc;
-          const uint32_t amax_bits = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(fabsf(h)));
-          const int se = mxfp8_block_exp(__uint_as_float(amax_bits));
-          const uint8_t code = (uint8_t)(e4m3x2(h * exp2_neg_int(se), 0.0f) & 0xFF);
-          if (n < rt.nrows) {
-            hq_base[(size_t)(rt.row0 + n) * a.f] = code;
-            if (lane == 0) hsf_base[(n & 31) * 16 + (n >> 5) * 4] = (uint8_t)(se + 127);
-          }
+        for (int j = 0; j < 32; ++j) {
+          const float gc = fminf(v0[j], L);
+          const float uc = fminf(fmaxf(v1[j], -L), L);
+          h[j] = silu_f(gc) * uc;
+          amax = fmaxf(amax, fabsf(h[j]));
         }
-      } else {
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&acc_empty[acc]);
-        const int dcol = mt * kMmaM + m;
+        const int se = mxfp8_block_exp(amax);
+        const float mul = exp2_neg_int(se);
+        uint32_t packed[8];
 #pragma unroll
-        for (int n = 0; n < kBN; ++n) {
-          if (n < rt.nrows) {
-            const int r = rt.row0 + n;
-            const float wr = a.row_w ? __ldg(&a.row_w[r]) : 1.0f;
-            if (a.y_f32)
-              a.y_f32[(size_t)r * a.d + dcol] = g[n] * wr;
-            else
-              a.y_bf16[(size_t)r * a.d + dcol] = __float2bfloat16_rn(g[n] * wr);
+        for (int i = 0; i < 8; ++i) {
+          const uint32_t lo = e4m3x2(h[4 * i] * mul, h[4 * i + 1] * mul);
+          const uint32_t hi = e4m3x2(h[4 * i + 2] * mul, h[4 * i + 3] * mul);
+          packed[i] = lo | (hi << 16);
+        }
+        uint4* dst = reinterpret_cast<uint4*>(a.h_q + (size_t)r * a.f + mt * kKGroup + 32 * c);
+        dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+        dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+        a.h_sf[((size_t)ti * (a.f / kKGroup) + mt) * kSfAtomBytes + (lr & 31) * 16 + (lr >> 5) * 4 + c] =
+            (uint8_t)(se + 127);
+      } else {
+        const float wr = a.row_w ? __ldg(&a.row_w[r]) : 1.0f;
+        const size_t col0 = (size_t)mt * kN + 64 * c;
+        if (a.y_f32) {
+          float4* dst = reinterpret_cast<float4*>(a.y_f32 + (size_t)r * a.d + col0);
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            dst[i] = make_float4(v0[4 * i] * wr, v0[4 * i + 1] * wr, v0[4 * i + 2] * wr, v0[4 * i + 3] * wr);
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            dst[8 + i] = make_float4(v1[4 * i] * wr, v1[4 * i + 1] * wr, v1[4 * i + 2] * wr, v1[4 * i + 3] * wr);
+        } else {
+          uint4* dst = reinterpret_cast<uint4*>(a.y_bf16 + (size_t)r * a.d + col0);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float* src = i < 4 ? &v0[8 * i] : &v1[8 * (i - 4)];
+            uint4 o;
+            __nv_bfloat162* ov = reinterpret_cast<__nv_bfloat162*>(&o);
+#pragma unroll
+            for (int p = 0; p < 4; ++p) ov[p] = __floats2bfloat162_rn(src[2 * p] * wr, src[2 * p + 1] * wr);
+            dst[i] = o;
           }
         }
       }
@@ -301,31 +314,29 @@ __global__ void __launch_bounds__(192, 1)
   if (warp == 1) tmem_dealloc(tbase, C::kTmemCols);
 }
 
-template <int NMAT, int STAGES>
-cudaError_t launch_grouped(const CUtensorMap& w, const CUtensorMap& w_sh, const CUtensorMap& act, const GemmArgs& a,
-                           int num_sms, cudaStream_t s) {
-  using C = Cfg<NMAT, STAGES>;
+constexpr int kStages = 4;
+
+cudaError_t launch_grouped(const CUtensorMap& w, const CUtensorMap& w_sh, const CUtensorMap& act,
+                           const CUtensorMap& act_small, const GemmArgs& a, int num_sms, cudaStream_t s) {
+  using C = Cfg<kStages>;
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(grouped_mx_gemm_kernel<NMAT, STAGES>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+    cudaError_t e =
+        cudaFuncSetAttribute(grouped_mx_gemm_kernel<kStages>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  grouped_mx_gemm_kernel<NMAT, STAGES><<<num_sms, 192, C::kSmem, s>>>(w, w_sh, act, a);
+  grouped_mx_gemm_kernel<kStages><<<num_sms, kThreads, C::kSmem, s>>>(w, w_sh, act, act_small, a);
   return cudaGetLastError();
 }
-
-constexpr int kStagesGateUp = 5;
-constexpr int kStagesDown = 8;
 
 }  // namespace
 
 cudaError_t launch_gemm_gate_up(const CUtensorMap& w_routed, const CUtensorMap& w_shared, const uint8_t* sf_routed,
-                                const uint8_t* sf_shared, const CUtensorMap& act, const uint8_t* act_sf,
-                                const RowTile* tiles, const int32_t* n_tiles, int max_tiles, int E, int d, int f,
-                                float limit, uint8_t* h_q, uint8_t* h_sf, int* status, uint64_t wait_budget_ns,
-                                int stall_loads, int num_sms, cudaStream_t s) {
+                                const uint8_t* sf_shared, const CUtensorMap& act, const CUtensorMap& act_small,
+                                const uint8_t* act_sf, const RowTile* tiles, const int32_t* n_tiles, int max_tiles,
+                                int E, int d, int f, float limit, uint8_t* h_q, uint8_t* h_sf, int* status,
+                                uint64_t wait_budget_ns, int stall_loads, int num_sms, cudaStream_t s) {
   GemmArgs a{};
   a.sf_routed = sf_routed;
   a.sf_shared = sf_shared ? sf_shared : sf_routed;
@@ -335,24 +346,23 @@ cudaError_t launch_gemm_gate_up(const CUtensorMap& w_routed, const CUtensorMap& 
   a.max_tiles = max_tiles;
   a.E = E;
   a.KG = d / kKGroup;
-  a.m_tiles = f / kMmaM;
-  a.rows_per_expert = 2 * f;
-  a.up_row_offset = f;
-  a.w_mblocks = 2 * f / kMmaM;
+  a.m_tiles = f / kKGroup;
+  a.gate_up = 1;
   a.limit = limit;
   a.h_q = h_q;
   a.h_sf = h_sf;
   a.f = f;
+  a.d = d;
   a.status = status;
   a.budget_ns = wait_budget_ns;
   a.stall_loads = stall_loads;
-  return launch_grouped<2, kStagesGateUp>(w_routed, w_shared, act, a, num_sms, s);
+  return launch_grouped(w_routed, w_shared, act, act_small, a, num_sms, s);
 }
 
 cudaError_t launch_gemm_down(const CUtensorMap& w_routed, const CUtensorMap& w_shared, const uint8_t* sf_routed,
-                             const uint8_t* sf_shared, const CUtensorMap& act, const uint8_t* act_sf,
-                             const RowTile* tiles, const int32_t* n_tiles, int max_tiles, int E, int d, int f,
-                             const float* row_w, float* y_f32, __nv_bfloat16* y_bf16, int* status,
+                             const uint8_t* sf_shared, const CUtensorMap& act, const CUtensorMap& act_small,
+                             const uint8_t* act_sf, const RowTile* tiles, const int32_t* n_tiles, int max_tiles, int E,
+                             int d, int f, const float* row_w, float* y_f32, __nv_bfloat16* y_bf16, int* status,
                              uint64_t wait_budget_ns, int stall_loads, int num_sms, cudaStream_t s) {
   GemmArgs a{};
   a.sf_routed = sf_routed;
@@ -363,18 +373,17 @@ cudaError_t launch_gemm_down(const CUtensorMap& w_routed, const CUtensorMap& w_s
   a.max_tiles = max_tiles;
   a.E = E;
   a.KG = f / kKGroup;
-  a.m_tiles = d / kMmaM;
-  a.rows_per_expert = d;
-  a.up_row_offset = 0;
-  a.w_mblocks = d / kMmaM;
+  a.m_tiles = d / kN;
+  a.gate_up = 0;
   a.row_w = row_w;
   a.y_f32 = y_f32;
   a.y_bf16 = y_bf16;
   a.d = d;
+  a.f = f;
   a.status = status;
   a.budget_ns = wait_budget_ns;
   a.stall_loads = stall_loads;
-  return launch_grouped<1, kStagesDown>(w_routed, w_shared, act, a, num_sms, s);
+  return launch_grouped(w_routed, w_shared, act, act_small, a, num_sms, s);
 }
 
 }  // namespace moe

@@ -23,9 +23,9 @@
  *     returned status covers host-side argument checks and launch errors only.  Conditions found on
  *     the device (an out-of-range expert or token id, a bounded wait that ran out) are recorded in a
  *     sticky per-handle status word and reported by moe_check().
- *   - No call allocates device memory except moe_experts_create (its scale-factor copy); per-call
+ *   - No call allocates device memory except moe_experts_create (its copy of the weights); per-call
  *     scratch lives in a caller-provided workspace (moe_workspace_size / moe_set_workspace).
- *   - Shapes: d_model and d_ff multiples of 128; n_experts in [1, 1024]; top_k in [1, min(16,
+ *   - Shapes: d_model a multiple of 256, d_ff of 128; n_experts in [1, 1024]; top_k in [1, min(16,
  *     n_experts)]; n_experts <= 512 for the learned router (hash routing has no such limit).
  *   - Nothing is thread-safe per handle: calls on one handle must be ordered by the caller (one
  *     stream, or explicit events).  Two handles may be used concurrently.
@@ -59,7 +59,7 @@ typedef enum {
 } moe_status_t;
 
 typedef struct {
-  int32_t d_model;    /* hidden size d (4096 in the pages' model) */
+  int32_t d_model;    /* hidden size d (4096 in the pages' model), a multiple of 256 */
   int32_t d_ff;       /* expert FFN width f (2048) */
   int32_t n_experts;  /* routed experts E (256); 1 for a shared-expert handle */
   int32_t top_k;      /* experts per token k (6) */
@@ -83,11 +83,10 @@ typedef struct {
  *                                    exponent bits 2..1, mantissa bit 0;
  *   w13_e8m0 [n, 2*d_ff, d_model/32] one E8M0 scale byte (2^(b-127)) per 32 consecutive elements;
  *   w2_fp4  [n, d_model, d_ff/2], w2_e8m0 [n, d_model, d_ff/32]  the down projection (w2).
- * The FP4 code buffers are BORROWED: they must stay alive and unchanged until
- * moe_experts_destroy (the kernels stream them directly; 32-byte alignment required).  The scale
- * bytes are copied into a handle-owned, kernel-ordered buffer (enqueued on `stream`; the scale
- * inputs may be released once `stream` has passed this call).  A routed set uses
- * n = cfg->n_experts; a shared expert is a set with n = 1.
+ * The handle copies codes and scales into its own device buffers in a tile-contiguous order (every
+ * 16 KB block the GEMMs stream is contiguous in HBM); the copy is enqueued on `stream`, so the
+ * inputs may be released once `stream` has passed this call.  Code buffers 16-byte aligned, scale
+ * buffers 4-byte aligned.  A routed set uses n = cfg->n_experts; a shared expert is a set with n = 1.
  * Errors: MOE_ERR_INVALID_ARG (null / misaligned / n < 1), MOE_ERR_UNSUPPORTED (shape or GPU),
  * MOE_ERR_CUDA.  *out is NULL on error.
  */

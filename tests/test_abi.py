@@ -45,11 +45,12 @@ def test_host_side_validation_without_gpu(libmoe):
     assert L.moe_experts_create(ctypes.byref(cfg), 0, None, None, None, None, None, ctypes.byref(h)) == 1
     assert b"expert count" in L.moe_last_error()
     assert L.moe_experts_create(ctypes.byref(cfg), 256, None, None, None, None, None, ctypes.byref(h)) == 1
-    misaligned = ctypes.c_void_p(4096 + 16)
+    misaligned = ctypes.c_void_p(4096 + 8)
     ok_ptr = ctypes.c_void_p(4096)
     assert L.moe_experts_create(ctypes.byref(cfg), 256, misaligned, ok_ptr, ok_ptr, ok_ptr, None, ctypes.byref(h)) == 1
-    assert b"32-byte" in L.moe_last_error()
-    for bad in (libmoe.make_config(4000, 2048, 256, 6), libmoe.make_config(4096, 2048, 256, 17),
+    assert b"16-byte" in L.moe_last_error()
+    for bad in (libmoe.make_config(4000, 2048, 256, 6), libmoe.make_config(4096 + 128, 2048, 256, 6),
+                libmoe.make_config(4096, 2048, 256, 17),
                 libmoe.make_config(4096, 2048, 4, 6), libmoe.make_config(4096, 100, 256, 6)):
         assert L.moe_experts_create(ctypes.byref(bad), 1, ok_ptr, ok_ptr, ok_ptr, ok_ptr, None, ctypes.byref(h)) == 2
         assert libmoe.moe_workspace_size(bad, 512) == 0
