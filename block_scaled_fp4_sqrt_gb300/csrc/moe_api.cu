@@ -93,6 +93,21 @@ moe_status_t make_map(CUtensorMap* m, const void* base, bool fp4, uint64_t K, ui
   return MOE_OK;
 }
 
+// bf16 K-major map: inner dimension K, outer `rows`, box {64 elements (128 B), box_rows}, 128-byte swizzle.
+moe_status_t make_map_bf16(CUtensorMap* m, const void* base, uint64_t K, uint64_t rows, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  cuuint64_t gdim[2] = {K, rows};
+  cuuint64_t gstride[1] = {K * 2};
+  cuuint32_t box[2] = {64u, box_rows};
+  cuuint32_t estr[2] = {1u, 1u};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), gdim, gstride, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled (bf16) failed (%d)", (int)r);
+  return MOE_OK;
+}
+
 moe_status_t check_cfg(const moe_config_t* c) {
   if (!c) return fail(MOE_ERR_INVALID_ARG, "config is NULL");
   if (c->d_model <= 0 || c->d_ff <= 0 || c->d_model % 256 || c->d_ff % 128)
@@ -110,13 +125,13 @@ moe_status_t check_cfg(const moe_config_t* c) {
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-int max_ksplit_rows(int max_T, int E, int d) {
-  // largest ksplit * T over 1 <= T <= max_T, for the router partial sums: ksplit only changes with
-  // ceil(T / 64), so each 64-row bucket peaks at its last T
+int max_split_rows(int max_T, int E, int d) {
+  // largest split * T over 1 <= T <= max_T, for the router partial sums: the split only changes with
+  // ceil(T / 128), so each 128-row bucket peaks at its last T
   int best = 0;
-  for (int b = 1; (b - 1) * 64 < max_T; ++b) {
-    const int T = std::min(64 * b, max_T);
-    best = std::max(best, router_ksplit(T, E, d) * T);
+  for (int b = 1; (b - 1) * 128 < max_T; ++b) {
+    const int T = std::min(128 * b, max_T);
+    best = std::max(best, router_tc_split(T, E, d) * T);
   }
   return best;
 }
@@ -155,7 +170,8 @@ size_t workspace_layout(int max_T, int d, int f, int E, int k, Workspace* ws, vo
   Workspace w{};
   w.topk_ids = (int32_t*)take((size_t)max_T * k * 4);
   w.topk_w = (float*)take((size_t)max_T * k * 4);
-  w.logits = (float*)take((size_t)max_ksplit_rows(max_T, E, d) * E * 4);
+  w.logits = (float*)take((size_t)max_split_rows(max_T, E, d) * E * 4);
+  w.w_split = (__nv_bfloat16*)take((size_t)3 * router_tc_epad(E) * d * 2);
   w.chunk_hist = (int32_t*)take((size_t)dm.n_chunks * dm.G * 4);
   w.counts = (int32_t*)take((size_t)dm.G * 4);
   w.offsets = (int32_t*)take((size_t)(dm.G + 1) * 4);
@@ -320,10 +336,16 @@ static moe_status_t route_into(moe_experts_s* h, const moe_input_t* x, const flo
   if (E > 512) return fail(MOE_ERR_UNSUPPORTED, "the learned router supports up to 512 experts");
   if (!aligned(router_w, 16)) return fail(MOE_ERR_INVALID_ARG, "router_w must be 16-byte aligned");
   if (T == 0) return MOE_OK;
-  const int ks = router_ksplit(T, E, d);
-  MOE_CUDA(launch_router_logits(static_cast<const __nv_bfloat16*>(x->x_bf16), router_w, T, d, E, ks, h->ws.logits, s),
-           "router logits");
-  MOE_CUDA(launch_router_topk(h->ws.logits, ks, router_bias, T, E, k, h->cfg.route_scale, ids, wts, s), "router top-k");
+  CUtensorMap tm_x, tm_w;
+  const int Epad = router_tc_epad(E);
+  moe_status_t st = make_map_bf16(&tm_x, x->x_bf16, (uint64_t)d, (uint64_t)T, 128);
+  if (st == MOE_OK) st = make_map_bf16(&tm_w, h->ws.w_split, (uint64_t)d, (uint64_t)3 * Epad, 256);
+  if (st != MOE_OK) return st;
+  const int split = router_tc_split(T, E, d);
+  MOE_CUDA(launch_split_router(router_w, E, d, h->ws.w_split, s), "router weight split");
+  MOE_CUDA(launch_router_tc(tm_x, tm_w, T, E, d, split, h->ws.logits, h->status, h->budget_ns, s), "router logits");
+  MOE_CUDA(launch_router_topk(h->ws.logits, split, router_bias, T, E, k, h->cfg.route_scale, ids, wts, s),
+           "router top-k");
   return MOE_OK;
 }
 

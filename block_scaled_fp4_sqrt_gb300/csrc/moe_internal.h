@@ -45,7 +45,8 @@ struct Geometry {
 struct Workspace {
   int32_t* topk_ids;    // [T, k]
   float* topk_w;        // [T, k]
-  float* logits;        // [ksplit, T, E] router partial sums
+  float* logits;        // [split, T, E] router partial sums
+  __nv_bfloat16* w_split;  // [3, Epad, d] router weight as hi + mid + lo bf16
   int32_t* chunk_hist;  // [n_chunks, G]
   int32_t* counts;      // [G]
   int32_t* offsets;     // [G + 1]
@@ -72,6 +73,12 @@ constexpr int kRouterKSplitMax = 8;
 int router_ksplit(int T, int E, int d);
 cudaError_t launch_router_logits(const __nv_bfloat16* x, const float* w, int T, int d, int E, int ksplit,
                                  float* partial, cudaStream_t s);
+// Tensor-core router: split count for T rows, padded expert count, weight split, logits partials.
+int router_tc_split(int T, int E, int d);
+int router_tc_epad(int E);
+cudaError_t launch_split_router(const float* w, int E, int d, __nv_bfloat16* out, cudaStream_t s);
+cudaError_t launch_router_tc(const CUtensorMap& tm_x, const CUtensorMap& tm_w, int T, int E, int d, int split,
+                             float* partial, int* status, uint64_t budget_ns, cudaStream_t s);
 cudaError_t launch_router_topk(const float* partial, int ksplit, const float* bias, int T, int E, int k,
                                float route_scale, int32_t* ids, float* wts, cudaStream_t s);
 cudaError_t launch_hash_route(const int32_t* tok, const int32_t* table, int V, int T, int E, int k, float route_scale,

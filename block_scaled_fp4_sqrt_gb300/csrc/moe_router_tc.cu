@@ -1,0 +1,223 @@
+// Router logits on the tensor cores: l = x . Wr^T with x bf16 [T, d] and Wr fp32 [E, d].
+//
+// x is exactly bf16 and each fp32 weight splits exactly into three bf16 terms, w = hi + mid + lo
+// (hi = bf16(w), mid = bf16(w - hi), lo = bf16(w - hi - mid) cover its 24-bit significand), so three
+// bf16 x bf16 MMAs per K step, accumulated in fp32 in tensor memory, give the fp32 logits the
+// sqrt-softplus router needs (TensorSharp page, "How TensorSharp runs it") at tensor-core rate.  Each
+// CTA computes a 128-token x 256-expert tile over one K slice and writes fp32 partial sums
+// [split, T, E]; the top-k kernel adds the splits in a fixed order.
+#include <algorithm>
+
+#include "moe_device.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int kRM = 128;       // tokens per tile
+constexpr int kRN = 256;       // experts per tile
+constexpr int kRK = 64;        // bf16 elements per stage (one 128-byte swizzle row)
+constexpr int kRStages = 2;
+constexpr int kRATile = kRM * 128;       // 16 KB
+constexpr int kRBTile = kRN * 128;       // 32 KB per split
+constexpr int kRStage = kRATile + 3 * kRBTile;
+constexpr int kRSmem = kRStages * kRStage + 1024 + 64;
+static_assert(kRSmem <= 232448, "router shared memory");
+
+// kind::f16 instruction descriptor: D fp32, A and B bf16, both K-major.
+__host__ __device__ constexpr uint32_t bf16_idesc(uint32_t M, uint32_t N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+
+__device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Wr fp32 [E, d] -> three bf16 matrices [3, Epad, d] (rows E .. Epad-1 zero).
+__global__ void split_router_kernel(const float* __restrict__ w, int E, int Epad, int d,
+                                    __nv_bfloat16* __restrict__ out) {
+  const size_t total = (size_t)Epad * d;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
+    const int e = (int)(i / d);
+    const float v = e < E ? w[i] : 0.f;
+    const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+    const float r1 = v - __bfloat162float(hi);
+    const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+    const __nv_bfloat16 lo = __float2bfloat16_rn(r1 - __bfloat162float(mid));
+    out[i] = hi;
+    out[total + i] = mid;
+    out[2 * total + i] = lo;
+  }
+}
+
+struct RouterArgs {
+  float* partial;  // [split, T, E]
+  int T, E, Epad, d;
+  int k_per_split;  // multiple of kRK
+  int* status;
+  uint64_t budget_ns;
+};
+
+// grid (ceil(T / 128), Epad / 256, split); warps: 0 TMA, 1 MMA, 2..5 epilogue
+__global__ void __launch_bounds__(192, 1) router_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
+                                                           const __grid_constant__ CUtensorMap tm_w,
+                                                           const RouterArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kRStages * kRStage);
+  uint64_t* empty = full + kRStages;
+  uint64_t* acc_full = empty + kRStages;
+  __shared__ uint32_t tmem_slot;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t0 = blockIdx.x * kRM, e0 = blockIdx.y * kRN, z = blockIdx.z;
+  const int k0 = z * a.k_per_split, n_stages = a.k_per_split / kRK;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kRStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(acc_full, 1);
+    mbar_fence_init();
+  }
+  if (warp == 0) {
+    prefetch_tensormap(&tm_x);
+    prefetch_tensormap(&tm_w);
+  }
+  if (warp == 1) tmem_alloc(&tmem_slot, 256);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = tmem_slot;
+  bool acc_ok = true;
+
+  if (warp == 0 && lane == 0) {
+    const uint64_t pol = l2_policy_evict_last();
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t issued = 0, last_par = 0;
+    bool ok = true;
+    for (int s = 0; s < n_stages; ++s) {
+      if (!mbar_wait(&empty[stage], phase ^ 1u, a.budget_ns)) {
+        ok = false;
+        break;
+      }
+      uint8_t* st = smem + stage * kRStage;
+      mbar_arrive_expect_tx(&full[stage], kRStage);
+      const int kk = k0 + s * kRK;
+      tma_load_2d(st, &tm_x, kk, t0, &full[stage], pol);
+      for (int p = 0; p < 3; ++p) tma_load_2d(st + kRATile + p * kRBTile, &tm_w, kk, p * a.Epad + e0, &full[stage], pol);
+      issued |= 1u << stage;
+      last_par = (last_par & ~(1u << stage)) | (phase << stage);
+      if (++stage == kRStages) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+    if (!ok) {
+      set_status(a.status, DEV_TIMEOUT);
+      for (int s = 0; s < kRStages; ++s)
+        if ((issued >> s) & 1u) (void)mbar_wait(&full[s], (last_par >> s) & 1u, 20000000ull);
+    }
+  } else if (warp == 1 && lane == 0) {
+    constexpr uint32_t idesc = bf16_idesc(kRM, kRN);
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int s = 0; s < n_stages; ++s) {
+      if (!mbar_wait(&full[stage], phase, a.budget_ns)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint8_t* st = smem + stage * kRStage;
+      const uint32_t a_addr = smem_addr(st);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const uint64_t ad = smem_desc(a_addr + k * 32, 16, 1024, 2);
+#pragma unroll
+        for (int p = 0; p < 3; ++p)
+          tc_mma_bf16(tbase, ad, smem_desc(smem_addr(st + kRATile + p * kRBTile) + k * 32, 16, 1024, 2), idesc,
+                      (s | k | p) ? 1u : 0u);
+      }
+      tc_commit(&empty[stage]);
+      if (++stage == kRStages) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+    if (!ok) set_status(a.status, DEV_TIMEOUT);
+    tc_commit(acc_full);  // also retires every MMA issued so far
+  } else if (warp >= 2) {
+    const int q = warp & 3;
+    acc_ok = mbar_wait(acc_full, 0, a.budget_ns);
+    acc_ok = __all_sync(0xFFFFFFFFu, acc_ok);
+    tc_fence_after();
+    if (!acc_ok) {
+      if (lane == 0) set_status(a.status, DEV_TIMEOUT);
+    } else if (t0 + q * 32 < a.T) {
+      const int t = t0 + q * 32 + lane;
+      const uint32_t tl = tbase + ((uint32_t)(q * 32) << 16);
+      for (int c = 0; c < kRN / 32; ++c) {
+        if (e0 + c * 32 >= a.E) break;
+        float v[32];
+        tmem_ld32(tl + (uint32_t)(c * 32), v);
+        if (t < a.T) {
+          float* dst = a.partial + ((size_t)z * a.T + t) * a.E + e0 + c * 32;
+          if (e0 + c * 32 + 32 <= a.E && (a.E & 3) == 0) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              reinterpret_cast<float4*>(dst)[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (e0 + c * 32 + i < a.E) dst[i] = v[i];
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tbase, 256);
+}
+
+}  // namespace
+
+int router_tc_split(int T, int E, int d) {
+  const int mt = (T + kRM - 1) / kRM, nt = (E + kRN - 1) / kRN;
+  int s = 1;
+  while (s < 32 && mt * nt * s * 2 <= 152 && (d / kRK) % (s * 2) == 0) s *= 2;
+  return s;
+}
+
+int router_tc_epad(int E) { return (E + kRN - 1) / kRN * kRN; }
+
+cudaError_t launch_split_router(const float* w, int E, int d, __nv_bfloat16* out, cudaStream_t s) {
+  const int Epad = router_tc_epad(E);
+  const size_t total = (size_t)Epad * d;
+  const int blocks = (int)std::min<size_t>((total + 255) / 256, 152 * 8);
+  split_router_kernel<<<blocks, 256, 0, s>>>(w, E, Epad, d, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_router_tc(const CUtensorMap& tm_x, const CUtensorMap& tm_w, int T, int E, int d, int split,
+                             float* partial, int* status, uint64_t budget_ns, cudaStream_t s) {
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(router_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kRSmem);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  RouterArgs a{partial, T, E, router_tc_epad(E), d, d / split, status, budget_ns};
+  dim3 grid((T + kRM - 1) / kRM, a.Epad / kRN, split);
+  router_tc_kernel<<<grid, 192, kRSmem, s>>>(tm_x, tm_w, a);
+  return cudaGetLastError();
+}
+
+}  // namespace moe
