@@ -18,10 +18,10 @@ using namespace moe;
 struct moe_experts_s {
   moe_config_t cfg;
   int n = 0;                // experts in this set
-  uint8_t* w13 = nullptr;   // owned: packed gate-up codes [n, f/128, d/128, 256, 64]
-  uint8_t* w2 = nullptr;    // owned: packed down codes [n, d/256, f/128, 256, 64]
-  uint8_t* sf13 = nullptr;  // owned: scale atoms [n, f/128, d/128, 2, 512]
-  uint8_t* sf2 = nullptr;   // owned: [n, d/256, f/128, 2, 512]
+  uint8_t* w13 = nullptr;   // owned: packed gate-up codes [n, d/128, f/128, 256, 64]
+  uint8_t* w2 = nullptr;    // owned: packed down codes [n, f/128, d/256, 256, 64]
+  uint8_t* sf13 = nullptr;  // owned: scale atoms [n, d/128, f/128, 2, 512]
+  uint8_t* sf2 = nullptr;   // owned: [n, f/128, d/256, 2, 512]
   CUtensorMap tm13;
   CUtensorMap tm2;
   const int32_t* hash_table = nullptr;
@@ -148,7 +148,7 @@ Dims dims_for(int max_T, int E, int k) {
   dm.rows = max_T * (k + 1);
   dm.G = E + 1;
   dm.n_chunks = (max_T + 31) / 32;
-  dm.max_tiles = (dm.rows + kTileRows - 1) / kTileRows + dm.G;
+  dm.max_tiles = (dm.rows + kSmallTileRows - 1) / kSmallTileRows + dm.G;  // the short tile shape needs most
   return dm;
 }
 
@@ -393,9 +393,15 @@ static void mark_stage(const moe_experts_s* h, int i, cudaStream_t s) {
   if (h->stage_events) cudaEventRecord(static_cast<cudaEvent_t>(h->stage_events[i]), s);
 }
 
+// Row-tile height for a call: verify batches (at most ~16 rows per expert on average) use 32-row tiles,
+// whose short activation slots leave room for a deeper pipeline; larger batches use 128-row tiles.
+static int tile_rows_for(int rows, int groups) {
+  return rows <= 16 * groups ? kSmallTileRows : kTileRows;
+}
+
 static moe_status_t run_ffn(moe_experts_s* h, moe_experts_s* sh, int rows, int E_groups_shared_index,
                             const uint8_t* a_q, const uint8_t* a_sf_atoms, const float* row_w, float* y_f32,
-                            __nv_bfloat16* y_bf16, int max_tiles, bool timed, cudaStream_t s) {
+                            __nv_bfloat16* y_bf16, int max_tiles, int tile_rows, bool timed, cudaStream_t s) {
   const int d = h->cfg.d_model, f = h->cfg.d_ff;
   CUtensorMap tm_a, tm_a32, tm_h, tm_h32;
   moe_status_t st = make_map(&tm_a, a_q, false, (uint64_t)d, (uint64_t)rows, kTileRows);
@@ -406,12 +412,12 @@ static moe_status_t run_ffn(moe_experts_s* h, moe_experts_s* sh, int rows, int E
   const moe_experts_s* shx = sh ? sh : h;
   MOE_CUDA(launch_gemm_gate_up(h->tm13, shx->tm13, h->sf13, shx->sf13, tm_a, tm_a32, a_sf_atoms, h->ws.tiles, h->ws.n_tiles,
                                max_tiles, E_groups_shared_index, d, f, h->cfg.swiglu_limit, h->ws.h_q, h->ws.h_sf,
-                               h->status, h->budget_ns, h->stall_loads, h->num_sms, s),
+                               h->status, h->budget_ns, h->stall_loads, tile_rows, h->num_sms, s),
            "gate-up GEMM");
   if (timed) mark_stage(h, 3, s);
   MOE_CUDA(launch_gemm_down(h->tm2, shx->tm2, h->sf2, shx->sf2, tm_h, tm_h32, h->ws.h_sf, h->ws.tiles, h->ws.n_tiles, max_tiles,
                             E_groups_shared_index, d, f, row_w, y_f32, y_bf16, h->status, h->budget_ns,
-                            h->stall_loads, h->num_sms, s),
+                            h->stall_loads, tile_rows, h->num_sms, s),
            "down GEMM");
   return MOE_OK;
 }
@@ -429,13 +435,15 @@ moe_status_t moe_expert_ffn(moe_experts_t h, int32_t n_rows, const int32_t* offs
   if (!aligned(a_q, 16) || !aligned(a_s, 4) || !aligned(y_bf16, 16))
     return fail(MOE_ERR_INVALID_ARG, "a_q and y must be 16-byte aligned, a_s 4-byte aligned");
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  MOE_CUDA(launch_tiles_from_offsets(offsets, offsets ? h->n : 1, n_rows, kTileRows, dm.max_tiles, h->ws.tile_off,
+  const int groups = offsets ? h->n : 1;
+  const int bn = tile_rows_for(n_rows, groups);
+  MOE_CUDA(launch_tiles_from_offsets(offsets, groups, n_rows, bn, dm.max_tiles, h->ws.tile_off,
                                      h->ws.n_tiles, h->ws.tiles, h->status, s),
            "tile list");
   MOE_CUDA(launch_rows_sf_to_atoms(a_s, h->ws.tiles, h->ws.n_tiles, h->cfg.d_model, dm.max_tiles, h->ws.a_sf, s),
            "scale atoms");
   return run_ffn(h, nullptr, n_rows, h->n, a_q, h->ws.a_sf, row_w, nullptr, static_cast<__nv_bfloat16*>(y_bf16),
-                 dm.max_tiles, false, s);
+                 dm.max_tiles, bn, false, s);
 }
 
 moe_status_t moe_set_stage_events(moe_experts_t h, void* const* events, int32_t n) {
@@ -477,16 +485,17 @@ moe_status_t moe_forward(const moe_input_t* x, const float* router_w, const floa
   const int rows = R + (has_shared ? T : 0);
   const Dims dm = dims_for(h->ws_max_T, E, k);
   const int n_chunks = (T + 31) / 32;
+  const int bn = tile_rows_for(R, E);
   MOE_CUDA(launch_histogram(h->ws.topk_ids, T, k, E, G, h->ws.chunk_hist, h->status, s), "histogram");
-  MOE_CUDA(launch_scan(h->ws.chunk_hist, n_chunks, T, E, G, has_shared, kTileRows, dm.max_tiles, h->ws.counts,
+  MOE_CUDA(launch_scan(h->ws.chunk_hist, n_chunks, T, E, G, has_shared, bn, dm.max_tiles, h->ws.counts,
                        h->ws.offsets, h->ws.tile_off, h->ws.n_tiles, h->ws.tiles, h->status, s),
            "scan");
   MOE_CUDA(launch_gather(static_cast<const __nv_bfloat16*>(x->x_bf16), h->ws.topk_ids, h->ws.topk_w, h->ws.chunk_hist,
-                         h->ws.offsets, h->ws.tile_off, T, d, k, E, G, has_shared, kTileRows, h->ws.a_q, h->ws.a_sf,
+                         h->ws.offsets, h->ws.tile_off, T, d, k, E, G, has_shared, bn, h->ws.a_q, h->ws.a_sf,
                          nullptr, h->ws.perm_tok, h->ws.inv_pos, h->ws.row_w, s),
            "gather");
   mark_stage(h, 2, s);
-  st = run_ffn(h, sh, rows, E, h->ws.a_q, h->ws.a_sf, h->ws.row_w, h->ws.y_rows, nullptr, dm.max_tiles, true, s);
+  st = run_ffn(h, sh, rows, E, h->ws.a_q, h->ws.a_sf, h->ws.row_w, h->ws.y_rows, nullptr, dm.max_tiles, bn, true, s);
   if (st != MOE_OK) return st;
   mark_stage(h, 4, s);
   MOE_CUDA(launch_combine(h->ws.y_rows, h->ws.inv_pos, T, d, k, R, has_shared, static_cast<__nv_bfloat16*>(out_bf16), s),

@@ -16,6 +16,12 @@
 // The weights are stored tile-contiguous (see moe_api.cu), so every pipeline stage is one contiguous
 // 16 KB TMA box.
 //
+// Two shapes of the pipeline: row tiles of up to 128 token rows with 4 stages, and -- for verify
+// batches, whose expert groups hold a handful of rows -- row tiles of up to 32 rows whose activation
+// slots are only 32 rows high, which leaves room for 6 stages.  The MMA still has M = 128: its rows
+// 32..127 then read the following slots, whose products land in accumulator rows nobody stores (the
+// activation ring sits in front of the weight ring, so those reads stay inside the CTA's smem).
+//
 // One persistent CTA per SM walks a device-built list of (row tile, output tile) work items.  Warp 0
 // issues TMA loads, warp 1 the tcgen05 scale copies and MMAs, warps 2..17 drain the accumulator:
 // four warps per 32-lane TMEM quadrant, each owning a quarter of the 256 columns, so one thread holds
@@ -33,26 +39,29 @@ constexpr int kSmallRows = 32;  // groups this small load a 32-row activation bo
 constexpr int kEpiWarps = 16;
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 
-template <int STAGES>
+template <int STAGES, int AROWS>
 struct Cfg {
-  static constexpr int kATile = kBM * 128;           // 128 token rows x 128 FP8
-  static constexpr int kBTile = kN * 128;            // 256 weight rows x 128 FP4, padded to bytes
-  static constexpr int kSfBytes = 3 * kSfAtomBytes;  // activation atom + two weight atoms
-  static constexpr int kStageRaw = kATile + kBTile + kSfBytes;
-  static constexpr int kStage = (kStageRaw + 1023) / 1024 * 1024;
+  static constexpr int kASlot = AROWS * 128;         // activation rows x 128 FP8
+  static constexpr int kBSlot = kN * 128;            // 256 weight rows x 128 FP4, padded to bytes
+  static constexpr int kSfSlot = 3 * kSfAtomBytes;   // activation atom + two weight atoms
+  static constexpr int kAOff = 0;                    // [activation ring | weight ring | scale ring]
+  static constexpr int kBOff = STAGES * kASlot;
+  static constexpr int kSfOff = kBOff + STAGES * kBSlot;
   static constexpr int kBarBytes = (2 * STAGES + 3) * 8;
-  static constexpr int kSmem = STAGES * kStage + 1024 + kBarBytes;
+  static constexpr int kSmem = kSfOff + STAGES * kSfSlot + 1024 + kBarBytes;
   static constexpr uint32_t kTxB = kN * 64 + 2 * kSfAtomBytes;  // packed FP4 box (64 B per row) + weight atoms
   static constexpr int kAccCols = kN;                           // one fp32 accumulator [128 x 256]
   static constexpr int kSfCols = 12;                            // per stage: A atom 4 columns, B atoms 8
   static constexpr int kTmemCols = 512;
+  static_assert(kBOff % 1024 == 0 && kSfOff % 1024 == 0, "swizzled tiles need 1024-byte alignment");
+  static_assert(AROWS == kBM || kBOff >= (kBM - AROWS) * 128, "M = 128 reads past a short activation slot");
   static_assert(kAccCols + STAGES * kSfCols <= kTmemCols, "TMEM budget");
-  static_assert(kSmem <= 232448, "shared memory budget");
+  static_assert(kSmem <= 232448 - 64, "shared memory budget");
 };
 
 struct GemmArgs {
-  const uint8_t* sf_routed;  // weight scale atoms [E, m_tiles, KG, 2, 512]
-  const uint8_t* sf_shared;  // [1, m_tiles, KG, 2, 512]
+  const uint8_t* sf_routed;  // weight scale atoms [E, KG, m_tiles, 2, 512]
+  const uint8_t* sf_shared;  // [1, KG, m_tiles, 2, 512]
   const uint8_t* act_sf;     // activation scale atoms [tile, KG, 512]
   const RowTile* tiles;
   const int32_t* n_tiles;
@@ -78,15 +87,15 @@ struct GemmArgs {
 
 __device__ __forceinline__ float silu_f(float z) { return z / (1.0f + expf(-z)); }
 
-template <int STAGES>
+template <int STAGES, int AROWS>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_mx_gemm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_w_shared,
                            const __grid_constant__ CUtensorMap tm_act, const __grid_constant__ CUtensorMap tm_act_small,
                            const GemmArgs a) {
-  using C = Cfg<STAGES>;
+  using C = Cfg<STAGES, AROWS>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * C::kStage);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kSfOff + STAGES * C::kSfSlot);
   uint64_t* empty = full + STAGES;
   uint64_t* acc_full = empty + STAGES;
   uint64_t* acc_empty = acc_full + 1;
@@ -137,25 +146,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool sh = rt.group == a.E;
         const CUtensorMap* tw = sh ? &tm_w_shared : &tm_w;
         const int e = sh ? 0 : rt.group;
-        const bool small = rt.nrows <= kSmallRows;
+        const bool small = AROWS == kSmallRows || rt.nrows <= kSmallRows;
         const CUtensorMap* ta = small ? &tm_act_small : &tm_act;
         const uint32_t tx = C::kTxB + (small ? kSmallRows : kBM) * 128 + kSfAtomBytes;
-        const int wrow0 = (e * a.m_tiles + mt) * a.KG * kN;  // first packed row of this output tile
-        const uint8_t* sfw =
-            (sh ? a.sf_shared : a.sf_routed) + ((size_t)e * a.m_tiles + mt) * a.KG * 2 * kSfAtomBytes;
+        // packed weights are [expert][K group][output tile][256 rows]: slab (e, kg, mt)
+        const int wrow0 = (e * a.KG * a.m_tiles + mt) * kN;
+        const int wrow_kg = a.m_tiles * kN;
+        const uint8_t* sfw = (sh ? a.sf_shared : a.sf_routed) + ((size_t)e * a.KG * a.m_tiles + mt) * 2 * kSfAtomBytes;
+        const size_t sfw_kg = (size_t)a.m_tiles * 2 * kSfAtomBytes;
         const uint8_t* sfa = a.act_sf + (size_t)ti * a.KG * kSfAtomBytes;
         for (int kg = 0; kg < a.KG; ++kg) {
           if (abort_flag || !mbar_wait(&empty[stage], phase ^ 1u, a.budget_ns)) {
             ok = false;
             break;
           }
-          uint8_t* st = smem + stage * C::kStage;
           mbar_arrive_expect_tx(&full[stage], tx);
-          tma_load_2d(st + C::kATile, tw, 0, wrow0 + kg * kN, &full[stage], pol_w);
-          tma_load_2d(st, ta, kg * kKGroup, rt.row0, &full[stage], pol_a);
-          uint8_t* sf = st + C::kATile + C::kBTile;
+          tma_load_2d(smem + C::kBOff + stage * C::kBSlot, tw, 0, wrow0 + kg * wrow_kg, &full[stage], pol_w);
+          tma_load_2d(smem + C::kAOff + stage * C::kASlot, ta, kg * kKGroup, rt.row0, &full[stage], pol_a);
+          uint8_t* sf = smem + C::kSfOff + stage * C::kSfSlot;
           bulk_load(sf, sfa + kg * kSfAtomBytes, kSfAtomBytes, &full[stage]);
-          bulk_load(sf + kSfAtomBytes, sfw + kg * 2 * kSfAtomBytes, 2 * kSfAtomBytes, &full[stage]);
+          bulk_load(sf + kSfAtomBytes, sfw + kg * sfw_kg, 2 * kSfAtomBytes, &full[stage]);
           issued |= 1u << stage;
           last_par = (last_par & ~(1u << stage)) | (phase << stage);
           if (++stage == STAGES) {
@@ -194,13 +204,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          uint8_t* st = smem + stage * C::kStage;
-          const uint8_t* sf = st + C::kATile + C::kBTile;
+          const uint8_t* sf = smem + C::kSfOff + stage * C::kSfSlot;
           const uint32_t sf_t = tbase + (uint32_t)(C::kAccCols + stage * C::kSfCols);
 #pragma unroll
           for (int m = 0; m < 3; ++m)
             tc_copy_sf(sf_t + 4 * m, smem_desc(smem_addr(sf + m * kSfAtomBytes), 128, 128, 0));
-          const uint32_t a_addr = smem_addr(st), b_addr = smem_addr(st + C::kATile);
+          const uint32_t a_addr = smem_addr(smem + C::kAOff + stage * C::kASlot);
+          const uint32_t b_addr = smem_addr(smem + C::kBOff + stage * C::kBSlot);
 #pragma unroll
           for (int k = 0; k < 4; ++k)
             tc_mma_mx(tbase, smem_desc(a_addr + k * 32, 16, 1024, 2), smem_desc(b_addr + k * 32, 16, 1024, 2),
@@ -314,20 +324,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc(tbase, C::kTmemCols);
 }
 
-constexpr int kStages = 4;
-
-cudaError_t launch_grouped(const CUtensorMap& w, const CUtensorMap& w_sh, const CUtensorMap& act,
-                           const CUtensorMap& act_small, const GemmArgs& a, int num_sms, cudaStream_t s) {
-  using C = Cfg<kStages>;
+template <int STAGES, int AROWS>
+cudaError_t launch_shape(const CUtensorMap& w, const CUtensorMap& w_sh, const CUtensorMap& act,
+                         const CUtensorMap& act_small, const GemmArgs& a, int num_sms, cudaStream_t s) {
+  using C = Cfg<STAGES, AROWS>;
   static bool configured = false;
   if (!configured) {
-    cudaError_t e =
-        cudaFuncSetAttribute(grouped_mx_gemm_kernel<kStages>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+    cudaError_t e = cudaFuncSetAttribute(grouped_mx_gemm_kernel<STAGES, AROWS>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  grouped_mx_gemm_kernel<kStages><<<num_sms, kThreads, C::kSmem, s>>>(w, w_sh, act, act_small, a);
+  grouped_mx_gemm_kernel<STAGES, AROWS><<<num_sms, kThreads, C::kSmem, s>>>(w, w_sh, act, act_small, a);
   return cudaGetLastError();
+}
+
+// tile_rows 32: 6 stages of 32-row activation slots; tile_rows 128: 4 stages of 128-row slots.
+cudaError_t launch_grouped(const CUtensorMap& w, const CUtensorMap& w_sh, const CUtensorMap& act,
+                           const CUtensorMap& act_small, const GemmArgs& a, int tile_rows, int num_sms,
+                           cudaStream_t s) {
+  if (tile_rows == kSmallRows) return launch_shape<6, kSmallRows>(w, w_sh, act, act_small, a, num_sms, s);
+  return launch_shape<4, kBM>(w, w_sh, act, act_small, a, num_sms, s);
 }
 
 }  // namespace
@@ -336,7 +353,7 @@ cudaError_t launch_gemm_gate_up(const CUtensorMap& w_routed, const CUtensorMap& 
                                 const uint8_t* sf_shared, const CUtensorMap& act, const CUtensorMap& act_small,
                                 const uint8_t* act_sf, const RowTile* tiles, const int32_t* n_tiles, int max_tiles,
                                 int E, int d, int f, float limit, uint8_t* h_q, uint8_t* h_sf, int* status,
-                                uint64_t wait_budget_ns, int stall_loads, int num_sms, cudaStream_t s) {
+                                uint64_t wait_budget_ns, int stall_loads, int tile_rows, int num_sms, cudaStream_t s) {
   GemmArgs a{};
   a.sf_routed = sf_routed;
   a.sf_shared = sf_shared ? sf_shared : sf_routed;
@@ -356,14 +373,14 @@ cudaError_t launch_gemm_gate_up(const CUtensorMap& w_routed, const CUtensorMap& 
   a.status = status;
   a.budget_ns = wait_budget_ns;
   a.stall_loads = stall_loads;
-  return launch_grouped(w_routed, w_shared, act, act_small, a, num_sms, s);
+  return launch_grouped(w_routed, w_shared, act, act_small, a, tile_rows, num_sms, s);
 }
 
 cudaError_t launch_gemm_down(const CUtensorMap& w_routed, const CUtensorMap& w_shared, const uint8_t* sf_routed,
                              const uint8_t* sf_shared, const CUtensorMap& act, const CUtensorMap& act_small,
                              const uint8_t* act_sf, const RowTile* tiles, const int32_t* n_tiles, int max_tiles, int E,
                              int d, int f, const float* row_w, float* y_f32, __nv_bfloat16* y_bf16, int* status,
-                             uint64_t wait_budget_ns, int stall_loads, int num_sms, cudaStream_t s) {
+                             uint64_t wait_budget_ns, int stall_loads, int tile_rows, int num_sms, cudaStream_t s) {
   GemmArgs a{};
   a.sf_routed = sf_routed;
   a.sf_shared = sf_shared ? sf_shared : sf_routed;
@@ -383,7 +400,7 @@ cudaError_t launch_gemm_down(const CUtensorMap& w_routed, const CUtensorMap& w_s
   a.status = status;
   a.budget_ns = wait_budget_ns;
   a.stall_loads = stall_loads;
-  return launch_grouped(w_routed, w_shared, act, act_small, a, num_sms, s);
+  return launch_grouped(w_routed, w_shared, act, act_small, a, tile_rows, num_sms, s);
 }
 
 }  // namespace moe

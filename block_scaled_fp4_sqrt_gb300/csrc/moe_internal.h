@@ -21,6 +21,7 @@ constexpr int kMmaM = 128;         // weight rows per MMA tile (tcgen05 M)
 constexpr int kKGroup = 128;       // K elements per pipeline stage (one 128-byte swizzle row of FP8)
 constexpr int kSfAtomBytes = 512;  // scale-factor atom: 128 rows x 4 K-blocks of 32
 constexpr int kTileRows = 128;     // token rows per row tile (tcgen05 M) in the grouped GEMMs
+constexpr int kSmallTileRows = 32; // row tiles of the verify-batch shape (short activation slots)
 
 // One row tile of the grouped GEMMs: rows [row0, row0 + nrows) of group `group`.
 struct RowTile {
@@ -103,9 +104,9 @@ cudaError_t launch_tiles_from_offsets(const int32_t* offsets, int G, int n_rows,
                                       cudaStream_t s);
 
 // Weight repacking at handle creation.  mode 0: gate-up rows [n, 2f, K] (gate rows 0..f-1, up rows
-// f..2f-1); mode 1: down rows [n, d, K].  Packed codes [n, rows/256, K/128, 256, 64 B]: each 256-row
+// f..2f-1); mode 1: down rows [n, d, K].  Packed codes [n, K/128, rows/256, 256, 64 B]: each 256-row
 // slab is one output tile (mode 0: gate rows 128t.. then up rows 128t..; mode 1: rows 256t..) and one
-// 128-element K group, 16 KB contiguous.  Scale atoms [n, rows/256, K/128, 2, 512] in the same order.
+// 128-element K group, 16 KB contiguous.  Scale atoms [n, K/128, rows/256, 2, 512] in the same order.
 cudaError_t launch_pack_weights(const uint8_t* codes, int n, int rows, int K, int mode, uint8_t* packed,
                                 cudaStream_t s);
 cudaError_t launch_pack_weight_sf(const uint8_t* sc, int n, int rows, int K, int mode, uint8_t* atoms,
@@ -117,13 +118,13 @@ cudaError_t launch_gemm_gate_up(const CUtensorMap& w_routed, const CUtensorMap& 
                                 const RowTile* tiles, const int32_t* n_tiles, int max_tiles, int E, int d, int f,
                                 float limit,
                                 uint8_t* h_q, uint8_t* h_sf, int* status, uint64_t wait_budget_ns, int stall_loads,
-                                int num_sms, cudaStream_t s);
+                                int tile_rows, int num_sms, cudaStream_t s);
 cudaError_t launch_gemm_down(const CUtensorMap& w_routed, const CUtensorMap& w_shared, const uint8_t* sf_routed,
                              const uint8_t* sf_shared, const CUtensorMap& act, const CUtensorMap& act_small,
                              const uint8_t* act_sf,
                              const RowTile* tiles, const int32_t* n_tiles, int max_tiles, int E, int d, int f,
                              const float* row_w, float* y_f32, __nv_bfloat16* y_bf16, int* status,
-                             uint64_t wait_budget_ns, int stall_loads, int num_sms, cudaStream_t s);
+                             uint64_t wait_budget_ns, int stall_loads, int tile_rows, int num_sms, cudaStream_t s);
 
 cudaError_t launch_combine(const float* y_rows, const int32_t* inv_pos, int T, int d, int k, int R,
                            int has_shared, __nv_bfloat16* out, cudaStream_t s);

@@ -92,26 +92,44 @@ constexpr int kMaxTopK = 16;
 
 __device__ __forceinline__ float softplus_f(float l) { return fmaxf(l, 0.f) + log1pf(expf(-fabsf(l))); }
 
-// One warp per token: sum the split partials, score, select the k largest s + bias (ties to the lower
-// expert id), report ids ascending with weights route_scale * s_j / sum_j s_j.
-__global__ void router_topk_kernel(const float* __restrict__ partial, int ksplit, const float* __restrict__ bias,
-                                   int T, int E, int k, float route_scale, int32_t* __restrict__ ids,
-                                   float* __restrict__ wts) {
-  const int lane = threadIdx.x & 31;
-  const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  if (t >= T) return;
+// Block of 8 warps per 8 tokens.  Phase 1: every thread sums the split partials of some (token,
+// expert) pairs in a fixed order (coalesced over experts) and stores s = sqrt(softplus(l)) and
+// s + bias in shared memory.  Phase 2: warp w selects the k largest s + bias of token w (ties to the
+// lower expert id) and reports ids ascending with weights route_scale * s_j / sum_j s_j.
+constexpr int kTopkTokens = 8;
+
+constexpr int kMaxSplit = 32;
+
+__global__ void __launch_bounds__(512) router_topk_kernel(const float* __restrict__ partial, int ksplit,
+                                                          const float* __restrict__ bias, int T, int E, int k,
+                                                          float route_scale, int32_t* __restrict__ ids,
+                                                          float* __restrict__ wts) {
+  __shared__ float s_s[kTopkTokens][32 * kMaxPerLane];
+  __shared__ float s_sel[kTopkTokens][32 * kMaxPerLane];
+  const int t0 = blockIdx.x * kTopkTokens;
+  for (int idx = threadIdx.x; idx < kTopkTokens * E; idx += blockDim.x) {
+    const int i = idx / E, e = idx - i * E;
+    const int t = t0 + i;
+    if (t >= T) continue;
+    // unrolled so the split loads (independent) issue together; the sum runs in split order
+    float l = 0.f;
+#pragma unroll
+    for (int z = 0; z < kMaxSplit; ++z)
+      if (z < ksplit) l += __ldg(&partial[((size_t)z * T + t) * E + e]);
+    const float sv = sqrtf(softplus_f(l));
+    s_s[i][e] = sv;
+    s_sel[i][e] = sv + bias[e];
+  }
+  __syncthreads();
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int t = t0 + w;
+  if (w >= kTopkTokens || t >= T) return;
   float s[kMaxPerLane], sel[kMaxPerLane];
 #pragma unroll
   for (int i = 0; i < kMaxPerLane; ++i) {
-    int e = lane + 32 * i;
-    s[i] = 0.f;
-    sel[i] = -FLT_MAX;
-    if (e < E) {
-      float l = 0.f;
-      for (int z = 0; z < ksplit; ++z) l += partial[((size_t)z * T + t) * E + e];
-      s[i] = sqrtf(softplus_f(l));
-      sel[i] = s[i] + bias[e];
-    }
+    const int e = lane + 32 * i;
+    s[i] = e < E ? s_s[w][e] : 0.f;
+    sel[i] = e < E ? s_sel[w][e] : -FLT_MAX;
   }
   uint32_t taken = 0;
   int chosen[kMaxTopK];
@@ -121,23 +139,32 @@ __global__ void router_topk_kernel(const float* __restrict__ partial, int ksplit
     int be = 0x7FFFFFFF;
 #pragma unroll
     for (int i = 0; i < kMaxPerLane; ++i) {
-      int e = lane + 32 * i;
-      bool ok = e < E && !((taken >> i) & 1u);
-      if (ok && (be == 0x7FFFFFFF || sel[i] > bv)) { bv = sel[i]; be = e; }
+      const int e = lane + 32 * i;
+      const bool ok = e < E && !((taken >> i) & 1u);
+      if (ok && (be == 0x7FFFFFFF || sel[i] > bv)) {
+        bv = sel[i];
+        be = e;
+      }
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
-      float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, off);
-      int oe = __shfl_xor_sync(0xFFFFFFFFu, be, off);
-      bool better = (oe != 0x7FFFFFFF) && (be == 0x7FFFFFFF || ov > bv || (ov == bv && oe < be));
-      if (better) { bv = ov; be = oe; }
+      const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, off);
+      const int oe = __shfl_xor_sync(0xFFFFFFFFu, be, off);
+      const bool better = (oe != 0x7FFFFFFF) && (be == 0x7FFFFFFF || ov > bv || (ov == bv && oe < be));
+      if (better) {
+        bv = ov;
+        be = oe;
+      }
     }
     float sv = 0.f;
     if ((be & 31) == lane) {
-      int i_sel = be >> 5;
+      const int i_sel = be >> 5;
 #pragma unroll
       for (int i = 0; i < kMaxPerLane; ++i)
-        if (i == i_sel) { sv = s[i]; taken |= 1u << i; }
+        if (i == i_sel) {
+          sv = s[i];
+          taken |= 1u << i;
+        }
     }
     sv = __shfl_sync(0xFFFFFFFFu, sv, be & 31);
     chosen[j] = be;
@@ -145,10 +172,14 @@ __global__ void router_topk_kernel(const float* __restrict__ partial, int ksplit
   }
   if (lane == 0) {
     for (int a = 1; a < k; ++a) {  // insertion sort by expert id
-      int ci = chosen[a];
-      float cs = chosen_s[a];
+      const int ci = chosen[a];
+      const float cs = chosen_s[a];
       int b = a - 1;
-      while (b >= 0 && chosen[b] > ci) { chosen[b + 1] = chosen[b]; chosen_s[b + 1] = chosen_s[b]; --b; }
+      while (b >= 0 && chosen[b] > ci) {
+        chosen[b + 1] = chosen[b];
+        chosen_s[b + 1] = chosen_s[b];
+        --b;
+      }
       chosen[b + 1] = ci;
       chosen_s[b + 1] = cs;
     }
@@ -213,9 +244,9 @@ cudaError_t launch_router_logits(const __nv_bfloat16* x, const float* w, int T, 
 
 cudaError_t launch_router_topk(const float* partial, int ksplit, const float* bias, int T, int E, int k,
                                float route_scale, int32_t* ids, float* wts, cudaStream_t s) {
-  int threads = 256;
-  int blocks = (T * 32 + threads - 1) / threads;
-  router_topk_kernel<<<blocks, threads, 0, s>>>(partial, ksplit, bias, T, E, k, route_scale, ids, wts);
+  if (ksplit > kMaxSplit) return cudaErrorInvalidValue;
+  const int blocks = (T + kTopkTokens - 1) / kTopkTokens;
+  router_topk_kernel<<<blocks, 512, 0, s>>>(partial, ksplit, bias, T, E, k, route_scale, ids, wts);
   return cudaGetLastError();
 }
 
