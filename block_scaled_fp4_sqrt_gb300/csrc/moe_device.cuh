@@ -50,13 +50,26 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Wait for the phase with the given parity to complete, for at most budget_ns nanoseconds.
-// Returns false (and the caller reports MOE_DEV_TIMEOUT) when the budget runs out.
+// try_wait with a suspend-time hint: the thread sleeps until the phase completes or the hint runs
+// out, instead of spinning (spinning waiters steal issue slots from the MMA and TMA threads).
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for the phase with the given parity to complete, for at most budget_ns nanoseconds (plus at
+// most one suspend interval).  Returns false (and the caller reports MOE_DEV_TIMEOUT) when the
+// budget runs out.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t budget_ns) {
   if (mbar_test(bar, parity)) return true;
-  uint64_t t0 = globaltimer_ns();
+  const uint64_t t0 = globaltimer_ns();
   for (;;) {
-    if (mbar_test(bar, parity)) return true;
+    if (mbar_try_wait_suspend(bar, parity, 200000u)) return true;
     if (globaltimer_ns() - t0 > budget_ns) return false;
   }
 }
@@ -122,17 +135,10 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
 // Instruction descriptor of kind::mxf8f6f4 with E8M0 block scales.
 // Formats: 0 = E4M3, 5 = E2M1.  M in {128}, N multiple of 16 up to 256.  sf ids pick the byte of
 // the 32-bit scale word (the 32-element K block inside a 128-element group).
-__host__ __device__ __forceinline__ uint32_t mma_idesc(uint32_t a_fmt, uint32_t b_fmt, uint32_t M, uint32_t N,
-                                                       uint32_t a_sf_id, uint32_t b_sf_id) {
-  uint32_t d = 0;
-  d |= (b_sf_id & 3u) << 4;
-  d |= (a_fmt & 7u) << 7;
-  d |= (b_fmt & 7u) << 10;
-  d |= ((N >> 3) & 63u) << 17;
-  d |= 1u << 23;  // scale type UE8M0
-  d |= ((M >> 4) & 31u) << 24;
-  d |= (a_sf_id & 3u) << 29;
-  return d;
+__host__ __device__ __forceinline__ constexpr uint32_t mma_idesc(uint32_t a_fmt, uint32_t b_fmt, uint32_t M,
+                                                                 uint32_t N, uint32_t a_sf_id, uint32_t b_sf_id) {
+  return ((b_sf_id & 3u) << 4) | ((a_fmt & 7u) << 7) | ((b_fmt & 7u) << 10) | (((N >> 3) & 63u) << 17) |
+         (1u << 23) /* scale type UE8M0 */ | (((M >> 4) & 31u) << 24) | ((a_sf_id & 3u) << 29);
 }
 
 __device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
@@ -161,6 +167,38 @@ __device__ __forceinline__ void tc_mma_mx(uint32_t d_tmem, uint64_t a_desc, uint
           d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
       : "memory");
+}
+
+// One pipeline stage of four block-scaled MMAs (K = 4 x 32) fused with the stage's commit and a
+// non-blocking test of another stage's barrier.  The test is issued first and its result is read
+// only after the commit, so the barrier's latency overlaps the MMA issue instead of stalling the
+// issuing thread (which would leave the tensor pipe idle: it queues only a couple of MMAs).  MMA k
+// reads K columns 32k.. of the stage (descriptor address + 2k) and scale byte k (sf id k).
+__device__ __forceinline__ bool tc_stage4_mx_commit_poll(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                                         uint32_t idesc0, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                                         uint32_t accumulate, uint64_t* commit_bar,
+                                                         uint64_t* poll_bar, uint32_t poll_parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p, q, t;\n .reg .b64 a1, a2, a3, b1, b2, b3;\n .reg .b32 i1, i2, i3;\n"
+      " mbarrier.test_wait.parity.shared::cta.b64 q, [%8], %9;\n"
+      " setp.ne.b32 p, %4, 0;\n"
+      " setp.eq.b32 t, 0, 0;\n"
+      " add.s64 a1, %2, 2;\n add.s64 b1, %3, 2;\n"
+      " add.s64 a2, %2, 4;\n add.s64 b2, %3, 4;\n"
+      " add.s64 a3, %2, 6;\n add.s64 b3, %3, 6;\n"
+      " or.b32 i1, %5, 0x20000010;\n or.b32 i2, %5, 0x40000020;\n or.b32 i3, %5, 0x60000030;\n"
+      " tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%1], %2, %3, %5, [%6], [%7], p;\n"
+      " tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%1], a1, b1, i1, [%6], [%7], t;\n"
+      " tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%1], a2, b2, i2, [%6], [%7], t;\n"
+      " tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%1], a3, b3, i3, [%6], [%7], t;\n"
+      " tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%10];\n"
+      " selp.u32 %0, 1, 0, q;\n}\n"
+      : "=r"(ok)
+      : "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(accumulate), "r"(idesc0), "r"(sfa_tmem), "r"(sfb_tmem),
+        "r"(smem_addr(poll_bar)), "r"(poll_parity), "r"(smem_addr(commit_bar))
+      : "memory");
+  return ok != 0;
 }
 
 __device__ __forceinline__ void tc_commit(uint64_t* bar) {

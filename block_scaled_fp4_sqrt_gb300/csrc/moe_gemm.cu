@@ -53,6 +53,8 @@ struct Cfg {
   static constexpr int kAccCols = kN;                           // one fp32 accumulator [128 x 256]
   static constexpr int kSfCols = 12;                            // per stage: A atom 4 columns, B atoms 8
   static constexpr int kTmemCols = 512;
+  // warps that drain the accumulator: with rows only in TMEM lanes 0..31, the four warps of quadrant 0
+  static constexpr int kDrainWarps = AROWS == kSmallRows ? kEpiWarps / 4 : kEpiWarps;
   static_assert(kBOff % 1024 == 0 && kSfOff % 1024 == 0, "swizzled tiles need 1024-byte alignment");
   static_assert(AROWS == kBM || kBOff >= (kBM - AROWS) * 128, "M = 128 reads past a short activation slot");
   static_assert(kAccCols + STAGES * kSfCols <= kTmemCols, "TMEM budget");
@@ -114,7 +116,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&empty[s], 1);
     }
     mbar_init(acc_full, 1);
-    mbar_init(acc_empty, kEpiWarps);
+    mbar_init(acc_empty, C::kDrainWarps);
     mbar_init(drain, 1);
     abort_flag = 0;
     mbar_fence_init();
@@ -185,45 +187,80 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------------------------------------------------------- MMA issuer
-      // A = activations (E4M3), B = weights (E2M1); the sf id picks the 32-element block of the group
-      const uint32_t idesc_k[4] = {mma_idesc(0, 5, kBM, kN, 0, 0), mma_idesc(0, 5, kBM, kN, 1, 1),
-                                   mma_idesc(0, 5, kBM, kN, 2, 2), mma_idesc(0, 5, kBM, kN, 3, 3)};
-      int stage = 0;
-      uint32_t phase = 0;
+      // A = activations (E4M3), B = weights (E2M1).  The tensor pipe queues only a couple of MMAs, so
+      // this thread's instruction stream is on the critical path: descriptors are precomputed,
+      // slots and phases advance incrementally (the same stage sequence as the producer's), and the
+      // stage's four MMAs, its commit and a barrier test are one fused instruction block.  A scale
+      // copy or a barrier wait right in front of the MMAs that depend on it also leaves the pipe idle,
+      // so the scale atoms of a stage are copied into TMEM as soon as the stage is seen to have
+      // landed (tested inside the MMA block of an earlier stage, up to kAhead stages ahead); only a
+      // stage that has not landed by the time its MMAs are due is waited for in front of them.
+      constexpr uint32_t kIdesc0 = mma_idesc(0, 5, kBM, kN, 0, 0);
+      constexpr int kAhead = 2;
+      static_assert(STAGES > kAhead, "scale copies run up to kAhead stages ahead of the MMAs");
+      const uint64_t a_desc0 = smem_desc(smem_addr(smem + C::kAOff), 16, 1024, 2);
+      const uint64_t b_desc0 = smem_desc(smem_addr(smem + C::kBOff), 16, 1024, 2);
+      const uint64_t sf_desc0 = smem_desc(smem_addr(smem + C::kSfOff), 128, 128, 0);
+      const uint32_t sf_tmem0 = tbase + (uint32_t)C::kAccCols;
+      auto copy_sf = [&](int slot) {  // activation atom, then the two weight atoms (512 B apart)
+        const uint64_t dsc = sf_desc0 + (uint64_t)((slot * C::kSfSlot) >> 4);
+        const uint32_t t = sf_tmem0 + (uint32_t)(slot * C::kSfCols);
+        tc_copy_sf(t, dsc);
+        tc_copy_sf(t + 4, dsc + (kSfAtomBytes >> 4));
+        tc_copy_sf(t + 8, dsc + 2 * (kSfAtomBytes >> 4));
+      };
+      const int n_items = total > (int)blockIdx.x ? (total - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
+      const int n_st = n_items * a.KG;
       bool ok = true, any = false;
-      int it = 0;
-      for (int w = blockIdx.x; w < total && ok; w += gridDim.x, ++it) {
-        if (abort_flag || !mbar_wait(acc_empty, ((uint32_t)it & 1u) ^ 1u, a.budget_ns)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        for (int kg = 0; kg < a.KG; ++kg) {
-          if (abort_flag || !mbar_wait(&full[stage], phase, a.budget_ns)) {
-            ok = false;
-            break;
+      int cs = 0;          // slot of the stage being consumed
+      uint32_t cph = 0;    // its phase
+      int lg = 0, ls = 0;  // first stage whose scales are not in TMEM yet, and its slot / phase
+      uint32_t lph = 0;
+      int g = 0;
+      for (int item = 0; item < n_items && ok; ++item) {
+        for (int kg = 0; kg < a.KG; ++kg, ++g) {
+          if (lg == g) {  // this stage has not been seen yet: wait for it
+            if (abort_flag || !mbar_wait(&full[ls], lph, a.budget_ns)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            copy_sf(ls);
+            ++lg;
+            if (++ls == STAGES) {
+              ls = 0;
+              lph ^= 1u;
+            }
           }
-          tc_fence_after();
-          const uint8_t* sf = smem + C::kSfOff + stage * C::kSfSlot;
-          const uint32_t sf_t = tbase + (uint32_t)(C::kAccCols + stage * C::kSfCols);
-#pragma unroll
-          for (int m = 0; m < 3; ++m)
-            tc_copy_sf(sf_t + 4 * m, smem_desc(smem_addr(sf + m * kSfAtomBytes), 128, 128, 0));
-          const uint32_t a_addr = smem_addr(smem + C::kAOff + stage * C::kASlot);
-          const uint32_t b_addr = smem_addr(smem + C::kBOff + stage * C::kBSlot);
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            tc_mma_mx(tbase, smem_desc(a_addr + k * 32, 16, 1024, 2), smem_desc(b_addr + k * 32, 16, 1024, 2),
-                      idesc_k[k], sf_t, sf_t + 4, (kg | k) ? 1u : 0u);
+          if (kg == 0) {  // a new work item: the epilogue must have drained the accumulator
+            if (abort_flag || !mbar_wait(acc_empty, ((uint32_t)item & 1u) ^ 1u, a.budget_ns)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+          }
+          const bool look = lg < n_st && lg <= g + kAhead;
+          // with nothing to look ahead for, the test re-reads this stage's own (completed) barrier
+          const bool landed = tc_stage4_mx_commit_poll(
+              tbase, a_desc0 + (uint64_t)((cs * C::kASlot) >> 4), b_desc0 + (uint64_t)((cs * C::kBSlot) >> 4),
+              kIdesc0, sf_tmem0 + (uint32_t)(cs * C::kSfCols), sf_tmem0 + (uint32_t)(cs * C::kSfCols + 4),
+              kg != 0 ? 1u : 0u, &empty[cs], look ? &full[ls] : &full[cs], look ? lph : cph);
           any = true;
-          tc_commit(&empty[stage]);
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
+          if (kg == a.KG - 1) tc_commit(acc_full);
+          if (look && landed) {
+            tc_fence_after();
+            copy_sf(ls);
+            ++lg;
+            if (++ls == STAGES) {
+              ls = 0;
+              lph ^= 1u;
+            }
+          }
+          if (++cs == STAGES) {
+            cs = 0;
+            cph ^= 1u;
           }
         }
-        if (!ok) break;
-        tc_commit(acc_full);
       }
       if (!ok) {
         set_status(a.status, DEV_TIMEOUT);
@@ -240,7 +277,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int c = (warp - 2) >> 2;  // column quarter
     const int lr = q * 32 + lane;   // token row inside the tile
     int it = 0;
-    for (int w = blockIdx.x; w < total; w += gridDim.x, ++it) {
+    // 32-row tiles keep their rows in TMEM lanes 0..31: the other quadrants' warps have nothing to do
+    const int my_total = (AROWS == kSmallRows && q != 0) ? 0 : total;
+    for (int w = blockIdx.x; w < my_total; w += gridDim.x, ++it) {
       bool got = !abort_flag && mbar_wait(acc_full, (uint32_t)it & 1u, a.budget_ns);
       got = __all_sync(0xFFFFFFFFu, got);
       if (!got) {

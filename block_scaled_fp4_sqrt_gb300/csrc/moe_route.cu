@@ -98,9 +98,11 @@ __device__ __forceinline__ float softplus_f(float l) { return fmaxf(l, 0.f) + lo
 // lower expert id) and reports ids ascending with weights route_scale * s_j / sum_j s_j.
 constexpr int kTopkTokens = 8;
 
-constexpr int kMaxSplit = 32;
 
-__global__ void __launch_bounds__(512) router_topk_kernel(const float* __restrict__ partial, int ksplit,
+// KS = the number of split-K partials, a template argument so that the KS loads of a sum are issued
+// unconditionally and back to back (a runtime-bounded loop serialises them on the L2 latency).
+template <int KS>
+__global__ void __launch_bounds__(512) router_topk_kernel(const float* __restrict__ partial,
                                                           const float* __restrict__ bias, int T, int E, int k,
                                                           float route_scale, int32_t* __restrict__ ids,
                                                           float* __restrict__ wts) {
@@ -111,11 +113,12 @@ __global__ void __launch_bounds__(512) router_topk_kernel(const float* __restric
     const int i = idx / E, e = idx - i * E;
     const int t = t0 + i;
     if (t >= T) continue;
-    // unrolled so the split loads (independent) issue together; the sum runs in split order
+    float v[KS];
+#pragma unroll
+    for (int z = 0; z < KS; ++z) v[z] = __ldg(&partial[((size_t)z * T + t) * E + e]);
     float l = 0.f;
 #pragma unroll
-    for (int z = 0; z < kMaxSplit; ++z)
-      if (z < ksplit) l += __ldg(&partial[((size_t)z * T + t) * E + e]);
+    for (int z = 0; z < KS; ++z) l += v[z];
     const float sv = sqrtf(softplus_f(l));
     s_s[i][e] = sv;
     s_sel[i][e] = sv + bias[e];
@@ -244,9 +247,20 @@ cudaError_t launch_router_logits(const __nv_bfloat16* x, const float* w, int T, 
 
 cudaError_t launch_router_topk(const float* partial, int ksplit, const float* bias, int T, int E, int k,
                                float route_scale, int32_t* ids, float* wts, cudaStream_t s) {
-  if (ksplit > kMaxSplit) return cudaErrorInvalidValue;
   const int blocks = (T + kTopkTokens - 1) / kTopkTokens;
-  router_topk_kernel<<<blocks, 512, 0, s>>>(partial, ksplit, bias, T, E, k, route_scale, ids, wts);
+  switch (ksplit) {
+#define MOE_TOPK_CASE(KS) \
+  case KS: router_topk_kernel<KS><<<blocks, 512, 0, s>>>(partial, bias, T, E, k, route_scale, ids, wts); break;
+    MOE_TOPK_CASE(1)
+    MOE_TOPK_CASE(2)
+    MOE_TOPK_CASE(4)
+    MOE_TOPK_CASE(8)
+    MOE_TOPK_CASE(16)
+    MOE_TOPK_CASE(32)
+#undef MOE_TOPK_CASE
+    default:
+      return cudaErrorInvalidValue;
+  }
   return cudaGetLastError();
 }
 

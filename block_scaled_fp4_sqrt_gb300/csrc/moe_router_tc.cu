@@ -38,20 +38,26 @@ __device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t a_desc, ui
       : "memory");
 }
 
-// Wr fp32 [E, d] -> three bf16 matrices [3, Epad, d] (rows E .. Epad-1 zero).
-__global__ void split_router_kernel(const float* __restrict__ w, int E, int Epad, int d,
+// Wr fp32 [E, d] -> three bf16 matrices [3, Epad, d] (rows E .. Epad-1 zero); four weights per thread
+// and step (d is a multiple of 256, so a group of four never crosses a row).
+__global__ void split_router_kernel(const float4* __restrict__ w, int E, int Epad, int d,
                                     __nv_bfloat16* __restrict__ out) {
-  const size_t total = (size_t)Epad * d;
-  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
-    const int e = (int)(i / d);
-    const float v = e < E ? w[i] : 0.f;
-    const __nv_bfloat16 hi = __float2bfloat16_rn(v);
-    const float r1 = v - __bfloat162float(hi);
-    const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
-    const __nv_bfloat16 lo = __float2bfloat16_rn(r1 - __bfloat162float(mid));
-    out[i] = hi;
-    out[total + i] = mid;
-    out[2 * total + i] = lo;
+  const size_t total = (size_t)Epad * d, quads = total / 4;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < quads; i += (size_t)gridDim.x * blockDim.x) {
+    const int e = (int)(i * 4 / d);
+    const float4 v4 = e < E ? __ldg(&w[i]) : make_float4(0.f, 0.f, 0.f, 0.f);
+    const float v[4] = {v4.x, v4.y, v4.z, v4.w};
+    __nv_bfloat16 hi[4], mid[4], lo[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      hi[j] = __float2bfloat16_rn(v[j]);
+      const float r1 = v[j] - __bfloat162float(hi[j]);
+      mid[j] = __float2bfloat16_rn(r1);
+      lo[j] = __float2bfloat16_rn(r1 - __bfloat162float(mid[j]));
+    }
+    *reinterpret_cast<uint2*>(out + i * 4) = *reinterpret_cast<const uint2*>(hi);
+    *reinterpret_cast<uint2*>(out + total + i * 4) = *reinterpret_cast<const uint2*>(mid);
+    *reinterpret_cast<uint2*>(out + 2 * total + i * 4) = *reinterpret_cast<const uint2*>(lo);
   }
 }
 
@@ -201,8 +207,8 @@ int router_tc_epad(int E) { return (E + kRN - 1) / kRN * kRN; }
 cudaError_t launch_split_router(const float* w, int E, int d, __nv_bfloat16* out, cudaStream_t s) {
   const int Epad = router_tc_epad(E);
   const size_t total = (size_t)Epad * d;
-  const int blocks = (int)std::min<size_t>((total + 255) / 256, 152 * 8);
-  split_router_kernel<<<blocks, 256, 0, s>>>(w, E, Epad, d, out);
+  const int blocks = (int)std::min<size_t>((total / 4 + 255) / 256, 152 * 8);
+  split_router_kernel<<<blocks, 256, 0, s>>>(reinterpret_cast<const float4*>(w), E, Epad, d, out);
   return cudaGetLastError();
 }
 
