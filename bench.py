@@ -47,6 +47,38 @@ def dist_env():
     return int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")), int(os.environ.get("WORLD_SIZE", "1"))
 
 
+def replica_x(seed: int, rank: int, world: int, T: int, d: int):
+    """Each replica's own batch of token rows: with one GPU the workload's batch, under torchrun rank r
+    draws from seed + 7919 r (rank 0 keeps the one-GPU batch)."""
+    import synth
+    return synth.gen_x(seed + 7919 * rank if world > 1 else seed, T, d)
+
+
+def init_replicas(backend: str, timeout_s: float = 300.0) -> None:
+    """Join the torchrun job (RANK / WORLD_SIZE / MASTER_ADDR / MASTER_PORT from the environment).  A
+    finite timeout makes a barrier or reduction whose peer has died end in an error, not a hang."""
+    import datetime
+
+    import torch.distributed as dist
+    dist.init_process_group(backend, timeout=datetime.timedelta(seconds=timeout_s))
+
+
+def max_over_ranks(x: float, device=None) -> float:
+    """The largest value of x over all ranks (all-reduce MAX of one scalar); x itself on one rank."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(world: int, T: int, ms_per_step: float) -> float:
+    """Whole-job throughput: every replica processes T tokens per step; the slowest rank's time counts."""
+    return world * T / (ms_per_step * 1e-3)
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -143,10 +175,14 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+# sources that decide what the grouped GEMMs read and write (kernel, launch shape, work list, weight layout)
+GEMM_SOURCES = ("moe_gemm.cu", "moe_device.cuh", "moe_internal.h", "moe_api.cu", "moe_dispatch.cu", "moe_pack.cu")
+
+
 def kernel_source_digest():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "block_scaled_fp4_sqrt_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in GEMM_SOURCES:
         with open(os.path.join(csrc, name), "rb") as fh:
             h.update(name.encode())
             h.update(fh.read())
@@ -154,15 +190,25 @@ def kernel_source_digest():
 
 
 def measured_traffic(kernel: str, workload: str):
-    """DRAM bytes per launch from a committed ncu capture, only if the kernels have not changed since."""
-    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    """DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from the committed ncu
+    summary profiles/dram_traffic.txt, only if the GEMM sources have not changed since the capture.
+    Lines: "digest <hex>" and "<workload> <kernel> <bytes> <note...>"."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(path):
         return None
+    digest, table = None, {}
     with open(path) as fh:
-        rec = json.load(fh)
-    if rec.get("kernel_source_digest") != kernel_source_digest():
+        for line in fh:
+            parts = line.split()
+            if not parts or parts[0].startswith("#"):
+                continue
+            if parts[0] == "digest" and len(parts) > 1:
+                digest = parts[1]
+            elif len(parts) >= 3:
+                table[(parts[0], parts[1])] = int(parts[2])
+    if digest != kernel_source_digest():
         return None
-    return rec.get("per_launch_bytes", {}).get(workload, {}).get(kernel)
+    return table.get((workload, kernel))
 
 
 def oracle_tokens_per_s(inp, wl, n_tokens: int, seed: int):
@@ -239,14 +285,13 @@ def run_ours(args, wl):
     import block_scaled_fp4_sqrt_gb300 as moe
 
     if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl")
+        init_replicas("nccl")
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
 
     inp = synth.gen_layer(wl, args.seed)
     if world > 1:  # each replica gets its own batch of token rows
-        inp.x = synth.gen_x(args.seed + 7919 * rank, wl.T, wl.d)
+        inp.x = replica_x(args.seed, rank, world, wl.T, wl.d)
     layer = moe.MoELayer.from_host(inp, device=dev, max_T=wl.T)
     x = torch.from_numpy(inp.x.view(np.int16)).to(dev).view(torch.bfloat16)
     out = torch.empty((wl.T, wl.d), dtype=torch.bfloat16, device=dev)
@@ -262,6 +307,9 @@ def run_ours(args, wl):
     ids, _ = layer.last_routing()
     touched = int(torch.unique(ids).numel()) + 1  # + shared expert
     rows = wl.T * wl.k + wl.T
+
+    # block-scaled MMA peak of this GPU (the tensor roofline's denominator), before the timed region
+    mx_peak = moe.moe_measure_mxf8f6f4_peak(4096)
 
     # ---- device-timed steps, with per-stage events on the launching stream
     n_ev = moe.MOE_N_STAGES + 1
@@ -288,11 +336,7 @@ def run_ours(args, wl):
     clk = clocks.stop()
     moe.moe_set_stage_events(layer.h, None)
     layer.check()
-    ms = t_begin.elapsed_time(t_end) / args.steps
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(t_begin.elapsed_time(t_end) / args.steps, dev)
     stage_ms = {name: statistics.mean(ev[i].elapsed_time(ev[i + 1]) for ev in events)
                 for i, name in enumerate(moe.STAGE_NAMES)}
 
@@ -321,11 +365,7 @@ def run_ours(args, wl):
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
-    ms_e2e = e0.elapsed_time(e1) / args.steps
-    if world > 1:
-        t = torch.tensor([ms_e2e], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_e2e = float(t.item())
+    ms_e2e = max_over_ranks(e0.elapsed_time(e1) / args.steps, dev)
 
     if rank != 0:
         if world > 1:
@@ -341,10 +381,12 @@ def run_ours(args, wl):
     compute_bound = dom in fl and wl.T * wl.k / wl.E >= 64
     if compute_bound:
         achieved = fl[dom] / (stage_ms[dom] * 1e-3) / 1e12
-        peak = 2 * pk["bf16_tflops_sustained"]  # FP8-class block-scaled MMA: nominal 2x the bf16 rate
-        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+        roof = {"bound": "tensor", "achieved": achieved, "peak": mx_peak, "unit": "TFLOP/s", "frac": achieved / mx_peak,
                 "traffic": measured_traffic(dom, wl.name), "kernel": dom,
-                "peak_source": f"{pk['source']} bf16 sustained x 2 (nominal FP8/BF16 ratio)",
+                "peak_source": "measured in this run: back-to-back tcgen05.mma kind::mxf8f6f4.block_scale "
+                               "(E4M3 x E2M1, M=128 N=256 K=32) on every SM (moe_measure_mxf8f6f4_peak)",
+                "nominal_alt_peak": {"value": 2 * pk["bf16_tflops_sustained"],
+                                     "source": f"{pk['source']} bf16 sustained x 2 (nominal FP8/BF16 ratio)"},
                 "algorithmic_flops_per_launch": fl[dom]}
     else:
         achieved = sb[dom] / (stage_ms[dom] * 1e-3) / 1e9
@@ -356,15 +398,20 @@ def run_ours(args, wl):
     # histogram, column scan, group scan, gather; the two grouped GEMMs; combine
     kernels_per_step = (1 if wl.hashed else 3) + 4 + 2 + 1
     line = {
-        "metric": METRIC, "value": world * wl.T / (ms * 1e-3), "unit": "tokens/s", "n_gpus": world,
+        "metric": METRIC, "value": job_tokens_per_s(world, wl.T, ms), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "mxfp4 x mxfp8 -> f32", "data": "synthetic",
         "config": dict(workload_config(wl), touched_experts=touched, parallelism=f"replicas x{world}"),
         "roofline": roof,
         "layer_roofline": {"bound": "hbm", "algorithmic_bytes": lb, "achieved": lb / (ms * 1e-3) / 1e9,
                            "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": lb / (ms * 1e-3) / 1e9 / pk["hbm_gbs"]},
+        "gemm_tensor": {"achieved": (fl["gemm_gate_up"] + fl["gemm_down"]) /
+                        ((stage_ms["gemm_gate_up"] + stage_ms["gemm_down"]) * 1e-3) / 1e12,
+                        "peak": mx_peak, "unit": "TFLOP/s",
+                        "frac": (fl["gemm_gate_up"] + fl["gemm_down"]) /
+                        ((stage_ms["gemm_gate_up"] + stage_ms["gemm_down"]) * 1e-3) / 1e12 / mx_peak},
         "stage_ms": stage_ms,
-        "e2e": {"value": world * wl.T / (ms_e2e * 1e-3), "unit": "tokens/s",
+        "e2e": {"value": job_tokens_per_s(world, wl.T, ms_e2e), "unit": "tokens/s",
                 "h2d_bytes_per_step": wl.T * wl.d * 2 + (wl.T * 4 if wl.hashed else 0),
                 "d2h_bytes_per_step": wl.T * wl.d * 2},
         "gpu_launches": kernels_per_step * args.steps,

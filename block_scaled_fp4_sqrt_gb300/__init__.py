@@ -25,7 +25,7 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
 EXPORTED = ("moe_experts_create", "moe_experts_set_hash_table", "moe_workspace_size", "moe_set_workspace",
             "moe_route", "moe_permute", "moe_expert_ffn", "moe_forward", "moe_get_routing", "moe_check",
             "moe_set_wait_budget", "moe_experts_destroy", "moe_status_string", "moe_last_error",
-            "moe_testing_stall_loads", "moe_set_stage_events", "moe_route_noalloc")
+            "moe_testing_stall_loads", "moe_set_stage_events", "moe_route_noalloc", "moe_measure_mxf8f6f4_peak")
 
 MOE_N_STAGES = 5
 STAGE_NAMES = ("route", "dispatch", "gemm_gate_up", "gemm_down", "combine")
@@ -70,6 +70,7 @@ def lib() -> ctypes.CDLL:
         L.moe_testing_stall_loads.argtypes = [vp, i32]
         L.moe_set_stage_events.argtypes = [vp, ctypes.POINTER(vp), i32]
         L.moe_route_noalloc.argtypes = [cfgp, inp, vp, vp, vp, vp, vp]
+        L.moe_measure_mxf8f6f4_peak.argtypes = [i32, ctypes.POINTER(ctypes.c_double)]
         L.moe_experts_destroy.argtypes = [vp]
         L.moe_experts_destroy.restype = None
         L.moe_status_string.argtypes = [st]
@@ -166,6 +167,14 @@ def moe_set_wait_budget(h, budget_ns: int) -> None:
 
 def moe_testing_stall_loads(h, enable: bool) -> None:
     _ok("moe_testing_stall_loads", lib().moe_testing_stall_loads(h, 1 if enable else 0))
+
+
+def moe_measure_mxf8f6f4_peak(n_stages: int = 4096) -> float:
+    """Measured dense TFLOP/s of the block-scaled E4M3 x E2M1 MMA (M=128, N=256, K=32) on the
+    current device; synchronous."""
+    out = ctypes.c_double(0.0)
+    _ok("moe_measure_mxf8f6f4_peak", lib().moe_measure_mxf8f6f4_peak(int(n_stages), ctypes.byref(out)))
+    return out.value
 
 
 def moe_set_stage_events(h, events) -> object:
