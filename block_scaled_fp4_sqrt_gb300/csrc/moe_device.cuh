@@ -17,6 +17,14 @@ __device__ __forceinline__ void set_status(int* status, int code) {
   if (status) atomicOr(status, code);
 }
 
+// ------------------------------------------------------------------------- programmatic dependent launch
+// The small kernels of the layer call pdl_trigger() on entry, so that the next kernel in the stream may
+// be scheduled while they run; every kernel calls pdl_wait() after its prologue but before its first
+// access to global memory, which returns once the previous kernel has completed and its writes are
+// visible.  Without the launch attribute (launch_pdl) both are no-ops.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ uint64_t globaltimer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

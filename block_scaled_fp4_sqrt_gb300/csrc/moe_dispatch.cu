@@ -31,6 +31,8 @@ __device__ __forceinline__ int clamp_id(int e, int E, int* status) {
 // one warp per 32-token chunk; chunk_hist[g][c] = number of (t, j) in chunk c with ids[t, j] = g
 __global__ void histogram_kernel(const int32_t* __restrict__ ids, int T, int k, int E, int G, int n_chunks,
                                  int32_t* __restrict__ chunk_hist, int* status) {
+  pdl_trigger();
+  pdl_wait();
   extern __shared__ int sh_hist[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int chunk = blockIdx.x * (blockDim.x >> 5) + warp;
@@ -80,6 +82,8 @@ __device__ int block_exclusive_scan(int v, int* total) {
 // its total goes to counts[g].  The shared group (index E when has_shared) holds all T rows.
 __global__ void __launch_bounds__(256) colscan_kernel(int32_t* __restrict__ chunk_hist, int n_chunks, int T, int E,
                                                       int has_shared, int32_t* __restrict__ counts) {
+  pdl_trigger();
+  pdl_wait();
   const int g = blockIdx.x;
   if (has_shared && g == E) {
     if (threadIdx.x == 0) counts[g] = T;
@@ -108,6 +112,8 @@ __global__ void __launch_bounds__(1024) groupscan_kernel(const int32_t* __restri
                                                          int* status) {
   __shared__ int s_cnt[kMaxGroups], s_off[kMaxGroups], s_toff[kMaxGroups];
   __shared__ int bad;
+  pdl_trigger();
+  pdl_wait();
   if (threadIdx.x == 0) bad = (offsets_in && (offsets_in[0] != 0 || offsets_in[G] != n_rows)) ? 1 : 0;
   __syncthreads();
   int carry_r = 0, carry_t = 0;
@@ -179,6 +185,8 @@ __global__ void __launch_bounds__(128) gather_kernel(
     uint8_t* __restrict__ a_q, uint8_t* __restrict__ a_sf_atoms, uint8_t* __restrict__ a_s_rows,
     int32_t* __restrict__ perm_tok, int32_t* __restrict__ inv_pos, float* __restrict__ row_w) {
   constexpr int kMaxDst = 17;  // top-k <= 16, plus the shared row
+  pdl_trigger();
+  pdl_wait();
   const int lane = threadIdx.x & 31;
   const int nb = d / 32;
   for (int t = blockIdx.x; t < T; t += gridDim.x) {
@@ -279,6 +287,8 @@ __global__ void __launch_bounds__(128) gather_kernel(
 // out[t, c] = bf16( sum_j Yr[inv_pos[t, j], c] + Yr[R + t, c] ), fp32 rows, 8 columns per thread
 __global__ void combine_kernel(const float* __restrict__ y_rows, const int32_t* __restrict__ inv_pos, int T, int d,
                                int k, int R, int has_shared, __nv_bfloat16* __restrict__ out) {
+  pdl_trigger();
+  pdl_wait();
   const int vec_per_row = d / 8;
   const size_t total = (size_t)T * vec_per_row;
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
@@ -315,9 +325,8 @@ cudaError_t launch_histogram(const int32_t* ids, int T, int k, int E, int G, int
   const int n_chunks = (T + 31) / 32;
   const int warps = 8;
   const int blocks = (n_chunks + warps - 1) / warps;
-  histogram_kernel<<<blocks, warps * 32, (size_t)warps * G * sizeof(int), s>>>(ids, T, k, E, G, n_chunks, chunk_hist,
-                                                                               status);
-  return cudaGetLastError();
+  return launch_pdl(histogram_kernel, dim3(blocks), dim3(warps * 32), (size_t)warps * G * sizeof(int), s, ids, T, k, E,
+                    G, n_chunks, chunk_hist, status);
 }
 
 cudaError_t launch_scan(int32_t* chunk_hist, int n_chunks, int T, int E, int G, int has_shared, int bn, int max_tiles,
@@ -325,19 +334,19 @@ cudaError_t launch_scan(int32_t* chunk_hist, int n_chunks, int T, int E, int G, 
                         int* status, cudaStream_t s) {
   if (G > kMaxGroups) return cudaErrorInvalidValue;
   const int threads = n_chunks >= 256 ? 256 : ((n_chunks + 31) / 32) * 32;
-  colscan_kernel<<<G, threads, 0, s>>>(chunk_hist, n_chunks, T, E, has_shared, counts);
-  groupscan_kernel<<<1, 1024, 0, s>>>(counts, nullptr, G, 0, bn, max_tiles, offsets, tile_off, n_tiles, tiles,
-                                      status);
-  return cudaGetLastError();
+  cudaError_t e = launch_pdl(colscan_kernel, dim3(G), dim3(threads), 0, s, chunk_hist, n_chunks, T, E, has_shared,
+                             counts);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(groupscan_kernel, dim3(1), dim3(1024), 0, s, (const int32_t*)counts, (const int32_t*)nullptr, G, 0,
+                    bn, max_tiles, offsets, tile_off, n_tiles, tiles, status);
 }
 
 cudaError_t launch_tiles_from_offsets(const int32_t* offsets, int G, int n_rows, int bn, int max_tiles,
                                       int32_t* tile_off, int32_t* n_tiles, RowTile* tiles, int* status,
                                       cudaStream_t s) {
   if (G > kMaxGroups) return cudaErrorInvalidValue;
-  groupscan_kernel<<<1, 1024, 0, s>>>(nullptr, offsets, G, n_rows, bn, max_tiles, nullptr, tile_off, n_tiles, tiles,
-                                      status);
-  return cudaGetLastError();
+  return launch_pdl(groupscan_kernel, dim3(1), dim3(1024), 0, s, (const int32_t*)nullptr, offsets, G, n_rows, bn,
+                    max_tiles, (int32_t*)nullptr, tile_off, n_tiles, tiles, status);
 }
 
 cudaError_t launch_gather(const __nv_bfloat16* x, const int32_t* ids, const float* wts, const int32_t* chunk_hist,
@@ -349,9 +358,8 @@ cudaError_t launch_gather(const __nv_bfloat16* x, const int32_t* ids, const floa
   const int nb = d / 32;
   const int threads = nb >= 128 ? 128 : ((nb + 31) / 32) * 32;
   const int blocks = T < 152 * 16 ? T : 152 * 16;
-  gather_kernel<<<blocks, threads, 0, s>>>(x, ids, wts, chunk_hist, n_chunks, offsets, tile_off, T, d, k, E,
-                                           has_shared, bn, a_q, a_sf_atoms, a_s_rows, perm_tok, inv_pos, row_w);
-  return cudaGetLastError();
+  return launch_pdl(gather_kernel, dim3(blocks), dim3(threads), 0, s, x, ids, wts, chunk_hist, n_chunks, offsets,
+                    tile_off, T, d, k, E, has_shared, bn, a_q, a_sf_atoms, a_s_rows, perm_tok, inv_pos, row_w);
 }
 
 cudaError_t launch_combine(const float* y_rows, const int32_t* inv_pos, int T, int d, int k, int R,
@@ -360,8 +368,7 @@ cudaError_t launch_combine(const float* y_rows, const int32_t* inv_pos, int T, i
   int blocks = (int)((total + 255) / 256);
   if (blocks > 152 * 16) blocks = 152 * 16;
   if (blocks < 1) blocks = 1;
-  combine_kernel<<<blocks, 256, 0, s>>>(y_rows, inv_pos, T, d, k, R, has_shared, out);
-  return cudaGetLastError();
+  return launch_pdl(combine_kernel, dim3(blocks), dim3(256), 0, s, y_rows, inv_pos, T, d, k, R, has_shared, out);
 }
 
 }  // namespace moe

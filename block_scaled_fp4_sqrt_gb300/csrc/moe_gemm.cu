@@ -39,7 +39,15 @@ constexpr int kSmallRows = 32;  // groups this small load a 32-row activation bo
 constexpr int kEpiWarps = 16;
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 
-template <int STAGES, int AROWS>
+// Staging buffer of one epilogue warp for coalesced fp32 row stores: 32 rows x 32 columns, rows 144 B
+// apart (36 floats) so that the row-per-lane writes and the line-per-quarter-warp reads are both free
+// of bank conflicts.
+constexpr int kStageStride = 36;
+constexpr int kStageFloats = 32 * kStageStride;
+
+// EPI = 1: the down projection's fp32 rows leave through a per-warp shared-memory transpose (full
+// 128-byte lines per quarter warp) instead of 16-byte stores to 32 different rows per instruction.
+template <int STAGES, int AROWS, int EPI = 0>
 struct Cfg {
   static constexpr int kASlot = AROWS * 128;         // activation rows x 128 FP8
   static constexpr int kBSlot = kN * 128;            // 256 weight rows x 128 FP4, padded to bytes
@@ -47,8 +55,11 @@ struct Cfg {
   static constexpr int kAOff = 0;                    // [activation ring | weight ring | scale ring]
   static constexpr int kBOff = STAGES * kASlot;
   static constexpr int kSfOff = kBOff + STAGES * kBSlot;
+  static constexpr int kEpiOff = kSfOff + STAGES * kSfSlot;  // [ ... | scale ring | staging | barriers]
+  static constexpr int kEpiBytes = EPI ? kEpiWarps * kStageFloats * 4 : 0;
+  static constexpr int kBarOff = kEpiOff + kEpiBytes;
   static constexpr int kBarBytes = (2 * STAGES + 3) * 8;
-  static constexpr int kSmem = kSfOff + STAGES * kSfSlot + 1024 + kBarBytes;
+  static constexpr int kSmem = kBarOff + 1024 + kBarBytes;
   static constexpr uint32_t kTxB = kN * 64 + 2 * kSfAtomBytes;  // packed FP4 box (64 B per row) + weight atoms
   static constexpr int kAccCols = kN;                           // one fp32 accumulator [128 x 256]
   static constexpr int kSfCols = 12;                            // per stage: A atom 4 columns, B atoms 8
@@ -58,6 +69,7 @@ struct Cfg {
   static_assert(kBOff % 1024 == 0 && kSfOff % 1024 == 0, "swizzled tiles need 1024-byte alignment");
   static_assert(AROWS == kBM || kBOff >= (kBM - AROWS) * 128, "M = 128 reads past a short activation slot");
   static_assert(kAccCols + STAGES * kSfCols <= kTmemCols, "TMEM budget");
+  static_assert(kEpiOff % 16 == 0, "staging rows are float4-aligned");
   static_assert(kSmem <= 232448 - 64, "shared memory budget");
 };
 
@@ -89,15 +101,15 @@ struct GemmArgs {
 
 __device__ __forceinline__ float silu_f(float z) { return z / (1.0f + expf(-z)); }
 
-template <int STAGES, int AROWS>
+template <int STAGES, int AROWS, int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_mx_gemm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_w_shared,
                            const __grid_constant__ CUtensorMap tm_act, const __grid_constant__ CUtensorMap tm_act_small,
                            const GemmArgs a) {
-  using C = Cfg<STAGES, AROWS>;
+  using C = Cfg<STAGES, AROWS, EPI>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kSfOff + STAGES * C::kSfSlot);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
   uint64_t* empty = full + STAGES;
   uint64_t* acc_full = empty + STAGES;
   uint64_t* acc_empty = acc_full + 1;
@@ -105,10 +117,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ uint32_t tmem_slot;
   __shared__ volatile int abort_flag;
 
+  // No pdl_trigger() here: letting the next kernel's CTAs in while the GEMM still runs slowed the
+  // T = 8192 step by 4 % (measured); they launch when the GEMM completes.
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  int n_tiles = *reinterpret_cast<const volatile int32_t*>(a.n_tiles);
-  if (n_tiles > a.max_tiles) n_tiles = a.max_tiles;
-  const int total = n_tiles * a.m_tiles;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -132,6 +143,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = tmem_slot;
+  // the work list and the activations come from earlier kernels
+  pdl_wait();
+  int n_tiles = *reinterpret_cast<const volatile int32_t*>(a.n_tiles);
+  if (n_tiles > a.max_tiles) n_tiles = a.max_tiles;
+  const int total = n_tiles * a.m_tiles;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -303,6 +319,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(acc_empty);
+      if (EPI && !a.gate_up) {
+        // fp32 rows through the warp's staging buffer: lane l writes its row's 32 values, then each
+        // quarter warp stores one row's 128 contiguous bytes
+        if (active) {
+          const bool row_ok = lr < rt.nrows;
+          const float wr = !row_ok ? 0.f : (a.row_w ? __ldg(&a.row_w[rt.row0 + lr]) : 1.0f);
+          float* stg = reinterpret_cast<float*>(smem + C::kEpiOff) + (warp - 2) * kStageFloats;
+          float* ybase = a.y_f32 + (size_t)rt.row0 * a.d + (size_t)mt * kN + 64 * c;
+          auto stage_half = [&](const float(&v)[32], int half) {
+            float4* srow = reinterpret_cast<float4*>(stg + lane * kStageStride);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              srow[i] = make_float4(v[4 * i] * wr, v[4 * i + 1] * wr, v[4 * i + 2] * wr, v[4 * i + 3] * wr);
+            __syncwarp();
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const int rr = q * 32 + 4 * i + (lane >> 3);  // row inside the tile
+              const float4 val = reinterpret_cast<const float4*>(stg + (4 * i + (lane >> 3)) * kStageStride)[lane & 7];
+              if (rr < rt.nrows) reinterpret_cast<float4*>(ybase + (size_t)rr * a.d + 32 * half)[lane & 7] = val;
+            }
+            __syncwarp();
+          };
+          stage_half(v0, 0);
+          stage_half(v1, 1);
+        }
+        continue;
+      }
       if (!active || lr >= rt.nrows) continue;
       const int r = rt.row0 + lr;
       if (a.gate_up) {
@@ -363,27 +406,31 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc(tbase, C::kTmemCols);
 }
 
-template <int STAGES, int AROWS>
+template <int STAGES, int AROWS, int EPI>
 cudaError_t launch_shape(const CUtensorMap& w, const CUtensorMap& w_sh, const CUtensorMap& act,
                          const CUtensorMap& act_small, const GemmArgs& a, int num_sms, cudaStream_t s) {
-  using C = Cfg<STAGES, AROWS>;
+  using C = Cfg<STAGES, AROWS, EPI>;
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(grouped_mx_gemm_kernel<STAGES, AROWS>,
+    cudaError_t e = cudaFuncSetAttribute(grouped_mx_gemm_kernel<STAGES, AROWS, EPI>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  grouped_mx_gemm_kernel<STAGES, AROWS><<<num_sms, kThreads, C::kSmem, s>>>(w, w_sh, act, act_small, a);
-  return cudaGetLastError();
+  return launch_pdl(grouped_mx_gemm_kernel<STAGES, AROWS, EPI>, dim3(num_sms), dim3(kThreads), C::kSmem, s, w, w_sh,
+                    act, act_small, a);
 }
 
-// tile_rows 32: 6 stages of 32-row activation slots; tile_rows 128: 4 stages of 128-row slots.
+// tile_rows 32: 6 stages of 32-row activation slots.  tile_rows 128: 4 stages of 128-row slots, or for
+// the down projection's fp32 rows 3 stages plus the epilogue's staging buffers (the 16-byte scattered
+// stores of the direct epilogue bound that GEMM at the 8192-token shape: 835 us with them, 373 us
+// without any stores).
 cudaError_t launch_grouped(const CUtensorMap& w, const CUtensorMap& w_sh, const CUtensorMap& act,
                            const CUtensorMap& act_small, const GemmArgs& a, int tile_rows, int num_sms,
                            cudaStream_t s) {
-  if (tile_rows == kSmallRows) return launch_shape<6, kSmallRows>(w, w_sh, act, act_small, a, num_sms, s);
-  return launch_shape<4, kBM>(w, w_sh, act, act_small, a, num_sms, s);
+  if (tile_rows == kSmallRows) return launch_shape<6, kSmallRows, 0>(w, w_sh, act, act_small, a, num_sms, s);
+  if (!a.gate_up && a.y_f32) return launch_shape<3, kBM, 1>(w, w_sh, act, act_small, a, num_sms, s);
+  return launch_shape<4, kBM, 0>(w, w_sh, act, act_small, a, num_sms, s);
 }
 
 }  // namespace

@@ -7,6 +7,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace moe {
 
 // Device status bits (sticky, OR-ed into the handle's status word).
@@ -66,6 +68,23 @@ struct Workspace {
 
 // Text returned by moe_last_error() on this thread.
 void set_last_error(const char* msg);
+
+// Launch with programmatic stream serialization: the kernel may be scheduled before the previous kernel
+// in the stream has finished (it must call pdl_wait() before touching global memory, see moe_device.cuh).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 size_t workspace_layout(int max_T, int d, int f, int E, int k, Workspace* ws, void* base);
 

@@ -106,6 +106,8 @@ __global__ void __launch_bounds__(512) router_topk_kernel(const float* __restric
                                                           const float* __restrict__ bias, int T, int E, int k,
                                                           float route_scale, int32_t* __restrict__ ids,
                                                           float* __restrict__ wts) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ float s_s[kTopkTokens][32 * kMaxPerLane];
   __shared__ float s_sel[kTopkTokens][32 * kMaxPerLane];
   const int t0 = blockIdx.x * kTopkTokens;
@@ -201,6 +203,8 @@ __global__ void __launch_bounds__(512) router_topk_kernel(const float* __restric
 __global__ void hash_route_kernel(const int32_t* __restrict__ tok, const int32_t* __restrict__ table, int V, int T,
                                   int E, int k, float route_scale, int32_t* __restrict__ ids, float* __restrict__ wts,
                                   int* status) {
+  pdl_trigger();
+  pdl_wait();
   int t = blockIdx.x * blockDim.x + threadIdx.x;
   if (t >= T) return;
   int v = tok[t];
@@ -250,7 +254,8 @@ cudaError_t launch_router_topk(const float* partial, int ksplit, const float* bi
   const int blocks = (T + kTopkTokens - 1) / kTopkTokens;
   switch (ksplit) {
 #define MOE_TOPK_CASE(KS) \
-  case KS: router_topk_kernel<KS><<<blocks, 512, 0, s>>>(partial, bias, T, E, k, route_scale, ids, wts); break;
+  case KS: return launch_pdl(router_topk_kernel<KS>, dim3(blocks), dim3(512), 0, s, partial, bias, T, E, k, \
+                             route_scale, ids, wts);
     MOE_TOPK_CASE(1)
     MOE_TOPK_CASE(2)
     MOE_TOPK_CASE(4)
@@ -261,13 +266,12 @@ cudaError_t launch_router_topk(const float* partial, int ksplit, const float* bi
     default:
       return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
 }
 
 cudaError_t launch_hash_route(const int32_t* tok, const int32_t* table, int V, int T, int E, int k, float route_scale,
                               int32_t* ids, float* wts, int* status, cudaStream_t s) {
-  hash_route_kernel<<<(T + 127) / 128, 128, 0, s>>>(tok, table, V, T, E, k, route_scale, ids, wts, status);
-  return cudaGetLastError();
+  return launch_pdl(hash_route_kernel, dim3((T + 127) / 128), dim3(128), 0, s, tok, table, V, T, E, k, route_scale, ids,
+                    wts, status);
 }
 
 }  // namespace moe

@@ -42,6 +42,8 @@ __device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t a_desc, ui
 // and step (d is a multiple of 256, so a group of four never crosses a row).
 __global__ void split_router_kernel(const float4* __restrict__ w, int E, int Epad, int d,
                                     __nv_bfloat16* __restrict__ out) {
+  pdl_trigger();
+  pdl_wait();
   const size_t total = (size_t)Epad * d, quads = total / 4;
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < quads; i += (size_t)gridDim.x * blockDim.x) {
     const int e = (int)(i * 4 / d);
@@ -79,6 +81,7 @@ __global__ void __launch_bounds__(192, 1) router_tc_kernel(const __grid_constant
   uint64_t* empty = full + kRStages;
   uint64_t* acc_full = empty + kRStages;
   __shared__ uint32_t tmem_slot;
+  pdl_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t0 = blockIdx.x * kRM, e0 = blockIdx.y * kRN, z = blockIdx.z;
   const int k0 = z * a.k_per_split, n_stages = a.k_per_split / kRK;
@@ -99,6 +102,7 @@ __global__ void __launch_bounds__(192, 1) router_tc_kernel(const __grid_constant
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = tmem_slot;
+  pdl_wait();  // x and the split weights come from earlier kernels
   bool acc_ok = true;
 
   if (warp == 0 && lane == 0) {
@@ -208,8 +212,8 @@ cudaError_t launch_split_router(const float* w, int E, int d, __nv_bfloat16* out
   const int Epad = router_tc_epad(E);
   const size_t total = (size_t)Epad * d;
   const int blocks = (int)std::min<size_t>((total / 4 + 255) / 256, 152 * 8);
-  split_router_kernel<<<blocks, 256, 0, s>>>(reinterpret_cast<const float4*>(w), E, Epad, d, out);
-  return cudaGetLastError();
+  return launch_pdl(split_router_kernel, dim3(blocks), dim3(256), 0, s, reinterpret_cast<const float4*>(w), E, Epad,
+                    d, out);
 }
 
 cudaError_t launch_router_tc(const CUtensorMap& tm_x, const CUtensorMap& tm_w, int T, int E, int d, int split,
@@ -222,8 +226,7 @@ cudaError_t launch_router_tc(const CUtensorMap& tm_x, const CUtensorMap& tm_w, i
   }
   RouterArgs a{partial, T, E, router_tc_epad(E), d, d / split, status, budget_ns};
   dim3 grid((T + kRM - 1) / kRM, a.Epad / kRN, split);
-  router_tc_kernel<<<grid, 192, kRSmem, s>>>(tm_x, tm_w, a);
-  return cudaGetLastError();
+  return launch_pdl(router_tc_kernel, grid, dim3(192), kRSmem, s, tm_x, tm_w, a);
 }
 
 }  // namespace moe
