@@ -339,10 +339,17 @@ static moe_status_t route_into(moe_experts_s* h, const moe_input_t* x, const flo
   CUtensorMap tm_x, tm_w;
   const int Epad = router_tc_epad(E);
   moe_status_t st = make_map_bf16(&tm_x, x->x_bf16, (uint64_t)d, (uint64_t)T, 128);
-  if (st == MOE_OK) st = make_map_bf16(&tm_w, h->ws.w_split, (uint64_t)d, (uint64_t)3 * Epad, 256);
+  // the split planes are tile-contiguous [256 x 64] blocks: viewed as a [3 * Epad * d / 64, 64] matrix
+  if (st == MOE_OK) st = make_map_bf16(&tm_w, h->ws.w_split, 64, (uint64_t)3 * Epad * (d / 64), 256);
   if (st != MOE_OK) return st;
-  const int split = router_tc_split(T, E, d);
   MOE_CUDA(launch_split_router(router_w, E, d, h->ws.w_split, s), "router weight split");
+  if (E <= 256) {  // logits, split-K reduction and top-k in one cluster kernel
+    MOE_CUDA(launch_router_fused(tm_x, tm_w, router_bias, T, E, d, k, h->cfg.route_scale, router_fused_split(T, d), ids,
+                                 wts, h->status, h->budget_ns, s),
+             "router");
+    return MOE_OK;
+  }
+  const int split = router_tc_split(T, E, d);
   MOE_CUDA(launch_router_tc(tm_x, tm_w, T, E, d, split, h->ws.logits, h->status, h->budget_ns, s), "router logits");
   MOE_CUDA(launch_router_topk(h->ws.logits, split, router_bias, T, E, k, h->cfg.route_scale, ids, wts, s),
            "router top-k");

@@ -8,6 +8,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <float.h>
+
 #include "moe_internal.h"
 
 namespace moe {
@@ -79,6 +81,64 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64
   for (;;) {
     if (mbar_try_wait_suspend(bar, parity, 200000u)) return true;
     if (globaltimer_ns() - t0 > budget_ns) return false;
+  }
+}
+
+// ------------------------------------------------------------------------- routing
+__device__ __forceinline__ float softplus_f(float l) { return fmaxf(l, 0.f) + log1pf(expf(-fabsf(l))); }
+
+// Warp-wide top-k of one token (the sqrt-softplus router's selection).  Lane l holds expert
+// e = l + 32 i in s[i] (its score) and sel[i] (its selection key score + bias; pass -FLT_MAX where
+// e >= E).  Selects the k largest keys, ties to the lower expert id, and writes the chosen ids in
+// ascending order with weights route_scale * s_j / sum over the chosen s.  Ascending order comes from
+// ballot prefix counts (slot i first, then lane), so nothing is sorted; the sum is lane 0's
+// butterfly total, broadcast, so every weight divides by the same value.
+template <int NPL>
+__device__ __forceinline__ void warp_route_topk(const float (&s)[NPL], const float (&sel)[NPL], int E, int k,
+                                                float route_scale, int32_t* __restrict__ ids_row,
+                                                float* __restrict__ w_row) {
+  const int lane = threadIdx.x & 31;
+  uint32_t taken = 0;
+  for (int j = 0; j < k; ++j) {
+    float bv = -FLT_MAX;
+    int be = 0x7FFFFFFF;
+#pragma unroll
+    for (int i = 0; i < NPL; ++i) {
+      const bool ok = lane + 32 * i < E && !((taken >> i) & 1u);
+      if (ok && (be == 0x7FFFFFFF || sel[i] > bv)) {
+        bv = sel[i];
+        be = lane + 32 * i;
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, off);
+      const int oe = __shfl_xor_sync(0xFFFFFFFFu, be, off);
+      if (oe != 0x7FFFFFFF && (be == 0x7FFFFFFF || ov > bv || (ov == bv && oe < be))) {
+        bv = ov;
+        be = oe;
+      }
+    }
+    if ((be & 31) == lane) taken |= 1u << (be >> 5);
+  }
+  float ssum = 0.f;
+#pragma unroll
+  for (int i = 0; i < NPL; ++i)
+    if ((taken >> i) & 1u) ssum += s[i];
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) ssum += __shfl_xor_sync(0xFFFFFFFFu, ssum, off);
+  ssum = __shfl_sync(0xFFFFFFFFu, ssum, 0);
+  int base = 0;
+#pragma unroll
+  for (int i = 0; i < NPL; ++i) {
+    const bool mine = (taken >> i) & 1u;
+    const uint32_t m = __ballot_sync(0xFFFFFFFFu, mine);
+    if (mine) {
+      const int pos = base + __popc(m & ((1u << lane) - 1u));
+      ids_row[pos] = lane + 32 * i;
+      w_row[pos] = route_scale * s[i] / ssum;
+    }
+    base += __popc(m);
   }
 }
 

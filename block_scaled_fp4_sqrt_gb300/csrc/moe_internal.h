@@ -96,6 +96,10 @@ cudaError_t launch_router_logits(const __nv_bfloat16* x, const float* w, int T, 
 // Tensor-core router: split count for T rows, padded expert count, weight split, logits partials.
 int router_tc_split(int T, int E, int d);
 int router_tc_epad(int E);
+int router_fused_split(int T, int d);
+cudaError_t launch_router_fused(const CUtensorMap& tm_x, const CUtensorMap& tm_w, const float* bias, int T, int E,
+                                int d, int k, float route_scale, int split, int32_t* ids, float* wts, int* status,
+                                uint64_t budget_ns, cudaStream_t s);
 cudaError_t launch_split_router(const float* w, int E, int d, __nv_bfloat16* out, cudaStream_t s);
 cudaError_t launch_router_tc(const CUtensorMap& tm_x, const CUtensorMap& tm_w, int T, int E, int d, int split,
                              float* partial, int* status, uint64_t budget_ns, cudaStream_t s);

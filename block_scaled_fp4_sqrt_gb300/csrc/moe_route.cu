@@ -90,7 +90,6 @@ __global__ void __launch_bounds__(256) router_logits_kernel(const __nv_bfloat16*
 constexpr int kMaxPerLane = 16;  // E <= 512
 constexpr int kMaxTopK = 16;
 
-__device__ __forceinline__ float softplus_f(float l) { return fmaxf(l, 0.f) + log1pf(expf(-fabsf(l))); }
 
 // Block of 8 warps per 8 tokens.  Phase 1: every thread sums the split partials of some (token,
 // expert) pairs in a fixed order (coalesced over experts) and stores s = sqrt(softplus(l)) and
@@ -101,7 +100,7 @@ constexpr int kTopkTokens = 8;
 
 // KS = the number of split-K partials, a template argument so that the KS loads of a sum are issued
 // unconditionally and back to back (a runtime-bounded loop serialises them on the L2 latency).
-template <int KS>
+template <int KS, int NPL>
 __global__ void __launch_bounds__(512) router_topk_kernel(const float* __restrict__ partial,
                                                           const float* __restrict__ bias, int T, int E, int k,
                                                           float route_scale, int32_t* __restrict__ ids,
@@ -129,72 +128,14 @@ __global__ void __launch_bounds__(512) router_topk_kernel(const float* __restric
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int t = t0 + w;
   if (w >= kTopkTokens || t >= T) return;
-  float s[kMaxPerLane], sel[kMaxPerLane];
+  float sc[NPL], sel[NPL];
 #pragma unroll
-  for (int i = 0; i < kMaxPerLane; ++i) {
+  for (int i = 0; i < NPL; ++i) {
     const int e = lane + 32 * i;
-    s[i] = e < E ? s_s[w][e] : 0.f;
+    sc[i] = e < E ? s_s[w][e] : 0.f;
     sel[i] = e < E ? s_sel[w][e] : -FLT_MAX;
   }
-  uint32_t taken = 0;
-  int chosen[kMaxTopK];
-  float chosen_s[kMaxTopK];
-  for (int j = 0; j < k; ++j) {
-    float bv = -FLT_MAX;
-    int be = 0x7FFFFFFF;
-#pragma unroll
-    for (int i = 0; i < kMaxPerLane; ++i) {
-      const int e = lane + 32 * i;
-      const bool ok = e < E && !((taken >> i) & 1u);
-      if (ok && (be == 0x7FFFFFFF || sel[i] > bv)) {
-        bv = sel[i];
-        be = e;
-      }
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, off);
-      const int oe = __shfl_xor_sync(0xFFFFFFFFu, be, off);
-      const bool better = (oe != 0x7FFFFFFF) && (be == 0x7FFFFFFF || ov > bv || (ov == bv && oe < be));
-      if (better) {
-        bv = ov;
-        be = oe;
-      }
-    }
-    float sv = 0.f;
-    if ((be & 31) == lane) {
-      const int i_sel = be >> 5;
-#pragma unroll
-      for (int i = 0; i < kMaxPerLane; ++i)
-        if (i == i_sel) {
-          sv = s[i];
-          taken |= 1u << i;
-        }
-    }
-    sv = __shfl_sync(0xFFFFFFFFu, sv, be & 31);
-    chosen[j] = be;
-    chosen_s[j] = sv;
-  }
-  if (lane == 0) {
-    for (int a = 1; a < k; ++a) {  // insertion sort by expert id
-      const int ci = chosen[a];
-      const float cs = chosen_s[a];
-      int b = a - 1;
-      while (b >= 0 && chosen[b] > ci) {
-        chosen[b + 1] = chosen[b];
-        chosen_s[b + 1] = chosen_s[b];
-        --b;
-      }
-      chosen[b + 1] = ci;
-      chosen_s[b + 1] = cs;
-    }
-    float sum = 0.f;
-    for (int j = 0; j < k; ++j) sum += chosen_s[j];
-    for (int j = 0; j < k; ++j) {
-      ids[(size_t)t * k + j] = chosen[j];
-      wts[(size_t)t * k + j] = route_scale * chosen_s[j] / sum;
-    }
-  }
+  warp_route_topk<NPL>(sc, sel, E, k, route_scale, ids + (size_t)t * k, wts + (size_t)t * k);
 }
 
 // Hash routing: ids = the token's table row (ascending), weights route_scale / k.  Out-of-range token
@@ -254,8 +195,11 @@ cudaError_t launch_router_topk(const float* partial, int ksplit, const float* bi
   const int blocks = (T + kTopkTokens - 1) / kTopkTokens;
   switch (ksplit) {
 #define MOE_TOPK_CASE(KS) \
-  case KS: return launch_pdl(router_topk_kernel<KS>, dim3(blocks), dim3(512), 0, s, partial, bias, T, E, k, \
-                             route_scale, ids, wts);
+  case KS:                                                                                                \
+    return E <= 256 ? launch_pdl(router_topk_kernel<KS, 8>, dim3(blocks), dim3(512), 0, s, partial, bias, T, E, k, \
+                                 route_scale, ids, wts)                                                  \
+                    : launch_pdl(router_topk_kernel<KS, 16>, dim3(blocks), dim3(512), 0, s, partial, bias, T, E, k, \
+                                 route_scale, ids, wts);
     MOE_TOPK_CASE(1)
     MOE_TOPK_CASE(2)
     MOE_TOPK_CASE(4)

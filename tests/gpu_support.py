@@ -24,7 +24,11 @@ TOL_WEIGHT_REL = 1e-4
 # expert groups longer than one 32-row tile.
 MEDIUM = synth.Workload("medium", 512, 1024, 512, 16, 4, description="T=512, d=1024, f=512, 16 experts top-4")
 
-WORKLOADS = dict(synth.WORKLOADS, medium=MEDIUM)
+# More routed experts than one 256-wide router tile: the learned router's two-kernel path (logits, then a
+# separate split-K reduction with top-k over two expert tiles) instead of the fused cluster router.
+WIDE = synth.Workload("wide", 96, 512, 128, 384, 6, description="T=96, d=512, f=128, 384 experts top-6")
+
+WORKLOADS = dict(synth.WORKLOADS, medium=MEDIUM, wide=WIDE)
 
 
 def device():

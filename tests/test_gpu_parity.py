@@ -17,7 +17,7 @@ from gpu_support import (TOL_WEIGHT_REL, WORKLOADS, assert_close, bf16_to_f64, c
 
 pytestmark = pytest.mark.gpu
 
-SMALL = ["tiny", "medium"]
+SMALL = ["tiny", "medium", "wide"]
 FULL = ["verify8", "verify512", "hash512", "prefill8192"]
 
 
