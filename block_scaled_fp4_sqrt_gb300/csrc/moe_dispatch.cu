@@ -174,10 +174,17 @@ __global__ void __launch_bounds__(1024) groupscan_kernel(const int32_t* __restri
   }
 }
 
-// One block per token, one thread per 32-element MXFP8 block.  Every warp derives the token's rows
-// (rank among the lower tokens of its 32-token chunk by ballot, plus the chunk's exclusive base); four
-// consecutive threads (one 128-element K group) pack their scale bytes into one 32-bit word, which is
-// one word of a scale atom.
+// One block per token, one thread per 32-element MXFP8 block.
+//  * The token's x row is loaded first: nothing about it depends on the routing.
+//  * The ids of the token's 32-token chunk go to shared memory; warp 0 takes one ballot per routing
+//    slot j (rank of the token among the lower tokens of its chunk that chose the same expert), and
+//    lanes 0..k-1 then look up their expert's chunk base and offsets at the same time, so the block
+//    waits for one round of dependent loads instead of k.  The destinations (k routed rows and the
+//    shared row) are published in shared memory.
+//  * Each warp quantises 32 MX blocks (1 KB of E4M3) and stores them to every destination row with two
+//    instructions of 512 contiguous bytes (lane l stores 16-byte chunk l of each half, moved there by
+//    shuffles); four consecutive threads (one 128-element K group) pack their scale bytes into one
+//    32-bit word, which is one word of a scale atom.
 __global__ void __launch_bounds__(128) gather_kernel(
     const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ ids, const float* __restrict__ wts,
     const int32_t* __restrict__ chunk_base, int n_chunks, const int32_t* __restrict__ offsets,
@@ -185,66 +192,85 @@ __global__ void __launch_bounds__(128) gather_kernel(
     uint8_t* __restrict__ a_q, uint8_t* __restrict__ a_sf_atoms, uint8_t* __restrict__ a_s_rows,
     int32_t* __restrict__ perm_tok, int32_t* __restrict__ inv_pos, float* __restrict__ row_w) {
   constexpr int kMaxDst = 17;  // top-k <= 16, plus the shared row
+  __shared__ int s_ids[32 * 16];
+  __shared__ int s_row[kMaxDst], s_tile[kMaxDst], s_n[kMaxDst];
   pdl_trigger();
   pdl_wait();
-  const int lane = threadIdx.x & 31;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int nb = d / 32;
+  const int n_dst = k + (has_shared ? 1 : 0);
   for (int t = blockIdx.x; t < T; t += gridDim.x) {
-    const int chunk = t >> 5, tl = (chunk << 5) + lane;
-    // each lane holds the ids of one token of the chunk; the block's token is lane t & 31
-    int my_ids[16];
+    const int chunk = t >> 5, tc = t & 31;
+    // 1. this thread's first MX block of the row (the loop below loads the rest, if d > 32 * threads)
+    uint4 raw[4];
+    {
+      const int b = threadIdx.x;
+      if (b < nb) {
+        const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * d + b * 32);
 #pragma unroll
-    for (int jj = 0; jj < 16; ++jj)
-      my_ids[jj] = (jj < k && tl < T) ? clamp_id(__ldg(&ids[(size_t)tl * k + jj]), E, nullptr) : -1;
-    int dst_row[kMaxDst], dst_tile[kMaxDst], dst_n[kMaxDst];
-    int n_dst = 0;
-    for (int j = 0; j < k; ++j) {
-      int mine = -1;
-#pragma unroll
-      for (int jj = 0; jj < 16; ++jj)
-        if (jj == j) mine = my_ids[jj];
-      const int e = __shfl_sync(0xFFFFFFFFu, mine, t & 31);
-      bool hit = false;
-      if (tl < t) {
-#pragma unroll
-        for (int jj = 0; jj < 16; ++jj) hit |= my_ids[jj] == e;
-      }
-      const int rank = __popc(__ballot_sync(0xFFFFFFFFu, hit));
-      const int local = chunk_base[(size_t)e * n_chunks + chunk] + rank;
-      const int row = offsets[e] + local;
-      dst_row[n_dst] = row;
-      dst_tile[n_dst] = tile_off[e] + local / bn;
-      dst_n[n_dst] = local % bn;
-      ++n_dst;
-      if (threadIdx.x == 0) {
-        perm_tok[row] = t;
-        inv_pos[(size_t)t * k + j] = row;
-        if (row_w) row_w[row] = wts ? wts[(size_t)t * k + j] : 1.0f;
+        for (int c = 0; c < 4; ++c) raw[c] = __ldg(src + c);
       }
     }
-    if (has_shared) {
-      const int row = offsets[E] + t;
-      dst_row[n_dst] = row;
-      dst_tile[n_dst] = tile_off[E] + t / bn;
-      dst_n[n_dst] = t % bn;
-      ++n_dst;
-      if (threadIdx.x == 0) {
+    // 2. the chunk's ids
+    for (int i = threadIdx.x; i < 32 * k; i += blockDim.x) {
+      const int tt = (chunk << 5) + i / k;
+      s_ids[i] = tt < T ? clamp_id(__ldg(&ids[(size_t)(chunk << 5) * k + i]), E, nullptr) : -1;
+    }
+    __syncthreads();
+    // 3. destinations
+    if (warp == 0) {
+      int my_ids[16];
+#pragma unroll
+      for (int jj = 0; jj < 16; ++jj) my_ids[jj] = jj < k ? s_ids[lane * k + jj] : -2;
+      int my_e = 0, my_rank = 0;
+      for (int j = 0; j < k; ++j) {
+        const int e = s_ids[tc * k + j];
+        bool hit = false;
+        if (lane < tc) {
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) hit |= my_ids[jj] == e;
+        }
+        const int rank = __popc(__ballot_sync(0xFFFFFFFFu, hit));
+        if (lane == j) {
+          my_e = e;
+          my_rank = rank;
+        }
+      }
+      if (lane < k) {
+        const int local = chunk_base[(size_t)my_e * n_chunks + chunk] + my_rank;
+        const int row = offsets[my_e] + local;
+        s_row[lane] = row;
+        s_tile[lane] = tile_off[my_e] + local / bn;
+        s_n[lane] = local % bn;
+        perm_tok[row] = t;
+        inv_pos[(size_t)t * k + lane] = row;
+        if (row_w) row_w[row] = wts ? wts[(size_t)t * k + lane] : 1.0f;
+      } else if (lane == k && has_shared) {
+        const int row = offsets[E] + t;
+        s_row[lane] = row;
+        s_tile[lane] = tile_off[E] + t / bn;
+        s_n[lane] = t % bn;
         perm_tok[row] = t;
         if (row_w) row_w[row] = 1.0f;
       }
     }
+    __syncthreads();
+    // 4. quantise and store
     for (int b0 = 0; b0 < nb; b0 += blockDim.x) {
       const int b = b0 + threadIdx.x;
       const bool on = b < nb;
+      if (b0 > 0 && on) {
+        const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * d + b * 32);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) raw[c] = __ldg(src + c);
+      }
       uint32_t packed[8];
       uint32_t byte = 0;
       if (on) {
-        const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * d + b * 32);
         float v[32];
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          const uint4 raw = __ldg(src + c);
-          const __nv_bfloat16* hv = reinterpret_cast<const __nv_bfloat16*>(&raw);
+          const __nv_bfloat16* hv = reinterpret_cast<const __nv_bfloat16*>(&raw[c]);
 #pragma unroll
           for (int i = 0; i < 8; ++i) v[c * 8 + i] = __bfloat162float(hv[i]);
         }
@@ -260,27 +286,50 @@ __global__ void __launch_bounds__(128) gather_kernel(
           packed[i] = lo | (hi << 16);
         }
         byte = (uint32_t)(se + 127);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) packed[i] = 0u;
       }
       uint32_t word = byte;
       word |= __shfl_down_sync(0xFFFFFFFFu, byte, 1) << 8;
       word |= __shfl_down_sync(0xFFFFFFFFu, byte, 2) << 16;
       word |= __shfl_down_sync(0xFFFFFFFFu, byte, 3) << 24;
-      if (!on) continue;
+      // the warp's 32 MX blocks are 64 chunks of 16 bytes; half h of the stores is chunks 32h .. 32h+31,
+      // and chunk c is half (c & 1) of MX block c / 2, i.e. of lane c / 2 of this warp
+      const int wb0 = b - lane;  // the warp's first MX block
+      uint4 outv[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int src_lane = 16 * h + (lane >> 1);
+        uint32_t w4[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t lo = __shfl_sync(0xFFFFFFFFu, packed[j], src_lane);
+          const uint32_t hi = __shfl_sync(0xFFFFFFFFu, packed[4 + j], src_lane);
+          w4[j] = (lane & 1) ? hi : lo;
+        }
+        outv[h] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+      }
       const int grp = b >> 2;
       for (int q = 0; q < n_dst; ++q) {
-        uint4* dst = reinterpret_cast<uint4*>(a_q + (size_t)dst_row[q] * d + b * 32);
-        dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-        dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
-        if ((b & 3) == 0) {
+        const int row = s_row[q];
+        uint8_t* rowp = a_q + (size_t)row * d;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int blk = wb0 + 16 * h + (lane >> 1);  // MX block whose half this lane stores
+          if (blk < nb) reinterpret_cast<uint4*>(rowp + (size_t)blk * 32)[lane & 1] = outv[h];
+        }
+        if (on && (b & 3) == 0) {
           if (a_sf_atoms) {
-            const int n = dst_n[q];
-            *reinterpret_cast<uint32_t*>(a_sf_atoms + ((size_t)dst_tile[q] * (d / kKGroup) + grp) * kSfAtomBytes +
+            const int n = s_n[q];
+            *reinterpret_cast<uint32_t*>(a_sf_atoms + ((size_t)s_tile[q] * (d / kKGroup) + grp) * kSfAtomBytes +
                                          (n & 31) * 16 + ((n >> 5) & 3) * 4) = word;
           }
-          if (a_s_rows) *reinterpret_cast<uint32_t*>(a_s_rows + (size_t)dst_row[q] * nb + b) = word;
+          if (a_s_rows) *reinterpret_cast<uint32_t*>(a_s_rows + (size_t)row * nb + b) = word;
         }
       }
     }
+    __syncthreads();  // s_ids and the destinations are rewritten by the next token
   }
 }
 
