@@ -357,8 +357,38 @@ __global__ void combine_kernel(const float* __restrict__ y_rows, const int32_t* 
       acc[6] += b.z;
       acc[7] += b.w;
     };
-    for (int j = 0; j < k; ++j) add_row(__ldg(&inv_pos[(size_t)t * k + j]));
-    if (has_shared) add_row(R + t);
+    const int n = k + (has_shared ? 1 : 0);
+    if (n <= 8) {
+      // all row indices, then all row loads, then the sum in slot order: the loads overlap instead of
+      // queueing behind one another's latency
+      int rows[8];
+      float4 va[8], vb[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        rows[j] = j < k ? __ldg(&inv_pos[(size_t)t * k + j]) : (j == k && has_shared ? R + t : -1);
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (rows[j] >= 0) {
+          const float4* src = reinterpret_cast<const float4*>(y_rows + (size_t)rows[j] * d) + 2 * c8;
+          va[j] = __ldg(src);
+          vb[j] = __ldg(src + 1);
+        }
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (rows[j] >= 0) {
+          acc[0] += va[j].x;
+          acc[1] += va[j].y;
+          acc[2] += va[j].z;
+          acc[3] += va[j].w;
+          acc[4] += vb[j].x;
+          acc[5] += vb[j].y;
+          acc[6] += vb[j].z;
+          acc[7] += vb[j].w;
+        }
+    } else {
+      for (int j = 0; j < k; ++j) add_row(__ldg(&inv_pos[(size_t)t * k + j]));
+      if (has_shared) add_row(R + t);
+    }
     uint4 o;
     __nv_bfloat16* ov = reinterpret_cast<__nv_bfloat16*>(&o);
 #pragma unroll
