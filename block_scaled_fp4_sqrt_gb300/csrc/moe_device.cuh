@@ -98,28 +98,29 @@ __device__ __forceinline__ void warp_route_topk(const float (&s)[NPL], const flo
                                                 float route_scale, int32_t* __restrict__ ids_row,
                                                 float* __restrict__ w_row) {
   const int lane = threadIdx.x & 31;
+  // order-preserving 32-bit keys of the selection values (larger float -> larger key), so that one
+  // round is a local scan, a warp max of the keys and a warp min of the ids holding it
+  uint32_t key[NPL];
+#pragma unroll
+  for (int i = 0; i < NPL; ++i) {
+    const uint32_t u = __float_as_uint(sel[i]);
+    key[i] = lane + 32 * i < E ? ((u & 0x80000000u) ? ~u : (u | 0x80000000u)) : 0u;
+  }
   uint32_t taken = 0;
   for (int j = 0; j < k; ++j) {
-    float bv = -FLT_MAX;
-    int be = 0x7FFFFFFF;
+    uint32_t best = 0;
+    int bi = NPL;
 #pragma unroll
-    for (int i = 0; i < NPL; ++i) {
-      const bool ok = lane + 32 * i < E && !((taken >> i) & 1u);
-      if (ok && (be == 0x7FFFFFFF || sel[i] > bv)) {
-        bv = sel[i];
-        be = lane + 32 * i;
+    for (int i = 0; i < NPL; ++i)
+      if (!((taken >> i) & 1u) && lane + 32 * i < E && (bi == NPL || key[i] > best)) {
+        best = key[i];
+        bi = i;
       }
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, off);
-      const int oe = __shfl_xor_sync(0xFFFFFFFFu, be, off);
-      if (oe != 0x7FFFFFFF && (be == 0x7FFFFFFF || ov > bv || (ov == bv && oe < be))) {
-        bv = ov;
-        be = oe;
-      }
-    }
-    if ((be & 31) == lane) taken |= 1u << (be >> 5);
+    const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, bi < NPL ? best : 0u);
+    // lowest expert id among the lanes holding the maximum (a lane's own first maximum is its lowest)
+    const uint32_t cand = (bi < NPL && best == m) ? (uint32_t)(lane + 32 * bi) : 0xFFFFFFFFu;
+    const uint32_t win = __reduce_min_sync(0xFFFFFFFFu, cand);
+    if ((int)(win & 31u) == lane) taken |= 1u << (win >> 5);
   }
   float ssum = 0.f;
 #pragma unroll

@@ -222,7 +222,8 @@ __global__ void __launch_bounds__(192, 1) router_tc_kernel(const __grid_constant
 // No partial reaches global memory.
 constexpr int kFThreads = 384;                 // warps 0 TMA, 1 MMA, 2..5 TMEM drain; all 12 select
 constexpr int kFStride = kRN + 4;              // partial row stride in floats (1040 B: conflict-free)
-static_assert(kRM * kFStride * 4 <= kRStages * kRStage, "partials fit in the drained pipeline buffers");
+static_assert(kRM * kFStride * 4 + (kFThreads / 32) * kRN * 4 <= kRStages * kRStage,
+              "partials and the per-warp logit rows fit in the drained pipeline buffers");
 
 struct FusedArgs {
   const float* bias;
@@ -247,9 +248,9 @@ __device__ __forceinline__ uint32_t cluster_map(uint32_t saddr, uint32_t rank) {
 
 // Volatile (kept in order after the cluster barrier, which is a compiler barrier too) but without a
 // memory clobber, so that a run of these loads issues back to back before their sum consumes them.
-__device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+__device__ __forceinline__ float4 ld_cluster_f4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
   return v;
 }
 
@@ -375,24 +376,38 @@ __global__ void __launch_bounds__(kFThreads, 1) router_fused_kernel(const __grid
   const uint32_t part_addr = smem_addr(smem);
 #pragma unroll
   for (int src = 0; src < S; ++src) remote[src] = cluster_map(part_addr, (uint32_t)src);
+  // the warp's logit row, re-read in the one-expert-per-lane layout of the selection
+  float* lrow = reinterpret_cast<float*>(smem + kRM * kFStride * 4) + warp * kRN;
   for (int rr = warp; rr < rows_per; rr += kFThreads / 32) {
     const int r = z * rows_per + rr, t = t0 + r;
     if (t >= a.T) continue;  // warp-uniform
+    // lane l sums experts 4l..4l+3 and 128+4l..: per half, S 16-byte loads in flight at once
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint32_t off = (uint32_t)((r * kFStride + 128 * h + 4 * lane) * 4);
+      float4 v[S];
+#pragma unroll
+      for (int src = 0; src < S; ++src) v[src] = ld_cluster_f4(remote[src] + off);
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int src = 0; src < S; ++src) {
+        acc.x += v[src].x;
+        acc.y += v[src].y;
+        acc.z += v[src].z;
+        acc.w += v[src].w;
+      }
+      reinterpret_cast<float4*>(lrow + 128 * h)[lane] = acc;
+    }
+    __syncwarp();
     float sc[8], sel[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const int e = lane + 32 * i;
-      const uint32_t off = (uint32_t)((r * kFStride + e) * 4);
-      float v[S];
-#pragma unroll
-      for (int src = 0; src < S; ++src) v[src] = ld_cluster_f32(remote[src] + off);
-      float l = 0.f;
-#pragma unroll
-      for (int src = 0; src < S; ++src) l += v[src];
-      const float sv = sqrtf(softplus_f(l));
+      const float sv = sqrtf(softplus_f(lrow[e]));
       sc[i] = e < a.E ? sv : 0.f;
       sel[i] = e < a.E ? sv + __ldg(&a.bias[e]) : -FLT_MAX;
     }
+    __syncwarp();
     warp_route_topk<8>(sc, sel, a.E, a.k, a.route_scale, a.ids + (size_t)t * a.k, a.wts + (size_t)t * a.k);
   }
   cluster_sync_all();  // no CTA leaves while another still reads its partial
