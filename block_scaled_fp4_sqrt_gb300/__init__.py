@@ -25,7 +25,8 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
 EXPORTED = ("moe_experts_create", "moe_experts_set_hash_table", "moe_workspace_size", "moe_set_workspace",
             "moe_route", "moe_permute", "moe_expert_ffn", "moe_forward", "moe_get_routing", "moe_check",
             "moe_set_wait_budget", "moe_experts_destroy", "moe_status_string", "moe_last_error",
-            "moe_testing_stall_loads", "moe_set_stage_events", "moe_route_noalloc", "moe_measure_mxf8f6f4_peak")
+            "moe_testing_stall_loads", "moe_set_stage_events", "moe_route_noalloc", "moe_measure_mxf8f6f4_peak",
+            "moe_stack_create", "moe_stack_forward", "moe_stack_destroy")
 
 MOE_N_STAGES = 5
 STAGE_NAMES = ("route", "dispatch", "gemm_gate_up", "gemm_down", "combine")
@@ -40,6 +41,11 @@ class MoEError(RuntimeError):
 class moe_config_t(ctypes.Structure):
     _fields_ = [("d_model", ctypes.c_int32), ("d_ff", ctypes.c_int32), ("n_experts", ctypes.c_int32),
                 ("top_k", ctypes.c_int32), ("route_scale", ctypes.c_float), ("swiglu_limit", ctypes.c_float)]
+
+
+class moe_stack_layer_t(ctypes.Structure):
+    _fields_ = [("experts", ctypes.c_void_p), ("shared", ctypes.c_void_p), ("router_w", ctypes.c_void_p),
+                ("router_bias", ctypes.c_void_p)]
 
 
 class moe_input_t(ctypes.Structure):
@@ -71,6 +77,10 @@ def lib() -> ctypes.CDLL:
         L.moe_set_stage_events.argtypes = [vp, ctypes.POINTER(vp), i32]
         L.moe_route_noalloc.argtypes = [cfgp, inp, vp, vp, vp, vp, vp]
         L.moe_measure_mxf8f6f4_peak.argtypes = [i32, ctypes.POINTER(ctypes.c_double)]
+        L.moe_stack_create.argtypes = [ctypes.POINTER(moe_stack_layer_t), i32, i32, ctypes.POINTER(vp)]
+        L.moe_stack_forward.argtypes = [vp, inp, vp, vp, vp]
+        L.moe_stack_destroy.argtypes = [vp]
+        L.moe_stack_destroy.restype = None
         L.moe_experts_destroy.argtypes = [vp]
         L.moe_experts_destroy.restype = None
         L.moe_status_string.argtypes = [st]
@@ -78,7 +88,8 @@ def lib() -> ctypes.CDLL:
         L.moe_last_error.argtypes = []
         L.moe_last_error.restype = ctypes.c_char_p
         for name in EXPORTED:
-            if name not in ("moe_workspace_size", "moe_experts_destroy", "moe_status_string", "moe_last_error"):
+            if name not in ("moe_workspace_size", "moe_experts_destroy", "moe_status_string", "moe_last_error",
+                            "moe_stack_destroy"):
                 getattr(L, name).restype = st
         _LIB = L
     return _LIB
@@ -195,6 +206,26 @@ def moe_route_noalloc(cfg: moe_config_t, x, router_w, router_bias, topk_ids, top
     """Learned router without a handle or workspace (fixed library scratch; see include/moe.h)."""
     _ok("moe_route_noalloc", lib().moe_route_noalloc(ctypes.byref(cfg), ctypes.byref(_input(x)), _p(router_w),
                                                      _p(router_bias), _p(topk_ids), _p(topk_w), _stream(stream)))
+
+
+def moe_stack_create(layers, use_graph: bool):
+    """layers: sequence of (experts handle, shared handle or None, router_w or None, router_bias or None)."""
+    arr = (moe_stack_layer_t * len(layers))()
+    for i, (h, sh, rw, rb) in enumerate(layers):
+        arr[i] = moe_stack_layer_t(h, sh, None if rw is None else rw.data_ptr(), None if rb is None else rb.data_ptr())
+    out = ctypes.c_void_p()
+    _ok("moe_stack_create", lib().moe_stack_create(arr, len(layers), 1 if use_graph else 0, ctypes.byref(out)))
+    return out
+
+
+def moe_stack_forward(stack, x, out, scratch, token_ids=None, stream=None) -> None:
+    _ok("moe_stack_forward", lib().moe_stack_forward(stack, ctypes.byref(_input(x, token_ids)), _p(out), _p(scratch),
+                                                     _stream(stream)))
+
+
+def moe_stack_destroy(stack) -> None:
+    if stack:
+        lib().moe_stack_destroy(stack)
 
 
 def moe_experts_destroy(h) -> None:
@@ -330,6 +361,49 @@ class MoELayer:
         for h in self._handles:
             moe_experts_destroy(h)
         self._handles = []
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class MoEStack:
+    """Layers run back to back by ``moe_stack_forward``: x_{l+1} = bf16(x_l + layer_l(x_l)).
+
+    ``layers`` are ``MoELayer`` objects (they keep their own handles and weights); all of them get one
+    shared workspace for ``max_T`` rows, and the stack owns the scratch buffer of the residual stream.
+    With ``use_graph`` the whole stack is captured once into a CUDA graph and replayed."""
+
+    def __init__(self, layers, max_T: int, use_graph: bool = True, device=None):
+        self.layers = list(layers)
+        self.device = torch.device(device or self.layers[0].device)
+        self.d, self.max_T = self.layers[0].d, max_T
+        with torch.cuda.device(self.device):
+            nbytes = max(moe_workspace_size(ly.cfg, max_T) for ly in self.layers)
+            self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=self.device)
+            for ly in self.layers:
+                moe_set_workspace(ly.h, self.workspace, max_T)
+            self.scratch = torch.empty((max_T, self.d), dtype=torch.bfloat16, device=self.device)
+            self.stack = moe_stack_create([(ly.h, ly.h_shared, ly.router_w, ly.router_bias) for ly in self.layers],
+                                          use_graph)
+
+    def forward(self, x: torch.Tensor, token_ids: torch.Tensor | None = None, out: torch.Tensor | None = None,
+                stream=None) -> torch.Tensor:
+        if out is None:
+            out = torch.empty((x.shape[0], self.d), dtype=torch.bfloat16, device=self.device)
+        moe_stack_forward(self.stack, x, out, self.scratch[: x.shape[0]], token_ids, stream)
+        return out
+
+    def check(self) -> None:
+        for ly in self.layers:
+            ly.check()
+
+    def close(self) -> None:
+        if getattr(self, "stack", None):
+            moe_stack_destroy(self.stack)
+            self.stack = None
 
     def __del__(self):
         try:

@@ -465,6 +465,15 @@ moe_status_t moe_set_stage_events(moe_experts_t h, void* const* events, int32_t 
 
 moe_status_t moe_forward(const moe_input_t* x, const float* router_w, const float* router_bias, moe_experts_t h,
                          moe_experts_t sh, void* out_bf16, moe_stream_t stream) {
+  return moe::forward_impl(x, router_w, router_bias, h, sh, out_bf16, nullptr, stream);
+}
+
+}  // extern "C"
+
+namespace moe {
+
+moe_status_t forward_impl(const moe_input_t* x, const float* router_w, const float* router_bias, moe_experts_t h,
+                          moe_experts_t sh, void* out_bf16, const void* residual_bf16, moe_stream_t stream) {
   moe_status_t st = check_input(h, x);
   if (st != MOE_OK) return st;
   if (h->n != h->cfg.n_experts) return fail(MOE_ERR_INVALID_ARG, "routed set must hold cfg.n_experts experts");
@@ -475,6 +484,7 @@ moe_status_t moe_forward(const moe_input_t* x, const float* router_w, const floa
   }
   if (x->T > 0 && !out_bf16) return fail(MOE_ERR_INVALID_ARG, "out is NULL");
   if (out_bf16 && !aligned(out_bf16, 16)) return fail(MOE_ERR_INVALID_ARG, "out must be 16-byte aligned");
+  if (residual_bf16 && !aligned(residual_bf16, 16)) return fail(MOE_ERR_INVALID_ARG, "residual must be 16-byte aligned");
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const int T = x->T, E = h->cfg.n_experts, k = h->cfg.top_k, d = h->cfg.d_model;
   mark_stage(h, 0, s);
@@ -505,11 +515,20 @@ moe_status_t moe_forward(const moe_input_t* x, const float* router_w, const floa
   st = run_ffn(h, sh, rows, E, h->ws.a_q, h->ws.a_sf, h->ws.row_w, h->ws.y_rows, nullptr, dm.max_tiles, bn, true, s);
   if (st != MOE_OK) return st;
   mark_stage(h, 4, s);
-  MOE_CUDA(launch_combine(h->ws.y_rows, h->ws.inv_pos, T, d, k, R, has_shared, static_cast<__nv_bfloat16*>(out_bf16), s),
+  MOE_CUDA(launch_combine(h->ws.y_rows, h->ws.inv_pos, T, d, k, R, has_shared,
+                          static_cast<const __nv_bfloat16*>(residual_bf16), static_cast<__nv_bfloat16*>(out_bf16), s),
            "combine");
   mark_stage(h, 5, s);
   return MOE_OK;
 }
+
+int experts_d_model(moe_experts_t h) { return h ? h->cfg.d_model : 0; }
+
+int experts_has_hash_table(moe_experts_t h) { return h && h->hash_table ? 1 : 0; }
+
+}  // namespace moe
+
+extern "C" {
 
 moe_status_t moe_get_routing(moe_experts_t h, const int32_t** ids, const float** w, int32_t* T) {
   if (!h || !ids || !w || !T) return fail(MOE_ERR_INVALID_ARG, "NULL argument");

@@ -335,7 +335,8 @@ __global__ void __launch_bounds__(128) gather_kernel(
 
 // out[t, c] = bf16( sum_j Yr[inv_pos[t, j], c] + Yr[R + t, c] ), fp32 rows, 8 columns per thread
 __global__ void combine_kernel(const float* __restrict__ y_rows, const int32_t* __restrict__ inv_pos, int T, int d,
-                               int k, int R, int has_shared, __nv_bfloat16* __restrict__ out) {
+                               int k, int R, int has_shared, const __nv_bfloat16* residual,
+                               __nv_bfloat16* out) {
   pdl_trigger();
   pdl_wait();
   const int vec_per_row = d / 8;
@@ -343,8 +344,15 @@ __global__ void combine_kernel(const float* __restrict__ y_rows, const int32_t* 
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
     const int t = (int)(i / vec_per_row), c8 = (int)(i % vec_per_row);
     float acc[8];
+    if (residual) {  // a residual stream enters first: out = bf16(x + sum of the rows); out may alias it
+      const uint4 rv = reinterpret_cast<const uint4*>(residual + (size_t)t * d)[c8];
+      const __nv_bfloat16* rh = reinterpret_cast<const __nv_bfloat16*>(&rv);
 #pragma unroll
-    for (int q = 0; q < 8; ++q) acc[q] = 0.f;
+      for (int q = 0; q < 8; ++q) acc[q] = __bfloat162float(rh[q]);
+    } else {
+#pragma unroll
+      for (int q = 0; q < 8; ++q) acc[q] = 0.f;
+    }
     auto add_row = [&](int r) {
       const float4* src = reinterpret_cast<const float4*>(y_rows + (size_t)r * d) + 2 * c8;
       const float4 a = __ldg(src), b = __ldg(src + 1);
@@ -442,12 +450,13 @@ cudaError_t launch_gather(const __nv_bfloat16* x, const int32_t* ids, const floa
 }
 
 cudaError_t launch_combine(const float* y_rows, const int32_t* inv_pos, int T, int d, int k, int R,
-                           int has_shared, __nv_bfloat16* out, cudaStream_t s) {
+                           int has_shared, const __nv_bfloat16* residual, __nv_bfloat16* out, cudaStream_t s) {
   const size_t total = (size_t)T * (d / 8);
   int blocks = (int)((total + 255) / 256);
   if (blocks > 152 * 16) blocks = 152 * 16;
   if (blocks < 1) blocks = 1;
-  return launch_pdl(combine_kernel, dim3(blocks), dim3(256), 0, s, y_rows, inv_pos, T, d, k, R, has_shared, out);
+  return launch_pdl(combine_kernel, dim3(blocks), dim3(256), 0, s, y_rows, inv_pos, T, d, k, R, has_shared, residual,
+                    out);
 }
 
 }  // namespace moe

@@ -9,6 +9,8 @@
 
 #include <utility>
 
+#include "moe.h"
+
 namespace moe {
 
 // Device status bits (sticky, OR-ed into the handle's status word).
@@ -68,6 +70,12 @@ struct Workspace {
 
 // Text returned by moe_last_error() on this thread.
 void set_last_error(const char* msg);
+
+// moe_forward with an optional bf16 residual stream: out = bf16(residual + layer(x)) (residual may alias out).
+moe_status_t forward_impl(const moe_input_t* x, const float* router_w, const float* router_bias, moe_experts_t h,
+                          moe_experts_t sh, void* out_bf16, const void* residual_bf16, moe_stream_t stream);
+int experts_d_model(moe_experts_t h);
+int experts_has_hash_table(moe_experts_t h);
 
 // Launch with programmatic stream serialization: the kernel may be scheduled before the previous kernel
 // in the stream has finished (it must call pdl_wait() before touching global memory, see moe_device.cuh).
@@ -149,7 +157,7 @@ cudaError_t launch_gemm_down(const CUtensorMap& w_routed, const CUtensorMap& w_s
                              const float* row_w, float* y_f32, __nv_bfloat16* y_bf16, int* status,
                              uint64_t wait_budget_ns, int stall_loads, int tile_rows, int num_sms, cudaStream_t s);
 
-cudaError_t launch_combine(const float* y_rows, const int32_t* inv_pos, int T, int d, int k, int R,
-                           int has_shared, __nv_bfloat16* out, cudaStream_t s);
+cudaError_t launch_combine(const float* y_rows, const int32_t* inv_pos, int T, int d, int k, int R, int has_shared,
+                           const __nv_bfloat16* residual, __nv_bfloat16* out, cudaStream_t s);
 
 }  // namespace moe

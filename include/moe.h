@@ -198,6 +198,56 @@ MOE_API moe_status_t moe_route_noalloc(const moe_config_t* cfg, const moe_input_
                                        const float* router_bias, int32_t* topk_ids, float* topk_w,
                                        moe_stream_t stream);
 
+/*
+ * A stack of MoE layers run back to back on one stream.  It is the MoE part of a whole model in the
+ * decode / verify regime: the model card's "Model Architecture and Objective" gives 43 layers, the first
+ * ones hash-routed.  Every layer's experts stay resident in HBM.
+ *
+ * Layer l reads the bf16 residual stream x_l and writes x_{l+1} = bf16(x_l + moe_forward_l(x_l)).  The
+ * residual enters the combine's fixed-order fp32 sum first, then the routed rows, then the shared row.
+ *
+ * moe_stack_layer_t (one layer)
+ *   experts      required; its hash table (moe_experts_set_hash_table) makes the layer hash-routed.
+ *   shared       may be NULL.
+ *   router_w     required exactly when the layer has no hash table; NULL on hash layers.
+ *   router_bias  likewise.
+ * The stack keeps these pointers; the caller owns the handles and buffers and keeps them alive.  Every
+ * layer handle needs a workspace (moe_set_workspace).  Layers may share one workspace: they run one after
+ * the other on the same stream.
+ *
+ * moe_stack_create
+ *   Validates the layers (same d_model; router weights exactly on the non-hash layers).
+ *   use_graph != 0: moe_stack_forward records all layers' launches once into a CUDA graph and replays it.
+ *   Returns MOE_ERR_INVALID_ARG on bad layers.
+ *
+ * moe_stack_forward
+ *   x           bf16 [T, d] (its token_ids serve the hash layers).
+ *   out         bf16 [T, d]: receives x_L.
+ *   scratch     bf16 [T, d]: intermediate x_l; needed when there is more than one layer.
+ *   x, out and scratch must be distinct and 16-byte aligned.
+ *   Without graph mode: enqueues L moe_forward-equivalent launch sequences on the stream.
+ *   With graph mode:
+ *     - On the first call, or when x, token_ids, out, scratch or T differ from the captured ones, it runs
+ *       the layers once directly on a private stream, captures them into a graph there, and synchronises.
+ *       The call returns with the result already in out.
+ *     - Otherwise it launches the cached graph on the stream.
+ *   Device-side status is reported per layer handle by moe_check.  Host-side validation and CUDA errors
+ *   are returned.
+ */
+typedef struct moe_stack_s* moe_stack_t;
+typedef struct {
+  moe_experts_t experts;
+  moe_experts_t shared;
+  const float* router_w;
+  const float* router_bias;
+} moe_stack_layer_t;
+
+MOE_API moe_status_t moe_stack_create(const moe_stack_layer_t* layers, int32_t n_layers, int32_t use_graph,
+                                      moe_stack_t* out);
+MOE_API moe_status_t moe_stack_forward(moe_stack_t stack, const moe_input_t* x, void* out_bf16, void* scratch_bf16,
+                                       moe_stream_t stream);
+MOE_API void moe_stack_destroy(moe_stack_t stack);
+
 MOE_API void moe_experts_destroy(moe_experts_t experts);
 MOE_API const char* moe_status_string(moe_status_t status);
 /* Text of the last host-side error on this thread ("" if none). */

@@ -95,6 +95,22 @@ def bf16_value(h: int) -> float:
     return _lib().orc_bf16_value(int(h))
 
 
+def bf16_encode(v) -> np.ndarray:
+    """fp64 values -> bf16 bit patterns, round to nearest with ties to even, straight from fp64 (no
+    intermediate fp32 rounding).  v = m 2^e with 0.5 <= |m| < 1; bf16 keeps 8 significant bits."""
+    v = np.asarray(v, dtype=np.float64)
+    m, e = np.frexp(v)
+    q = np.rint(m * 256.0) / 256.0  # numpy rint rounds halves to even
+    r = np.ldexp(q, e).astype(np.float32)  # exact: 8 significant bits
+    return (r.view(np.uint32) >> 16).astype(np.uint16)
+
+
+def stack_step(x_bf16, y) -> np.ndarray:
+    """One layer of a stack's bf16 residual stream: x_{l+1} = bf16(x_l + y_l), the sum in fp64."""
+    x = (np.asarray(x_bf16, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    return bf16_encode(x + np.asarray(y, dtype=np.float64))
+
+
 def mx_scale_exp(amax: float, emax_elem: int) -> int:
     return _lib().orc_mx_scale_exp(float(amax), int(emax_elem))
 

@@ -58,6 +58,9 @@ def test_host_side_validation_without_gpu(libmoe):
     assert L.moe_check(None, None) == 1
     assert L.moe_set_workspace(None, None, 0, 1) == 1
     assert L.moe_status_string(6) == b"device wait timed out"
+    st = ctypes.c_void_p()
+    assert L.moe_stack_create(None, 0, 0, ctypes.byref(st)) == 1 and not st.value
+    assert L.moe_stack_forward(None, None, None, None, None) == 1
 
 
 def test_workspace_size_grows_with_T(libmoe):

@@ -183,3 +183,35 @@ def test_mxfp4_values_already_on_grid_are_unchanged():
 def test_bf16_decode(h):
     import struct
     assert oracle.bf16_value(h) == struct.unpack("<f", struct.pack("<I", h << 16))[0]
+
+
+def test_bf16_encode_round_trip_and_ties():
+    h = np.arange(65536, dtype=np.uint32)
+    with np.errstate(invalid="ignore"):  # the NaN patterns
+        v = (h << 16).view(np.float32).astype(np.float64)
+    finite = np.isfinite(v)
+    enc = oracle.bf16_encode(v[finite])
+    # every finite bf16 value encodes to itself (-0 too)
+    assert np.array_equal(enc, h[finite].astype(np.uint16))
+    # half-way between consecutive positive normals: ties go to the even mantissa
+    lo = np.arange(0x0080, 0x7F7F, dtype=np.uint32)
+    a = (lo << 16).view(np.float32).astype(np.float64)
+    b = ((lo + 1) << 16).view(np.float32).astype(np.float64)
+    mid = (a + b) / 2  # exact in fp64
+    got = oracle.bf16_encode(mid)
+    want = np.where(lo % 2 == 0, lo, lo + 1).astype(np.uint16)
+    assert np.array_equal(got, want)
+    # just above / below the midpoint
+    assert np.array_equal(oracle.bf16_encode(mid + (b - a) * 1e-6), (lo + 1).astype(np.uint16))
+    assert np.array_equal(oracle.bf16_encode(mid - (b - a) * 1e-6), lo.astype(np.uint16))
+    # negative values mirror positive ones
+    assert np.array_equal(oracle.bf16_encode(-mid), want | 0x8000)
+
+
+def test_stack_step_adds_then_rounds_once():
+    x = oracle.bf16_encode(np.array([1.0, -2.0, 3.5]))
+    # bf16 spacing at 1 is 2^-7: 1 + 2^-8 lies half-way between 1 and 1 + 2^-7 and ties to the even 1
+    y = np.array([2.0 ** -8, 0.25, -3.5])
+    got = oracle.stack_step(x, y)
+    assert np.array_equal(got, oracle.bf16_encode(np.array([1.0 + 2.0 ** -8, -1.75, 0.0])))
+    assert got[0] == 0x3F80 and got[2] == 0
