@@ -40,6 +40,9 @@ def parse_args():
     p.add_argument("--experts", type=int, default=0,
                    help="override the routed-expert count (small cases for profiling; not a benchmark line)")
     p.add_argument("--tokens", type=int, default=0, help="override T (small cases for profiling)")
+    p.add_argument("--layers", type=int, default=1,
+                   help="> 1: time a stack of this many MoE layers (moe_stack_forward) instead of one layer")
+    p.add_argument("--hash-layers", type=int, default=3, help="hash-routed layers at the bottom of the stack")
     return p.parse_args()
 
 
@@ -436,6 +439,105 @@ def run_ours(args, wl):
         torch.distributed.destroy_process_group()
 
 
+def run_stack(args, wl):
+    """A stack of MoE layers with every layer's experts resident: the whole model's MoE part in the decode /
+    verify regime.  One canonical expert set is drawn on the host and uploaded once; each layer packs its
+    own resident copy (the bytes each layer streams are what count), with its own router weights or hash
+    table.  Times graph replay and direct launches; prints one JSON line."""
+    import dataclasses
+
+    import numpy as np
+    import torch
+
+    import __graft_entry__ as g
+    import synth
+    g.build()
+    import block_scaled_fp4_sqrt_gb300 as moe
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    L, n_hash = args.layers, min(args.hash_layers, args.layers)
+    per_layer = expert_bytes(wl) * wl.E + expert_bytes(wl)  # routed + shared resident bytes per layer
+    free = torch.cuda.mem_get_info(dev)[0]
+    if L * per_layer > 0.9 * free:
+        raise SystemExit(f"{L} layers need {L * per_layer / 1e9:.1f} GB of resident experts; {free / 1e9:.1f} GB free")
+    ex = synth.gen_experts(args.seed, wl.E, wl.d, wl.f)
+    sh = synth.gen_experts(args.seed, 1, wl.d, wl.f, shared=True)
+    dex = moe.DeviceExperts(*(torch.from_numpy(getattr(ex, n)).to(dev) for n in ("w13", "s13", "w2", "s2")))
+    dsh = moe.DeviceExperts(*(torch.from_numpy(getattr(sh, n)).to(dev) for n in ("w13", "s13", "w2", "s2")))
+    V = 131072
+    tok = torch.from_numpy(synth.gen_token_ids(args.seed, wl.T, V)).to(dev)
+    layers = []
+    for l in range(L):
+        if l < n_hash:
+            tab = torch.from_numpy(synth.gen_hash_table(args.seed + l, V, wl.E, wl.k)).to(dev)
+            layers.append(moe.MoELayer(wl.d, wl.f, wl.E, wl.k, dex, dsh, None, None, tab, wl.T, wl.route_scale,
+                                       wl.swiglu_limit, dev))
+        else:
+            rw, rb, _ = synth.gen_router(args.seed + l, wl.E, wl.d, wl.n_hot, wl.hot_bias)
+            layers.append(moe.MoELayer(wl.d, wl.f, wl.E, wl.k, dex, dsh, torch.from_numpy(rw).to(dev),
+                                       torch.from_numpy(rb).to(dev), None, wl.T, wl.route_scale, wl.swiglu_limit, dev))
+        layers[-1].workspace = None  # the stacks below give every layer one shared workspace
+    del dex, dsh
+    torch.cuda.empty_cache()
+    x = torch.from_numpy(synth.gen_x(args.seed, wl.T, wl.d).view(np.int16)).to(dev).view(torch.bfloat16)
+    out = torch.empty_like(x)
+    stream = torch.cuda.current_stream(dev)
+
+    def time_stack(use_graph):
+        st = moe.MoEStack(layers, max_T=wl.T, use_graph=use_graph)
+        for _ in range(max(args.warmup, 3)):
+            st.forward(x, token_ids=tok, out=out)
+        torch.cuda.synchronize()
+        st.check()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            st.forward(x, token_ids=tok, out=out)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        st.check()
+        return e0.elapsed_time(e1) / args.steps, st
+
+    ms_direct, st_d = time_stack(False)
+    st_d.close()
+    cvd = [v for v in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if v.strip()]
+    clocks = ClockSampler(cvd[0] if cvd else 0)
+    clocks.start()
+    ms_graph, st_g = time_stack(True)
+    clk = clocks.stop()
+    st_g.close()
+    # experts each layer touched: one more pass with a workspace per layer keeps every layer's routing
+    st_r = moe.MoEStack(layers, max_T=wl.T, use_graph=False, separate_workspaces=True)
+    st_r.forward(x, token_ids=tok, out=out)
+    torch.cuda.synchronize()
+    touched = [int(torch.unique(ly.last_routing()[0]).numel()) + 1 for ly in layers]
+    st_r.close()
+    del st_r
+    hl = dataclasses.replace(wl, hash_vocab=V)
+    stack_bytes = sum(layer_bytes(hl if l < n_hash else wl, touched[l]) for l in range(L))
+    pk = peaks()
+    line = {
+        "metric": f"MoE stack tokens/sec ({L} layers, {n_hash} hash-routed; x_(l+1) = x_l + MoE_l(x_l))",
+        "value": wl.T / (ms_graph * 1e-3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": ms_graph, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "mxfp4 x mxfp8 -> f32", "data": "synthetic",
+        "config": dict(workload_config(wl), layers=L, hash_layers=n_hash, graph=True,
+                       resident_expert_gb=round(L * per_layer / 1e9, 1)),
+        "per_layer_us": ms_graph * 1e3 / L,
+        "direct_launches": {"ms_per_step": ms_direct, "per_layer_us": ms_direct * 1e3 / L},
+        "stack_roofline": {"bound": "hbm", "algorithmic_bytes": stack_bytes, "achieved": stack_bytes / (ms_graph * 1e-3) / 1e9,
+                           "peak": pk["hbm_gbs"], "unit": "GB/s",
+                           "frac": stack_bytes / (ms_graph * 1e-3) / 1e9 / pk["hbm_gbs"]},
+        "touched_experts_per_layer": {"min": min(touched), "max": max(touched)},
+        "gpu_launches": (L - n_hash) * 9 + n_hash * 8,
+        "clocks": clk,
+    }
+    for ly in layers:
+        ly.close()
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse_args()
     import synth
@@ -451,6 +553,8 @@ def main():
         import __graft_entry__ as g
         g.build_cpu()
         run_reference(args, wl)
+    elif args.layers > 1:
+        run_stack(args, wl)
     else:
         run_ours(args, wl)
 

@@ -373,18 +373,20 @@ class MoEStack:
     """Layers run back to back by ``moe_stack_forward``: x_{l+1} = bf16(x_l + layer_l(x_l)).
 
     ``layers`` are ``MoELayer`` objects (they keep their own handles and weights); all of them get one
-    shared workspace for ``max_T`` rows, and the stack owns the scratch buffer of the residual stream.
-    With ``use_graph`` the whole stack is captured once into a CUDA graph and replayed."""
+    shared workspace for ``max_T`` rows (or one each with ``separate_workspaces``, which keeps every
+    layer's routing readable after a forward), and the stack owns the scratch buffer of the residual
+    stream.  With ``use_graph`` the whole stack is captured once into a CUDA graph and replayed."""
 
-    def __init__(self, layers, max_T: int, use_graph: bool = True, device=None):
+    def __init__(self, layers, max_T: int, use_graph: bool = True, device=None, separate_workspaces: bool = False):
         self.layers = list(layers)
         self.device = torch.device(device or self.layers[0].device)
         self.d, self.max_T = self.layers[0].d, max_T
         with torch.cuda.device(self.device):
             nbytes = max(moe_workspace_size(ly.cfg, max_T) for ly in self.layers)
-            self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=self.device)
-            for ly in self.layers:
-                moe_set_workspace(ly.h, self.workspace, max_T)
+            n_ws = len(self.layers) if separate_workspaces else 1
+            self.workspaces = [torch.empty(nbytes, dtype=torch.uint8, device=self.device) for _ in range(n_ws)]
+            for i, ly in enumerate(self.layers):
+                moe_set_workspace(ly.h, self.workspaces[i % n_ws], max_T)
             self.scratch = torch.empty((max_T, self.d), dtype=torch.bfloat16, device=self.device)
             self.stack = moe_stack_create([(ly.h, ly.h_shared, ly.router_w, ly.router_bias) for ly in self.layers],
                                           use_graph)
