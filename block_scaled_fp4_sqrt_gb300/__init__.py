@@ -26,7 +26,9 @@ EXPORTED = ("moe_experts_create", "moe_experts_set_hash_table", "moe_workspace_s
             "moe_route", "moe_permute", "moe_expert_ffn", "moe_forward", "moe_get_routing", "moe_check",
             "moe_set_wait_budget", "moe_experts_destroy", "moe_status_string", "moe_last_error",
             "moe_testing_stall_loads", "moe_set_stage_events", "moe_route_noalloc", "moe_measure_mxf8f6f4_peak",
-            "moe_stack_create", "moe_stack_forward", "moe_stack_destroy")
+            "moe_stack_create", "moe_stack_forward", "moe_stack_destroy", "moe_mx_blocks_unpack")
+
+MOE_MX_NIBBLES_PAIRED, MOE_MX_NIBBLES_SPLIT = 0, 1
 
 MOE_N_STAGES = 5
 STAGE_NAMES = ("route", "dispatch", "gemm_gate_up", "gemm_down", "combine")
@@ -80,6 +82,7 @@ def lib() -> ctypes.CDLL:
         L.moe_stack_create.argtypes = [ctypes.POINTER(moe_stack_layer_t), i32, i32, ctypes.POINTER(vp)]
         L.moe_stack_forward.argtypes = [vp, inp, vp, vp, vp]
         L.moe_stack_destroy.argtypes = [vp]
+        L.moe_mx_blocks_unpack.argtypes = [vp, ctypes.c_int64, i32, vp, vp, vp]
         L.moe_stack_destroy.restype = None
         L.moe_experts_destroy.argtypes = [vp]
         L.moe_experts_destroy.restype = None
@@ -226,6 +229,16 @@ def moe_stack_forward(stack, x, out, scratch, token_ids=None, stream=None) -> No
 def moe_stack_destroy(stack) -> None:
     if stack:
         lib().moe_stack_destroy(stack)
+
+
+def moe_mx_blocks_unpack(blocks: torch.Tensor, nibble_order: int, stream=None):
+    """17-byte MXFP4 blocks (uint8, 17 * n bytes) -> (codes uint8 [n, 16], scales uint8 [n])."""
+    n = blocks.numel() // 17
+    codes = torch.empty((n, 16), dtype=torch.uint8, device=blocks.device)
+    scales = torch.empty((n,), dtype=torch.uint8, device=blocks.device)
+    _ok("moe_mx_blocks_unpack", lib().moe_mx_blocks_unpack(_p(blocks), n, int(nibble_order), _p(codes), _p(scales),
+                                                           _stream(stream)))
+    return codes, scales
 
 
 def moe_experts_destroy(h) -> None:

@@ -248,6 +248,25 @@ MOE_API moe_status_t moe_stack_forward(moe_stack_t stack, const moe_input_t* x, 
                                        moe_stream_t stream);
 MOE_API void moe_stack_destroy(moe_stack_t stack);
 
+/*
+ * Checkpoint ingest: an array of 17-byte MXFP4 blocks -> the canonical codes and scales of
+ * moe_experts_create.  Each block is one E8M0 scale byte followed by 16 bytes holding 32 E2M1 codes
+ * (sign bit 3).  The format comes from the model card's "Conversion to the .fst container" (17-byte
+ * blocks, 1 e8m0 scale + the FP4 codes).  The TensorSharp page's "Getting a drafter" says the checkpoint
+ * is GGUF's MXFP4 layout up to nibble order, so the caller names the order:
+ *   MOE_MX_NIBBLES_PAIRED  byte i holds elements 2i (low nibble) and 2i+1 (high nibble): canonical.
+ *   MOE_MX_NIBBLES_SPLIT   byte i holds elements i (low nibble) and i+16 (high nibble).
+ * A [rows x K] matrix stored as rows * K/32 blocks, row-major, becomes:
+ *   codes   [rows][K/2], element 2i in the low nibble of byte i;
+ *   scales  [rows][K/32].
+ * blocks is device memory of 17 * n_blocks bytes; codes (16 * n_blocks) and scales (n_blocks) are
+ * caller-owned device memory.  Asynchronous on the stream.  Returns MOE_ERR_INVALID_ARG for a NULL
+ * buffer, a negative count or an unknown order; n_blocks = 0 does nothing.
+ */
+enum { MOE_MX_NIBBLES_PAIRED = 0, MOE_MX_NIBBLES_SPLIT = 1 };
+MOE_API moe_status_t moe_mx_blocks_unpack(const uint8_t* blocks, int64_t n_blocks, int32_t nibble_order,
+                                          uint8_t* codes, uint8_t* scales, moe_stream_t stream);
+
 MOE_API void moe_experts_destroy(moe_experts_t experts);
 MOE_API const char* moe_status_string(moe_status_t status);
 /* Text of the last host-side error on this thread ("" if none). */

@@ -105,6 +105,20 @@ def bf16_encode(v) -> np.ndarray:
     return (r.view(np.uint32) >> 16).astype(np.uint16)
 
 
+def mx_blocks_unpack(blocks, split: bool):
+    """17-byte MXFP4 blocks [n, 17] (E8M0 byte, then 16 bytes of 32 E2M1 codes) -> (codes [n, 16] with
+    element 2i in the low nibble of byte i, scales [n]).  split: byte i of a block holds elements i (low
+    nibble) and i+16 (high nibble); otherwise elements 2i and 2i+1."""
+    b = np.asarray(blocks, dtype=np.uint8).reshape(-1, 17)
+    q = b[:, 1:]
+    if split:
+        elems = np.concatenate([q & 0xF, q >> 4], axis=1)  # element e at column e
+    else:
+        elems = np.stack([q & 0xF, q >> 4], axis=2).reshape(-1, 32)
+    codes = (elems[:, 0::2] | (elems[:, 1::2] << 4)).astype(np.uint8)
+    return codes, b[:, 0].copy()
+
+
 def stack_step(x_bf16, y) -> np.ndarray:
     """One layer of a stack's bf16 residual stream: x_{l+1} = bf16(x_l + y_l), the sum in fp64."""
     x = (np.asarray(x_bf16, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)

@@ -215,3 +215,37 @@ def test_stack_step_adds_then_rounds_once():
     got = oracle.stack_step(x, y)
     assert np.array_equal(got, oracle.bf16_encode(np.array([1.0 + 2.0 ** -8, -1.75, 0.0])))
     assert got[0] == 0x3F80 and got[2] == 0
+
+
+def _block(scale, elems, split):
+    """A 17-byte block from 32 element codes, written element by element (test helper)."""
+    q = np.zeros(16, dtype=np.uint8)
+    for e, c in enumerate(elems):
+        byte, high = (e % 16, e >= 16) if split else (e // 2, e % 2 == 1)
+        q[byte] |= (c & 0xF) << (4 if high else 0)
+    return np.concatenate([[scale], q]).astype(np.uint8)
+
+
+@pytest.mark.parametrize("split", [False, True])
+def test_mx_blocks_unpack_places_every_element(split):
+    rng = np.random.default_rng(3)
+    elems = rng.integers(0, 16, size=(5, 32))
+    scales = rng.integers(0, 256, size=5)
+    blocks = np.stack([_block(s, e, split) for s, e in zip(scales, elems)])
+    codes, sc = oracle.mx_blocks_unpack(blocks, split)
+    assert np.array_equal(sc, scales.astype(np.uint8))
+    # canonical: element 2i in the low nibble of byte i
+    assert np.array_equal(codes & 0xF, elems[:, 0::2]) and np.array_equal(codes >> 4, elems[:, 1::2])
+    # the values the codes stand for: E2M1 table times 2^(scale - 127)
+    v = oracle.mxfp4_dequantize(codes, sc[:, None])
+    want = np.array([[oracle.e2m1_value(int(c)) for c in row] for row in elems]) * 2.0 ** (scales[:, None] - 127.0)
+    assert np.array_equal(v, want)
+
+
+def test_mx_blocks_unpack_hand_worked():
+    # one block, scale 2^1: elements 0..31 = codes 0..15, 0..15; split order puts element i and i+16 in byte i
+    elems = list(range(16)) * 2
+    blk = _block(128, elems, True)
+    assert blk[1] == 0x00 and blk[2] == 0x11 and blk[16] == 0xFF
+    codes, sc = oracle.mx_blocks_unpack(blk[None], True)
+    assert sc[0] == 128 and codes[0, 0] == 0x10 and codes[0, 7] == 0xFE and codes[0, 8] == 0x10
