@@ -269,6 +269,14 @@ def run_reference(args, wl):
     print(json.dumps(line), flush=True)
 
 
+def layer_launches(wl) -> int:
+    """Kernels one layer forward launches.  Route: the hash-table kernel, or the router weight split then
+    the fused cluster router (up to 256 experts; above that tensor-core logits + a top-k kernel).
+    Dispatch: histogram, column scan, group scan, gather.  The two grouped GEMMs, then the combine."""
+    route = 1 if wl.hashed else (2 if wl.E <= 256 else 3)
+    return route + 4 + 2 + 1
+
+
 def workload_config(wl):
     return {"workload": wl.name, "T": wl.T, "d_model": wl.d, "d_ff": wl.f, "routed_experts": wl.E, "top_k": wl.k,
             "shared_experts": 1, "routing": "hash table" if wl.hashed else "sqrt-softplus",
@@ -406,9 +414,7 @@ def run_ours(args, wl):
                 "frac": achieved / pk["hbm_gbs"], "traffic": measured_traffic(dom, wl.name), "kernel": dom,
                 "peak_source": f"{pk['source']} HBM copy bandwidth", "algorithmic_bytes_per_launch": sb[dom]}
     lb = layer_bytes(wl, touched)
-    # route: weight split + tensor-core logits + top-k (hash layers: one table kernel); dispatch:
-    # histogram, column scan, group scan, gather; the two grouped GEMMs; combine
-    kernels_per_step = (1 if wl.hashed else 3) + 4 + 2 + 1
+    kernels_per_step = layer_launches(wl)
     line = {
         "metric": METRIC, "value": job_tokens_per_s(world, wl.T, ms), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms, "higher_is_better": True,
@@ -530,7 +536,7 @@ def run_stack(args, wl):
                            "peak": pk["hbm_gbs"], "unit": "GB/s",
                            "frac": stack_bytes / (ms_graph * 1e-3) / 1e9 / pk["hbm_gbs"]},
         "touched_experts_per_layer": {"min": min(touched), "max": max(touched)},
-        "gpu_launches": (L - n_hash) * 9 + n_hash * 8,
+        "gpu_launches": ((L - n_hash) * layer_launches(wl) + n_hash * layer_launches(hl)) * args.steps,
         "clocks": clk,
     }
     for ly in layers:
