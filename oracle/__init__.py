@@ -52,15 +52,16 @@ def _lib():
         L.orc_mxfp4_quantize.argtypes = [vp, i64, vp, vp]
         L.orc_mxfp4_dequantize.argtypes = [vp, vp, i64, vp]
         L.orc_mxfp8_dequantize.argtypes = [vp, vp, i64, vp]
-        L.orc_quantize_x.argtypes = [vp, i64, i64, vp, vp, i32]
+        L.orc_quantize_x.argtypes = [vp, i64, i64, vp, vp, i32, i32]
         L.orc_route.argtypes = [vp, i64, i64, vp, vp, i64, i64, dbl, i32, vp, vp, vp, vp, vp, i32]
         L.orc_hash_route.argtypes = [vp, i64, vp, i64, i64, dbl, vp, vp]
         L.orc_hash_route.restype = i64
         L.orc_permute.argtypes = [vp, i64, i64, i64, vp, vp, vp, vp]
-        L.orc_expert_row.argtypes = [vp, vp, i64, i64, vp, vp, vp, vp, dbl, vp, vp, vp, vp]
-        L.orc_expert_ffn.argtypes = [i64, i64, vp, vp, vp, i64, i64, vp, vp, vp, vp, dbl, vp, vp, vp, vp, i32]
+        L.orc_expert_row.argtypes = [vp, vp, i64, i64, vp, vp, vp, vp, dbl, vp, vp, vp, vp, i32]
+        L.orc_expert_ffn.argtypes = [i64, i64, vp, vp, vp, i64, i64, vp, vp, vp, vp, dbl, vp, vp, vp, vp, vp, i32,
+                                     i32]
         L.orc_layer.argtypes = [vp, i64, i64, i64, i64, i64, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, dbl, vp, i64, i32,
-                                vp, i32]
+                                vp, i32, i32]
         _LIB = L
     return _LIB
 
@@ -173,12 +174,32 @@ def mxfp8_dequantize(q: np.ndarray, s: np.ndarray) -> np.ndarray:
     return out
 
 
-def quantize_x(x_bf16: np.ndarray):
+# Activation formats: "mxfp8" (the layer's: E4M3 codes, one byte per element) and "mxfp4" (the FP4
+# variant: E2M1 codes, element 2i in the low nibble of byte i), one E8M0 scale per 32 elements.
+ACT_FORMATS = {"mxfp8": 0, "mxfp4": 1}
+
+
+def _act(act: str) -> int:
+    if act not in ACT_FORMATS:
+        raise ValueError(f"unknown activation format {act!r}")
+    return ACT_FORMATS[act]
+
+
+def act_row_bytes(act: str, n: int) -> int:
+    return n // 2 if _act(act) else n
+
+
+def act_dequantize(q: np.ndarray, s: np.ndarray, act: str = "mxfp8") -> np.ndarray:
+    return mxfp4_dequantize(q, s) if _act(act) else mxfp8_dequantize(q, s)
+
+
+def quantize_x(x_bf16: np.ndarray, act: str = "mxfp8"):
+    """x bf16 [T, d] -> activation codes [T, d] (mxfp8) or [T, d/2] (mxfp4) and scales [T, d/32]."""
     x = _c(x_bf16, np.uint16)
     T, d = x.shape
-    q = np.empty((T, d), dtype=np.uint8)
+    q = np.empty((T, act_row_bytes(act, d)), dtype=np.uint8)
     s = np.empty((T, d // 32), dtype=np.uint8)
-    _lib().orc_quantize_x(_p(x), T, d, _p(q), _p(s), 0)
+    _lib().orc_quantize_x(_p(x), T, d, _p(q), _p(s), 0, _act(act))
     return q, s
 
 
@@ -227,45 +248,55 @@ def permute(ids, E: int):
 
 
 # ----------------------------------------------------------------------------- experts and layer
-def expert_row(aq, as_, w13, s13, w2, s2, limit: float = 10.0):
-    """One expert (slices [2f, d/2], [2f, d/32], [d, f/2], [d, f/32]) on one MXFP8 row.
-    Returns y fp64 [d], h codes [f], h scales [f/32], h before quantisation fp64 [f]."""
+def expert_row(aq, as_, w13, s13, w2, s2, limit: float = 10.0, act: str = "mxfp8"):
+    """One expert (slices [2f, d/2], [2f, d/32], [d, f/2], [d, f/32]) on one activation row.
+    Returns y fp64 [d], h codes [f] (mxfp8) or [f/2] (mxfp4), h scales [f/32], h before quantisation
+    fp64 [f]."""
     aq, as_ = _c(aq, np.uint8), _c(as_, np.uint8)
     w13, s13, w2, s2 = (_c(a, np.uint8) for a in (w13, s13, w2, s2))
-    d = aq.shape[-1]
+    d = as_.shape[-1] * 32
     f = w13.shape[0] // 2
+    assert aq.shape[-1] == act_row_bytes(act, d)
     y = np.empty((d,), dtype=np.float64)
-    hq = np.empty((f,), dtype=np.uint8)
+    hq = np.empty((act_row_bytes(act, f),), dtype=np.uint8)
     hs = np.empty((f // 32,), dtype=np.uint8)
     hpre = np.empty((f,), dtype=np.float64)
     _lib().orc_expert_row(_p(aq), _p(as_), d, f, _p(w13), _p(s13), _p(w2), _p(s2), limit, _p(y), _p(hq), _p(hs),
-                          _p(hpre))
+                          _p(hpre), _act(act))
     return y, hq, hs, hpre
 
 
-def expert_ffn(aq, as_, weights: "synth.ExpertWeights", offsets=None, row_w=None, limit: float = 10.0):
-    """Grouped FFN over MXFP8 rows [n, d]: row r uses expert g with offsets[g] <= r < offsets[g+1]
-    (offsets None: expert 0 for every row), scaled by row_w[r] (None: 1).  Returns y fp64 [n, d]
-    plus the MXFP8 h codes [n, f] and scales [n, f/32]."""
+def expert_ffn(aq, as_, weights: "synth.ExpertWeights", offsets=None, row_w=None, limit: float = 10.0,
+               act: str = "mxfp8", want_hpre: bool = False):
+    """Grouped FFN over activation rows (codes [n, d] for mxfp8, [n, d/2] for mxfp4; scales [n, d/32]):
+    row r uses expert g with offsets[g] <= r < offsets[g+1] (offsets None: expert 0 for every row),
+    scaled by row_w[r] (None: 1).  Returns y fp64 [n, d] plus the h codes and scales in the same
+    format (and, with want_hpre, h before quantisation fp64 [n, f])."""
     aq, as_ = _c(aq, np.uint8), _c(as_, np.uint8)
-    n, d = aq.shape
+    n = as_.shape[0]
+    d = as_.shape[1] * 32
+    assert aq.shape == (n, act_row_bytes(act, d))
     f = weights.w13.shape[1] // 2
     offs = None if offsets is None else _c(offsets, np.int32)
     rw = None if row_w is None else _c(row_w, np.float64)
     y = np.zeros((n, d), dtype=np.float64)
-    hq = np.zeros((n, f), dtype=np.uint8)
+    hq = np.zeros((n, act_row_bytes(act, f)), dtype=np.uint8)
     hs = np.zeros((n, f // 32), dtype=np.uint8)
+    hpre = np.zeros((n, f), dtype=np.float64) if want_hpre else None
     ng = 1 if offs is None else offs.shape[0] - 1
     _lib().orc_expert_ffn(n, ng, _p(offs), _p(aq), _p(as_), d, f, _p(_c(weights.w13, np.uint8)),
                           _p(_c(weights.s13, np.uint8)), _p(_c(weights.w2, np.uint8)), _p(_c(weights.s2, np.uint8)),
-                          limit, _p(rw), _p(y), _p(hq), _p(hs), 0)
+                          limit, _p(rw), _p(y), _p(hq), _p(hs), _p(hpre), 0, _act(act))
+    if want_hpre:
+        return y, hq, hs, hpre
     return y, hq, hs
 
 
 def layer(x_bf16, ids, wts, experts: "synth.ExpertWeights", shared: "synth.ExpertWeights | None",
-          limit: float = 10.0, tokens=None, mode: int = 1):
+          limit: float = 10.0, tokens=None, mode: int = 1, act: str = "mxfp8"):
     """y fp64 [n_sel, d] for the listed tokens (None: all), given the routing (ids, wts).
-    mode 1 goes through the permutation; mode 0 evaluates each (token, expert) pair directly."""
+    mode 1 goes through the permutation; mode 0 evaluates each (token, expert) pair directly.
+    act: the activation format x and h are quantised to ("mxfp8", or "mxfp4" for the FP4 variant)."""
     x = _c(x_bf16, np.uint16)
     T, d = x.shape
     ids = _c(ids, np.int32)
@@ -279,7 +310,7 @@ def layer(x_bf16, ids, wts, experts: "synth.ExpertWeights", shared: "synth.Exper
     sh = [None] * 4 if shared is None else [_c(a, np.uint8) for a in (shared.w13, shared.s13, shared.w2, shared.s2)]
     ex = [_c(a, np.uint8) for a in (experts.w13, experts.s13, experts.w2, experts.s2)]
     _lib().orc_layer(_p(x), T, d, f, E, k, _p(ids), _p(wts), *(_p(a) for a in ex), *(_p(a) for a in sh), limit,
-                     _p(tok), n_sel, mode, _p(y), 0)
+                     _p(tok), n_sel, mode, _p(y), 0, _act(act))
     return y
 
 

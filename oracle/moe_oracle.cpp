@@ -29,7 +29,9 @@
 //  * gate clamped from above at L, up clamped to [-L, L], h = silu(gate) * up;
 //  * w1 = gate, w3 = up, w2 = down; MX blocks run along the reduction dimension;
 //  * an all-zero block gets scale byte 0 (exponent -127);
-//  * the shared expert reads the same MXFP8 activations and enters with weight 1.
+//  * the shared expert reads the same MXFP8 activations and enters with weight 1;
+//  * the MXFP4-activation variant (act = 1) quantises x and h with the weights' own MXFP4 rule
+//    (E2M1, scale floor(log2 amax) - 2) where the layer uses MXFP8; nothing else changes.
 //
 // Build: g++ -O2 -std=c++17 -ffp-contract=off -fPIC -shared -pthread moe_oracle.cpp -o liboracle.so
 #include <algorithm>
@@ -182,6 +184,22 @@ void mxfp8_quantize(const double* v, int64_t n, uint8_t* q, uint8_t* s) {
   }
 }
 
+// MXFP4 (E2M1, emax 2) quantisation of n values, blocks of 32; packed codes, element 2i in the low
+// nibble of byte i.
+void mxfp4_quantize(const double* v, int64_t n, uint8_t* codes, uint8_t* s) {
+  for (int64_t b = 0; b < n / 32; ++b) {
+    double amax = 0.0;
+    for (int i = 0; i < 32; ++i) amax = std::max(amax, std::fabs(v[b * 32 + i]));
+    int se = mx_scale_exp(amax, 2);
+    s[b] = (uint8_t)(se + 127);
+    for (int i = 0; i < 32; i += 2) {
+      uint8_t lo = e2m1_encode(std::ldexp(v[b * 32 + i], -se));
+      uint8_t hi = e2m1_encode(std::ldexp(v[b * 32 + i + 1], -se));
+      codes[(b * 32 + i) / 2] = (uint8_t)(lo | (hi << 4));
+    }
+  }
+}
+
 double mxfp8_value(const uint8_t* q, const uint8_t* s, int64_t i) { return e4m3_value(q[i]) * e8m0_value(s[i / 32]); }
 
 double mxfp4_value(const uint8_t* codes, const uint8_t* s, int64_t i) {
@@ -207,13 +225,24 @@ Expert expert_at(const uint8_t* w13, const uint8_t* s13, const uint8_t* w2, cons
   return x;
 }
 
-// One expert applied to one MXFP8 activation row: gate/up dot products over d, clamp, SiLU * up,
-// MXFP8 requantisation of h along f, down projection over f.  hq/hs/hpre may be null.
+// Activation formats: the layer's MXFP8 (E4M3 codes, one byte per element) and the MXFP4 variant
+// (E2M1 codes, two per byte), both with one E8M0 scale per 32 elements along the reduction dimension.
+constexpr int kActMxfp8 = 0, kActMxfp4 = 1;
+
+int64_t act_row_bytes(int act, int64_t n) { return act == kActMxfp4 ? n / 2 : n; }
+
+double act_value(int act, const uint8_t* q, const uint8_t* s, int64_t i) {
+  return act == kActMxfp4 ? mxfp4_value(q, s, i) : mxfp8_value(q, s, i);
+}
+
+// One expert applied to one activation row: gate/up dot products over d, clamp, SiLU * up,
+// requantisation of h along f in the activation format, down projection over f.  hq/hs/hpre may be
+// null.
 void expert_row(const uint8_t* aq, const uint8_t* as, int64_t d, int64_t f, const Expert& ex, double limit, double* y,
-                uint8_t* hq_out, uint8_t* hs_out, double* hpre_out) {
+                uint8_t* hq_out, uint8_t* hs_out, double* hpre_out, int act) {
   std::vector<double> xd(d), h(f), hd(f);
-  std::vector<uint8_t> hq(f), hs(f / 32);
-  for (int64_t i = 0; i < d; ++i) xd[i] = mxfp8_value(aq, as, i);
+  std::vector<uint8_t> hq(act_row_bytes(act, f)), hs(f / 32);
+  for (int64_t i = 0; i < d; ++i) xd[i] = act_value(act, aq, as, i);
   for (int64_t o = 0; o < f; ++o) {
     const uint8_t* wg = ex.w13 + o * (d / 2);
     const uint8_t* sg = ex.s13 + o * (d / 32);
@@ -228,8 +257,11 @@ void expert_row(const uint8_t* aq, const uint8_t* as, int64_t d, int64_t f, cons
     double uc = std::min(std::max(u, -limit), limit);
     h[o] = silu(gc) * uc;
   }
-  mxfp8_quantize(h.data(), f, hq.data(), hs.data());
-  for (int64_t j = 0; j < f; ++j) hd[j] = mxfp8_value(hq.data(), hs.data(), j);
+  if (act == kActMxfp4)
+    mxfp4_quantize(h.data(), f, hq.data(), hs.data());
+  else
+    mxfp8_quantize(h.data(), f, hq.data(), hs.data());
+  for (int64_t j = 0; j < f; ++j) hd[j] = act_value(act, hq.data(), hs.data(), j);
   for (int64_t o = 0; o < d; ++o) {
     const uint8_t* wd = ex.w2 + o * (f / 2);
     const uint8_t* sd = ex.s2 + o * (f / 32);
@@ -237,7 +269,7 @@ void expert_row(const uint8_t* aq, const uint8_t* as, int64_t d, int64_t f, cons
     for (int64_t j = 0; j < f; ++j) acc += hd[j] * mxfp4_value(wd, sd, j);
     y[o] = acc;
   }
-  if (hq_out) std::memcpy(hq_out, hq.data(), (size_t)f);
+  if (hq_out) std::memcpy(hq_out, hq.data(), hq.size());
   if (hs_out) std::memcpy(hs_out, hs.data(), (size_t)(f / 32));
   if (hpre_out) std::memcpy(hpre_out, h.data(), sizeof(double) * (size_t)f);
 }
@@ -284,19 +316,7 @@ void orc_e4m3_encode_many(const double* v, int64_t n, uint8_t* out) {
 void orc_mxfp8_quantize(const double* v, int64_t n, uint8_t* q, uint8_t* s) { mxfp8_quantize(v, n, q, s); }
 
 // MXFP4 quantisation (E2M1, emax 2), packed codes (element 2i in the low nibble of byte i).
-void orc_mxfp4_quantize(const double* v, int64_t n, uint8_t* codes, uint8_t* s) {
-  for (int64_t b = 0; b < n / 32; ++b) {
-    double amax = 0.0;
-    for (int i = 0; i < 32; ++i) amax = std::max(amax, std::fabs(v[b * 32 + i]));
-    int se = mx_scale_exp(amax, 2);
-    s[b] = (uint8_t)(se + 127);
-    for (int i = 0; i < 32; i += 2) {
-      uint8_t lo = e2m1_encode(std::ldexp(v[b * 32 + i], -se));
-      uint8_t hi = e2m1_encode(std::ldexp(v[b * 32 + i + 1], -se));
-      codes[(b * 32 + i) / 2] = (uint8_t)(lo | (hi << 4));
-    }
-  }
-}
+void orc_mxfp4_quantize(const double* v, int64_t n, uint8_t* codes, uint8_t* s) { mxfp4_quantize(v, n, codes, s); }
 
 void orc_mxfp4_dequantize(const uint8_t* codes, const uint8_t* s, int64_t n, double* out) {
   for (int64_t i = 0; i < n; ++i) out[i] = mxfp4_value(codes, s, i);
@@ -306,13 +326,16 @@ void orc_mxfp8_dequantize(const uint8_t* q, const uint8_t* s, int64_t n, double*
   for (int64_t i = 0; i < n; ++i) out[i] = mxfp8_value(q, s, i);
 }
 
-// x (bf16 [T, d]) -> MXFP8 codes [T, d] and scale bytes [T, d/32].
-void orc_quantize_x(const uint16_t* x, int64_t T, int64_t d, uint8_t* q, uint8_t* s, int threads) {
+// x (bf16 [T, d]) -> activation codes [T, d] (MXFP8) or [T, d/2] (MXFP4) and scale bytes [T, d/32].
+void orc_quantize_x(const uint16_t* x, int64_t T, int64_t d, uint8_t* q, uint8_t* s, int threads, int act) {
   parallel_for(T, threads, [&](int64_t lo, int64_t hi) {
     std::vector<double> row(d);
     for (int64_t t = lo; t < hi; ++t) {
       for (int64_t i = 0; i < d; ++i) row[i] = bf16_value(x[t * d + i]);
-      mxfp8_quantize(row.data(), d, q + t * d, s + t * (d / 32));
+      if (act == kActMxfp4)
+        mxfp4_quantize(row.data(), d, q + t * (d / 2), s + t * (d / 32));
+      else
+        mxfp8_quantize(row.data(), d, q + t * d, s + t * (d / 32));
     }
   });
 }
@@ -396,16 +419,18 @@ void orc_permute(const int32_t* ids, int64_t T, int64_t k, int64_t E, int32_t* c
 // One expert on one activation row (for stage-level checks).
 void orc_expert_row(const uint8_t* aq, const uint8_t* as, int64_t d, int64_t f, const uint8_t* w13,
                     const uint8_t* s13, const uint8_t* w2, const uint8_t* s2, double limit, double* y, uint8_t* hq,
-                    uint8_t* hs, double* hpre) {
+                    uint8_t* hs, double* hpre, int act) {
   Expert ex{w13, s13, w2, s2};
-  expert_row(aq, as, d, f, ex, limit, y, hq, hs, hpre);
+  expert_row(aq, as, d, f, ex, limit, y, hq, hs, hpre, act);
 }
 
-// Grouped expert FFN over n_rows MXFP8 rows: row r belongs to group g where offsets[g] <= r <
+// Grouped expert FFN over n_rows activation rows: row r belongs to group g where offsets[g] <= r <
 // offsets[g+1] (offsets may be null: one group); y[r] = row_w[r] * expert_g(a[r]) (row_w null = 1).
+// hq/hs/hpre (h codes, scales, and h before quantisation [n_rows, f]) may be null.
 void orc_expert_ffn(int64_t n_rows, int64_t n_groups, const int32_t* offsets, const uint8_t* aq, const uint8_t* as,
                     int64_t d, int64_t f, const uint8_t* w13, const uint8_t* s13, const uint8_t* w2, const uint8_t* s2,
-                    double limit, const double* row_w, double* y, uint8_t* hq, uint8_t* hs, int threads) {
+                    double limit, const double* row_w, double* y, uint8_t* hq, uint8_t* hs, double* hpre, int threads,
+                    int act) {
   parallel_for(n_rows, threads, [&](int64_t lo, int64_t hi) {
     for (int64_t r = lo; r < hi; ++r) {
       int64_t g = 0;
@@ -414,8 +439,9 @@ void orc_expert_ffn(int64_t n_rows, int64_t n_groups, const int32_t* offsets, co
         if (g == n_groups) continue;
       }
       Expert ex = expert_at(w13, s13, w2, s2, g, d, f);
-      expert_row(aq + r * d, as + r * (d / 32), d, f, ex, limit, y + r * d, hq ? hq + r * f : nullptr,
-                 hs ? hs + r * (f / 32) : nullptr, nullptr);
+      expert_row(aq + r * act_row_bytes(act, d), as + r * (d / 32), d, f, ex, limit, y + r * d,
+                 hq ? hq + r * act_row_bytes(act, f) : nullptr, hs ? hs + r * (f / 32) : nullptr,
+                 hpre ? hpre + r * f : nullptr, act);
       double wr = row_w ? row_w[r] : 1.0;
       for (int64_t o = 0; o < d; ++o) y[r * d + o] *= wr;
     }
@@ -429,25 +455,29 @@ void orc_expert_ffn(int64_t n_rows, int64_t n_groups, const int32_t* offsets, co
 void orc_layer(const uint16_t* x, int64_t T, int64_t d, int64_t f, int64_t E, int64_t k, const int32_t* ids,
                const double* wts, const uint8_t* w13, const uint8_t* s13, const uint8_t* w2, const uint8_t* s2,
                const uint8_t* sh_w13, const uint8_t* sh_s13, const uint8_t* sh_w2, const uint8_t* sh_s2,
-               double limit, const int32_t* tokens, int64_t n_sel, int mode, double* y_out, int threads) {
+               double limit, const int32_t* tokens, int64_t n_sel, int mode, double* y_out, int threads, int act) {
   if (!tokens) n_sel = T;
   auto tok_of = [&](int64_t i) -> int64_t { return tokens ? tokens[i] : i; };
-  // MXFP8 activations of the selected tokens
-  std::vector<uint8_t> q((size_t)n_sel * d), s((size_t)n_sel * (d / 32));
+  // activations of the selected tokens (MXFP8, or MXFP4 for the FP4 variant)
+  const int64_t ab = act_row_bytes(act, d);
+  std::vector<uint8_t> q((size_t)n_sel * ab), s((size_t)n_sel * (d / 32));
   parallel_for(n_sel, threads, [&](int64_t lo, int64_t hi) {
     std::vector<double> row(d);
     for (int64_t i = lo; i < hi; ++i) {
       int64_t t = tok_of(i);
       for (int64_t c = 0; c < d; ++c) row[c] = bf16_value(x[t * d + c]);
-      mxfp8_quantize(row.data(), d, &q[i * d], &s[i * (d / 32)]);
+      if (act == kActMxfp4)
+        mxfp4_quantize(row.data(), d, &q[i * ab], &s[i * (d / 32)]);
+      else
+        mxfp8_quantize(row.data(), d, &q[i * ab], &s[i * (d / 32)]);
     }
   });
   std::vector<double> ysh((size_t)n_sel * d, 0.0);
   if (sh_w13) {
     Expert sh{sh_w13, sh_s13, sh_w2, sh_s2};
     parallel_for(n_sel, threads, [&](int64_t lo, int64_t hi) {
-      for (int64_t i = lo; i < hi; ++i) expert_row(&q[i * d], &s[i * (d / 32)], d, f, sh, limit, &ysh[i * d], nullptr,
-                                                   nullptr, nullptr);
+      for (int64_t i = lo; i < hi; ++i)
+        expert_row(&q[i * ab], &s[i * (d / 32)], d, f, sh, limit, &ysh[i * d], nullptr, nullptr, nullptr, act);
     });
   }
   if (mode == 0) {
@@ -459,7 +489,7 @@ void orc_layer(const uint16_t* x, int64_t T, int64_t d, int64_t f, int64_t E, in
         for (int64_t o = 0; o < d; ++o) y[o] = 0.0;
         for (int64_t j = 0; j < k; ++j) {
           Expert ex = expert_at(w13, s13, w2, s2, ids[t * k + j], d, f);
-          expert_row(&q[i * d], &s[i * (d / 32)], d, f, ex, limit, ye.data(), nullptr, nullptr, nullptr);
+          expert_row(&q[i * ab], &s[i * (d / 32)], d, f, ex, limit, ye.data(), nullptr, nullptr, nullptr, act);
           for (int64_t o = 0; o < d; ++o) y[o] += wts[t * k + j] * ye[o];
         }
         for (int64_t o = 0; o < d; ++o) y[o] += ysh[i * d + o];
@@ -481,7 +511,7 @@ void orc_layer(const uint16_t* x, int64_t T, int64_t d, int64_t f, int64_t E, in
       while (!(offsets[e] <= r && r < offsets[e + 1])) ++e;
       Expert ex = expert_at(w13, s13, w2, s2, e, d, f);
       int64_t i = perm[r];
-      expert_row(&q[i * d], &s[i * (d / 32)], d, f, ex, limit, &yr[r * d], nullptr, nullptr, nullptr);
+      expert_row(&q[i * ab], &s[i * (d / 32)], d, f, ex, limit, &yr[r * d], nullptr, nullptr, nullptr, act);
     }
   });
   for (int64_t i = 0; i < n_sel; ++i) {

@@ -21,7 +21,7 @@ void orc_permute(const int32_t* ids, int64_t T, int64_t k, int64_t E, int32_t* c
 void orc_layer(const uint16_t* x, int64_t T, int64_t d, int64_t f, int64_t E, int64_t k, const int32_t* ids,
                const double* wts, const uint8_t* w13, const uint8_t* s13, const uint8_t* w2, const uint8_t* s2,
                const uint8_t* sh_w13, const uint8_t* sh_s13, const uint8_t* sh_w2, const uint8_t* sh_s2,
-               double limit, const int32_t* tokens, int64_t n_sel, int mode, double* y_out, int threads);
+               double limit, const int32_t* tokens, int64_t n_sel, int mode, double* y_out, int threads, int act);
 }
 
 int main() {
@@ -44,18 +44,22 @@ int main() {
               logits.data(), scores.data(), threads);
   std::vector<int32_t> counts(E), offsets(E + 1), perm(T * k), inv(T * k);
   orc_permute(ids.data(), T, k, E, counts.data(), offsets.data(), perm.data(), inv.data());
-  std::vector<double> y(T * d), y2(T * d);
-  for (int mode = 0; mode < 2; ++mode)
+  std::vector<double> y(T * d), y2(T * d), y4(T * d), y42(T * d);
+  for (int mode = 0; mode < 2; ++mode) {
     orc_layer(x.data(), T, d, f, E, k, ids.data(), wts.data(), w13.data(), s13.data(), w2.data(), s2.data(),
               h13.data(), hs13.data(), h2.data(), hs2.data(), 10.0, nullptr, 0, mode, mode ? y2.data() : y.data(),
-              threads);
+              threads, 0);
+    orc_layer(x.data(), T, d, f, E, k, ids.data(), wts.data(), w13.data(), s13.data(), w2.data(), s2.data(),
+              h13.data(), hs13.data(), h2.data(), hs2.data(), 10.0, nullptr, 0, mode, mode ? y42.data() : y4.data(),
+              threads, 1);
+  }
   std::vector<int32_t> tok(T), table(V * k), hids(T * k);
   std::vector<double> hw(T * k);
   synth_token_ids(0, T, V, tok.data());
   synth_hash_table(0, V, E, k, table.data());
   if (orc_hash_route(tok.data(), T, table.data(), V, k, 1.5, hids.data(), hw.data()) != 0) return 2;
   for (int64_t i = 0; i < T * d; ++i)
-    if (y[i] != y2[i]) return 3;  // dense and permuted evaluation agree bit for bit
+    if (y[i] != y2[i] || y4[i] != y42[i]) return 3;  // dense and permuted evaluation agree bit for bit
   std::printf("ok\n");
   return 0;
 }
