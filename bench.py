@@ -37,6 +37,8 @@ def parse_args():
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--cpu-seconds", type=float, default=10.0, help="target CPU time of the oracle baseline sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--act", choices=["mxfp8", "mxfp4"], default="mxfp8",
+                   help="activation format: the layer's MXFP8, or the MXFP4-activation variant (kind::mxf4)")
     p.add_argument("--experts", type=int, default=0,
                    help="override the routed-expert count (small cases for profiling; not a benchmark line)")
     p.add_argument("--tokens", type=int, default=0, help="override T (small cases for profiling)")
@@ -98,17 +100,19 @@ def expert_bytes(wl):
     return n // 2 + n // 32
 
 
-def stage_bytes(wl, touched, rows):
-    """Algorithmic HBM bytes per launch of each stage (touched = experts read, including the shared one)."""
+def stage_bytes(wl, touched, rows, act: str = "mxfp8"):
+    """Algorithmic HBM bytes per launch of each stage (touched = experts read, including the shared one).
+    Activation rows (A, H) take one byte per element in MXFP8 and half a byte in MXFP4."""
     d, f, T, k, E = wl.d, wl.f, wl.T, wl.k, wl.E
+    per = 2 if act == "mxfp4" else 1
     gate_up_w = 2 * f * d // 2 + 2 * f * d // 32
     down_w = d * f // 2 + d * f // 32
     router = (0 if wl.hashed else E * d * 4 + E * 4) + T * d * 2 + T * k * 8
     return {
         "route": router,
-        "dispatch": T * d * 2 + rows * (d + d // 32),
-        "gemm_gate_up": touched * gate_up_w + rows * (d + d // 32) + rows * (f + f // 32),
-        "gemm_down": touched * down_w + rows * (f + f // 32) + rows * d * 4,
+        "dispatch": T * d * 2 + rows * (d // per + d // 32),
+        "gemm_gate_up": touched * gate_up_w + rows * (d // per + d // 32) + rows * (f // per + f // 32),
+        "gemm_down": touched * down_w + rows * (f // per + f // 32) + rows * d * 4,
         "combine": rows * d * 4 + T * d * 2,
     }
 
@@ -214,7 +218,7 @@ def measured_traffic(kernel: str, workload: str):
     return table.get((workload, kernel))
 
 
-def oracle_tokens_per_s(inp, wl, n_tokens: int, seed: int):
+def oracle_tokens_per_s(inp, wl, n_tokens: int, seed: int, act: str = "mxfp8"):
     """Time the fp64 oracle (routing + layer) on n_tokens sampled token rows."""
     import numpy as np
 
@@ -226,17 +230,17 @@ def oracle_tokens_per_s(inp, wl, n_tokens: int, seed: int):
         ids, wts = oracle.hash_route(inp.token_ids[toks], inp.hash_table, wl.k, wl.route_scale)
     else:
         ids, wts, _ = oracle.route(inp.x[toks], inp.router_w, inp.router_bias, wl.k, wl.route_scale)
-    oracle.layer(inp.x[toks], ids, wts, inp.experts, inp.shared, wl.swiglu_limit)
+    oracle.layer(inp.x[toks], ids, wts, inp.experts, inp.shared, wl.swiglu_limit, act=act)
     dt = time.perf_counter() - t0
     return len(toks), dt
 
 
-def cpu_baseline(inp, wl, target_s: float, seed: int):
+def cpu_baseline(inp, wl, target_s: float, seed: int, act: str = "mxfp8"):
     import oracle
     n0 = 4
-    _, t0 = oracle_tokens_per_s(inp, wl, n0, seed)
+    _, t0 = oracle_tokens_per_s(inp, wl, n0, seed, act)
     n = int(max(n0, min(wl.T, round(target_s / max(t0 / n0, 1e-9)))))
-    n, dt = oracle_tokens_per_s(inp, wl, n, seed + 1)
+    n, dt = oracle_tokens_per_s(inp, wl, n, seed + 1, act)
     return {"value": n / dt, "unit": "tokens/s", "cores": oracle.threads(), "kind": "oracle",
             "sample": f"{n} of the {wl.T} token rows of {wl.name} (routing + all expert rows + combine), fp64, {dt:.1f} s"}
 
@@ -251,10 +255,10 @@ def run_reference(args, wl):
     import oracle
     per_step = max(1, min(wl.T, 4 if wl.d >= 4096 else 16))
     for i in range(args.warmup):
-        oracle_tokens_per_s(inp, wl, per_step, 1000 + i)
+        oracle_tokens_per_s(inp, wl, per_step, 1000 + i, args.act)
     total_tok, total_s = 0, 0.0
     for i in range(args.steps):
-        n, dt = oracle_tokens_per_s(inp, wl, per_step, 2000 + i)
+        n, dt = oracle_tokens_per_s(inp, wl, per_step, 2000 + i, args.act)
         total_tok += n
         total_s += dt
     value = total_tok / total_s
@@ -262,7 +266,7 @@ def run_reference(args, wl):
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
-            "config": workload_config(wl),
+            "config": workload_config(wl, args.act),
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                              "sample": f"{per_step} token rows of {wl.name} per step"},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -277,8 +281,8 @@ def layer_launches(wl) -> int:
     return route + 4 + 2 + 1
 
 
-def workload_config(wl):
-    return {"workload": wl.name, "T": wl.T, "d_model": wl.d, "d_ff": wl.f, "routed_experts": wl.E, "top_k": wl.k,
+def workload_config(wl, act: str = "mxfp8"):
+    return {"act": act, "workload": wl.name, "T": wl.T, "d_model": wl.d, "d_ff": wl.f, "routed_experts": wl.E, "top_k": wl.k,
             "shared_experts": 1, "routing": "hash table" if wl.hashed else "sqrt-softplus",
             "weights": "MXFP4 (E2M1 + E8M0/32), resident in HBM",
             "l2": "no flush: expert weights read per step exceed the 129 MB L2"}
@@ -303,7 +307,7 @@ def run_ours(args, wl):
     inp = synth.gen_layer(wl, args.seed)
     if world > 1:  # each replica gets its own batch of token rows
         inp.x = replica_x(args.seed, rank, world, wl.T, wl.d)
-    layer = moe.MoELayer.from_host(inp, device=dev, max_T=wl.T)
+    layer = moe.MoELayer.from_host(inp, device=dev, max_T=wl.T, act=args.act)
     x = torch.from_numpy(inp.x.view(np.int16)).to(dev).view(torch.bfloat16)
     out = torch.empty((wl.T, wl.d), dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -320,7 +324,11 @@ def run_ours(args, wl):
     rows = wl.T * wl.k + wl.T
 
     # block-scaled MMA peak of this GPU (the tensor roofline's denominator), before the timed region
-    mx_peak = moe.moe_measure_mxf8f6f4_peak(4096)
+    fp4 = args.act == "mxfp4"
+    mx_peak = moe.moe_measure_mxf4_peak(4096) if fp4 else moe.moe_measure_mxf8f6f4_peak(4096)
+    mma_name = ("tcgen05.mma kind::mxf4.block_scale (E2M1 x E2M1, M=128 N=256 K=64) on every SM (moe_measure_mxf4_peak)"
+                if fp4 else "tcgen05.mma kind::mxf8f6f4.block_scale (E4M3 x E2M1, M=128 N=256 K=32) on every SM "
+                "(moe_measure_mxf8f6f4_peak)")
 
     # ---- device-timed steps: the headline value, plain steps back to back on the launching stream
     cvd = [v for v in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if v.strip()]
@@ -394,7 +402,7 @@ def run_ours(args, wl):
 
     pk = peaks()
     dom = max(stage_ms, key=stage_ms.get)
-    sb = stage_bytes(wl, touched, rows)
+    sb = stage_bytes(wl, touched, rows, args.act)
     fl = gemm_flops(wl, rows)
     # verify shapes stream the expert weights (HBM bound); with >= 64 rows per expert (the prefill
     # chunk) the grouped GEMMs are dense block-scaled contractions (tensor bound)
@@ -402,24 +410,26 @@ def run_ours(args, wl):
     if compute_bound:
         achieved = fl[dom] / (stage_ms[dom] * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": mx_peak, "unit": "TFLOP/s", "frac": achieved / mx_peak,
-                "traffic": measured_traffic(dom, wl.name), "kernel": dom,
-                "peak_source": "measured in this run: back-to-back tcgen05.mma kind::mxf8f6f4.block_scale "
-                               "(E4M3 x E2M1, M=128 N=256 K=32) on every SM (moe_measure_mxf8f6f4_peak)",
-                "nominal_alt_peak": {"value": 2 * pk["bf16_tflops_sustained"],
-                                     "source": f"{pk['source']} bf16 sustained x 2 (nominal FP8/BF16 ratio)"},
+                "traffic": None if fp4 else measured_traffic(dom, wl.name), "kernel": dom,
+                "peak_source": "measured in this run: back-to-back " + mma_name,
+                "nominal_alt_peak": {"value": (6 if fp4 else 2) * pk["bf16_tflops_sustained"],
+                                     "source": f"{pk['source']} bf16 sustained x {6 if fp4 else 2} (nominal "
+                                               f"{'FP4' if fp4 else 'FP8'}/BF16 ratio)"},
                 "algorithmic_flops_per_launch": fl[dom]}
     else:
         achieved = sb[dom] / (stage_ms[dom] * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved / pk["hbm_gbs"], "traffic": measured_traffic(dom, wl.name), "kernel": dom,
+                "frac": achieved / pk["hbm_gbs"], "traffic": None if fp4 else measured_traffic(dom, wl.name),
+                "kernel": dom,
                 "peak_source": f"{pk['source']} HBM copy bandwidth", "algorithmic_bytes_per_launch": sb[dom]}
     lb = layer_bytes(wl, touched)
     kernels_per_step = layer_launches(wl)
     line = {
         "metric": METRIC, "value": job_tokens_per_s(world, wl.T, ms), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "mxfp4 x mxfp8 -> f32", "data": "synthetic",
-        "config": dict(workload_config(wl), touched_experts=touched, parallelism=f"replicas x{world}"),
+        "scaling": "weak", "vs_baseline": None, "dtype": "mxfp4 x mxfp4 -> f32" if fp4 else "mxfp4 x mxfp8 -> f32",
+        "data": "synthetic",
+        "config": dict(workload_config(wl, args.act), touched_experts=touched, parallelism=f"replicas x{world}"),
         "roofline": roof,
         "layer_roofline": {"bound": "hbm", "algorithmic_bytes": lb, "achieved": lb / (ms * 1e-3) / 1e9,
                            "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": lb / (ms * 1e-3) / 1e9 / pk["hbm_gbs"]},
@@ -438,7 +448,7 @@ def run_ours(args, wl):
         "clocks": clk,
     }
     if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(inp, wl, args.cpu_seconds, args.seed)
+        line["cpu_baseline"] = cpu_baseline(inp, wl, args.cpu_seconds, args.seed, args.act)
     layer.close()
     print(json.dumps(line), flush=True)
     if world > 1:
@@ -478,11 +488,12 @@ def run_stack(args, wl):
         if l < n_hash:
             tab = torch.from_numpy(synth.gen_hash_table(args.seed + l, V, wl.E, wl.k)).to(dev)
             layers.append(moe.MoELayer(wl.d, wl.f, wl.E, wl.k, dex, dsh, None, None, tab, wl.T, wl.route_scale,
-                                       wl.swiglu_limit, dev))
+                                       wl.swiglu_limit, dev, args.act))
         else:
             rw, rb, _ = synth.gen_router(args.seed + l, wl.E, wl.d, wl.n_hot, wl.hot_bias)
             layers.append(moe.MoELayer(wl.d, wl.f, wl.E, wl.k, dex, dsh, torch.from_numpy(rw).to(dev),
-                                       torch.from_numpy(rb).to(dev), None, wl.T, wl.route_scale, wl.swiglu_limit, dev))
+                                       torch.from_numpy(rb).to(dev), None, wl.T, wl.route_scale, wl.swiglu_limit, dev,
+                                       args.act))
         layers[-1].workspace = None  # the stacks below give every layer one shared workspace
     del dex, dsh
     torch.cuda.empty_cache()
@@ -527,8 +538,8 @@ def run_stack(args, wl):
         "metric": f"MoE stack tokens/sec ({L} layers, {n_hash} hash-routed; x_(l+1) = x_l + MoE_l(x_l))",
         "value": wl.T / (ms_graph * 1e-3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
         "warmup": max(args.warmup, 3), "ms_per_step": ms_graph, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "mxfp4 x mxfp8 -> f32", "data": "synthetic",
-        "config": dict(workload_config(wl), layers=L, hash_layers=n_hash, graph=True,
+        "vs_baseline": None, "dtype": "mxfp4 x mxfp4 -> f32" if args.act == "mxfp4" else "mxfp4 x mxfp8 -> f32", "data": "synthetic",
+        "config": dict(workload_config(wl, args.act), layers=L, hash_layers=n_hash, graph=True,
                        resident_expert_gb=round(L * per_layer / 1e9, 1)),
         "per_layer_us": ms_graph * 1e3 / L,
         "direct_launches": {"ms_per_step": ms_direct, "per_layer_us": ms_direct * 1e3 / L},

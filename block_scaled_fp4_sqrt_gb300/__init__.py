@@ -26,9 +26,12 @@ EXPORTED = ("moe_experts_create", "moe_experts_set_hash_table", "moe_workspace_s
             "moe_route", "moe_permute", "moe_expert_ffn", "moe_forward", "moe_get_routing", "moe_check",
             "moe_set_wait_budget", "moe_experts_destroy", "moe_status_string", "moe_last_error",
             "moe_testing_stall_loads", "moe_set_stage_events", "moe_route_noalloc", "moe_measure_mxf8f6f4_peak",
-            "moe_stack_create", "moe_stack_forward", "moe_stack_destroy", "moe_mx_blocks_unpack")
+            "moe_stack_create", "moe_stack_forward", "moe_stack_destroy", "moe_mx_blocks_unpack",
+            "moe_experts_set_activation_format", "moe_measure_mxf4_peak", "moe_testing_read_h")
 
 MOE_MX_NIBBLES_PAIRED, MOE_MX_NIBBLES_SPLIT = 0, 1
+MOE_ACT_MXFP8, MOE_ACT_MXFP4 = 0, 1
+ACT_FORMATS = {"mxfp8": MOE_ACT_MXFP8, "mxfp4": MOE_ACT_MXFP4}
 
 MOE_N_STAGES = 5
 STAGE_NAMES = ("route", "dispatch", "gemm_gate_up", "gemm_down", "combine")
@@ -79,6 +82,9 @@ def lib() -> ctypes.CDLL:
         L.moe_set_stage_events.argtypes = [vp, ctypes.POINTER(vp), i32]
         L.moe_route_noalloc.argtypes = [cfgp, inp, vp, vp, vp, vp, vp]
         L.moe_measure_mxf8f6f4_peak.argtypes = [i32, ctypes.POINTER(ctypes.c_double)]
+        L.moe_measure_mxf4_peak.argtypes = [i32, ctypes.POINTER(ctypes.c_double)]
+        L.moe_experts_set_activation_format.argtypes = [vp, i32]
+        L.moe_testing_read_h.argtypes = [vp, vp, vp, ctypes.POINTER(i32), vp]
         L.moe_stack_create.argtypes = [ctypes.POINTER(moe_stack_layer_t), i32, i32, ctypes.POINTER(vp)]
         L.moe_stack_forward.argtypes = [vp, inp, vp, vp, vp]
         L.moe_stack_destroy.argtypes = [vp]
@@ -191,6 +197,33 @@ def moe_measure_mxf8f6f4_peak(n_stages: int = 4096) -> float:
     return out.value
 
 
+def moe_measure_mxf4_peak(n_stages: int = 4096) -> float:
+    """Measured dense TFLOP/s of the block-scaled E2M1 x E2M1 MMA (kind::mxf4, M=128, N=256, K=64) on
+    the current device; synchronous."""
+    out = ctypes.c_double(0.0)
+    _ok("moe_measure_mxf4_peak", lib().moe_measure_mxf4_peak(int(n_stages), ctypes.byref(out)))
+    return out.value
+
+
+def moe_testing_read_h(h, f: int, act: str, stream=None):
+    """The h codes and canonical scales of the last grouped FFN on the handle (device tensors)."""
+    n = ctypes.c_int32(0)
+    _ok("moe_testing_read_h", lib().moe_testing_read_h(h, None, None, ctypes.byref(n), _stream(stream)))
+    dev = torch.device("cuda", torch.cuda.current_device())
+    hq = torch.empty((n.value, f // 2 if act == "mxfp4" else f), dtype=torch.uint8, device=dev)
+    hs = torch.empty((n.value, f // 32), dtype=torch.uint8, device=dev)
+    if n.value:
+        _ok("moe_testing_read_h", lib().moe_testing_read_h(h, _p(hq), _p(hs), ctypes.byref(n), _stream(stream)))
+    return hq, hs
+
+
+def moe_experts_set_activation_format(h, fmt: str) -> None:
+    """fmt: "mxfp8" (the layer's) or "mxfp4" (the MXFP4-activation variant)."""
+    if fmt not in ACT_FORMATS:
+        raise ValueError(f"unknown activation format {fmt!r}")
+    _ok("moe_experts_set_activation_format", lib().moe_experts_set_activation_format(h, ACT_FORMATS[fmt]))
+
+
 def moe_set_stage_events(h, events) -> object:
     """events: MOE_N_STAGES + 1 torch.cuda.Event(enable_timing=True) (or None to stop).  Returns the
     ctypes array the library reads; keep it alive while recording."""
@@ -275,8 +308,9 @@ class MoELayer:
     def __init__(self, d_model, d_ff, n_experts, top_k, experts: DeviceExperts, shared: DeviceExperts | None,
                  router_w: torch.Tensor | None, router_bias: torch.Tensor | None,
                  hash_table: torch.Tensor | None = None, max_T: int = 512, route_scale: float = 1.5,
-                 swiglu_limit: float = 10.0, device=None):
+                 swiglu_limit: float = 10.0, device=None, act: str = "mxfp8"):
         self.device = torch.device(device or "cuda")
+        self.act = act
         self.cfg = make_config(d_model, d_ff, n_experts, top_k, route_scale, swiglu_limit)
         self.d, self.f, self.E, self.k, self.max_T = d_model, d_ff, n_experts, top_k, max_T
         self.experts, self.shared_w = experts, shared
@@ -291,14 +325,18 @@ class MoELayer:
                 self._handles.append(self.h_shared)
             if hash_table is not None:
                 moe_experts_set_hash_table(self.h, hash_table)
+            for h in self._handles:
+                moe_experts_set_activation_format(h, act)
             nbytes = moe_workspace_size(self.cfg, max_T)
             self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=self.device)
             moe_set_workspace(self.h, self.workspace, max_T)
             torch.cuda.current_stream(self.device).synchronize()
 
     @classmethod
-    def from_host(cls, inp, device=None, max_T: int | None = None, with_shared: bool = True) -> "MoELayer":
-        """Build from host arrays (an object with the fields of ``synth.LayerInputs``)."""
+    def from_host(cls, inp, device=None, max_T: int | None = None, with_shared: bool = True,
+                  act: str = "mxfp8") -> "MoELayer":
+        """Build from host arrays (an object with the fields of ``synth.LayerInputs``); act is the
+        activation format ("mxfp8", or "mxfp4" for the MXFP4-activation variant)."""
         dev = torch.device(device or "cuda")
         wl = inp.wl
         ex = DeviceExperts(*(_to_dev(getattr(inp.experts, n), dev) for n in ("w13", "s13", "w2", "s2")))
@@ -308,7 +346,8 @@ class MoELayer:
         rw = None if inp.router_w is None else _to_dev(inp.router_w, dev)
         rb = None if inp.router_bias is None else _to_dev(inp.router_bias, dev)
         tab = None if inp.hash_table is None else _to_dev(inp.hash_table, dev)
-        layer = cls(wl.d, wl.f, wl.E, wl.k, ex, sh, rw, rb, tab, max_T or wl.T, wl.route_scale, wl.swiglu_limit, dev)
+        layer = cls(wl.d, wl.f, wl.E, wl.k, ex, sh, rw, rb, tab, max_T or wl.T, wl.route_scale, wl.swiglu_limit, dev,
+                    act)
         layer.token_ids = None if inp.token_ids is None else _to_dev(inp.token_ids, dev)
         return layer
 
@@ -338,7 +377,8 @@ class MoELayer:
                    offsets=torch.empty(self.E + 1, dtype=torch.int32, device=dev),
                    perm_tok=torch.empty(R, dtype=torch.int32, device=dev),
                    inv_pos=torch.empty((T, self.k), dtype=torch.int32, device=dev),
-                   a_q=torch.empty((R, self.d), dtype=torch.uint8, device=dev),
+                   a_q=torch.empty((R, self.d // 2 if self.act == "mxfp4" else self.d), dtype=torch.uint8,
+                                   device=dev),
                    a_s=torch.empty((R, self.d // 32), dtype=torch.uint8, device=dev))
         moe_permute(self.h, x, ids, out["counts"], out["offsets"], out["perm_tok"], out["inv_pos"], out["a_q"],
                     out["a_s"])
@@ -361,6 +401,11 @@ class MoELayer:
         ids = torch.as_tensor(_DeviceView(ids_p, (T, self.k), "<i4", self), device=self.device)
         w = torch.as_tensor(_DeviceView(w_p, (T, self.k), "<f4", self), device=self.device)
         return ids.clone(), w.clone()
+
+    def last_h(self, shared: bool = False):
+        """(codes, scales) of h from the last forward / expert_ffn (test hook)."""
+        with torch.cuda.device(self.device):
+            return moe_testing_read_h(self.h_shared if shared else self.h, self.f, self.act)
 
     def last_topk_ids(self) -> torch.Tensor:
         return self.last_routing()[0]

@@ -22,8 +22,11 @@ struct moe_experts_s {
   uint8_t* w2 = nullptr;    // owned: packed down codes [n, f/128, d/256, 256, 64]
   uint8_t* sf13 = nullptr;  // owned: scale atoms [n, d/128, f/128, 2, 512]
   uint8_t* sf2 = nullptr;   // owned: [n, f/128, d/256, 2, 512]
-  CUtensorMap tm13;
+  CUtensorMap tm13;   // the same codes for kind::mxf8f6f4 (16U4_ALIGN16B, 128-byte rows in smem)
   CUtensorMap tm2;
+  CUtensorMap tm13p;  // ... and for kind::mxf4 (packed 64-byte rows, 64-byte swizzle)
+  CUtensorMap tm2p;
+  int act_fp4 = 0;    // activation format: 0 = MXFP8, 1 = MXFP4 (moe_experts_set_activation_format)
   const int32_t* hash_table = nullptr;
   int32_t hash_V = 0;
   void* ws_base = nullptr;
@@ -35,6 +38,7 @@ struct moe_experts_s {
   int num_sms = 0;
   int device = 0;
   int32_t last_T = 0;
+  int32_t last_rows = 0;  // rows of the last grouped FFN (its h stays in the workspace)
   int stall_loads = 0;
   void* const* stage_events = nullptr;  // MOE_N_STAGES + 1 caller-owned cudaEvent_t, or null
 };
@@ -90,6 +94,22 @@ moe_status_t make_map(CUtensorMap* m, const void* base, bool fp4, uint64_t K, ui
                   const_cast<void*>(base), gdim, gstride, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return MOE_OK;
+}
+
+// Packed 8-bit map for kind::mxf4 operands: rows of `row_bytes` bytes (K / 2 for MXFP4), box {64 B
+// (128 E2M1 codes, one stage), box_rows}, 64-byte swizzle.
+moe_status_t make_map_packed(CUtensorMap* m, const void* base, uint64_t row_bytes, uint64_t rows, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  cuuint64_t gdim[2] = {row_bytes, rows};
+  cuuint64_t gstride[1] = {row_bytes};
+  cuuint32_t box[2] = {64u, box_rows};
+  cuuint32_t estr[2] = {1u, 1u};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), gdim, gstride, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled (packed) failed (%d)", (int)r);
   return MOE_OK;
 }
 
@@ -262,6 +282,8 @@ moe_status_t moe_experts_create(const moe_config_t* cfg, int32_t n, const uint8_
   // packed codes as [slabs * 256 rows, 128 FP4]: one 256-row box per (output tile, K group)
   st = make_map(&h->tm13, h->w13, true, 128, (uint64_t)n * 2 * f * (d / 128), 256);
   if (st == MOE_OK) st = make_map(&h->tm2, h->w2, true, 128, (uint64_t)n * d * (f / 128), 256);
+  if (st == MOE_OK) st = make_map_packed(&h->tm13p, h->w13, 64, (uint64_t)n * 2 * f * (d / 128), 256);
+  if (st == MOE_OK) st = make_map_packed(&h->tm2p, h->w2, 64, (uint64_t)n * d * (f / 128), 256);
   if (st != MOE_OK) {
     moe_experts_destroy(h);
     return st;
@@ -299,6 +321,13 @@ moe_status_t moe_set_workspace(moe_experts_t h, void* ws, size_t bytes, int32_t 
   h->ws_base = ws;
   h->ws_bytes = bytes;
   h->ws_max_T = max_T;
+  return MOE_OK;
+}
+
+moe_status_t moe_experts_set_activation_format(moe_experts_t h, int32_t format) {
+  if (!h) return fail(MOE_ERR_INVALID_ARG, "handle is NULL");
+  if (format != MOE_ACT_MXFP8 && format != MOE_ACT_MXFP4) return fail(MOE_ERR_INVALID_ARG, "unknown activation format");
+  h->act_fp4 = format == MOE_ACT_MXFP4 ? 1 : 0;
   return MOE_OK;
 }
 
@@ -391,7 +420,8 @@ moe_status_t moe_permute(moe_experts_t h, const moe_input_t* x, const int32_t* t
            "scan");
   uint8_t* q = a_q ? a_q : h->ws.a_q;
   MOE_CUDA(launch_gather(static_cast<const __nv_bfloat16*>(x->x_bf16), topk_ids, nullptr, h->ws.chunk_hist, offsets,
-                         h->ws.tile_off, T, d, k, E, E, 0, kTileRows, q, nullptr, a_s, perm_tok, inv_pos, nullptr, s),
+                         h->ws.tile_off, T, d, k, E, E, 0, kTileRows, q, nullptr, a_s, perm_tok, inv_pos, nullptr,
+                         h->act_fp4, s),
            "gather");
   return MOE_OK;
 }
@@ -410,21 +440,31 @@ static moe_status_t run_ffn(moe_experts_s* h, moe_experts_s* sh, int rows, int E
                             const uint8_t* a_q, const uint8_t* a_sf_atoms, const float* row_w, float* y_f32,
                             __nv_bfloat16* y_bf16, int max_tiles, int tile_rows, bool timed, cudaStream_t s) {
   const int d = h->cfg.d_model, f = h->cfg.d_ff;
+  const int fp4 = h->act_fp4;
   CUtensorMap tm_a, tm_a32, tm_h, tm_h32;
-  moe_status_t st = make_map(&tm_a, a_q, false, (uint64_t)d, (uint64_t)rows, kTileRows);
-  if (st == MOE_OK) st = make_map(&tm_a32, a_q, false, (uint64_t)d, (uint64_t)rows, 32);
-  if (st == MOE_OK) st = make_map(&tm_h, h->ws.h_q, false, (uint64_t)f, (uint64_t)rows, kTileRows);
-  if (st == MOE_OK) st = make_map(&tm_h32, h->ws.h_q, false, (uint64_t)f, (uint64_t)rows, 32);
+  moe_status_t st;
+  if (fp4) {  // MXFP4 rows of d / 2 and f / 2 bytes
+    st = make_map_packed(&tm_a, a_q, (uint64_t)d / 2, (uint64_t)rows, kTileRows);
+    if (st == MOE_OK) st = make_map_packed(&tm_a32, a_q, (uint64_t)d / 2, (uint64_t)rows, 32);
+    if (st == MOE_OK) st = make_map_packed(&tm_h, h->ws.h_q, (uint64_t)f / 2, (uint64_t)rows, kTileRows);
+    if (st == MOE_OK) st = make_map_packed(&tm_h32, h->ws.h_q, (uint64_t)f / 2, (uint64_t)rows, 32);
+  } else {
+    st = make_map(&tm_a, a_q, false, (uint64_t)d, (uint64_t)rows, kTileRows);
+    if (st == MOE_OK) st = make_map(&tm_a32, a_q, false, (uint64_t)d, (uint64_t)rows, 32);
+    if (st == MOE_OK) st = make_map(&tm_h, h->ws.h_q, false, (uint64_t)f, (uint64_t)rows, kTileRows);
+    if (st == MOE_OK) st = make_map(&tm_h32, h->ws.h_q, false, (uint64_t)f, (uint64_t)rows, 32);
+  }
   if (st != MOE_OK) return st;
   const moe_experts_s* shx = sh ? sh : h;
-  MOE_CUDA(launch_gemm_gate_up(h->tm13, shx->tm13, h->sf13, shx->sf13, tm_a, tm_a32, a_sf_atoms, h->ws.tiles, h->ws.n_tiles,
-                               max_tiles, E_groups_shared_index, d, f, h->cfg.swiglu_limit, h->ws.h_q, h->ws.h_sf,
-                               h->status, h->budget_ns, h->stall_loads, tile_rows, h->num_sms, s),
+  MOE_CUDA(launch_gemm_gate_up(fp4 ? h->tm13p : h->tm13, fp4 ? shx->tm13p : shx->tm13, h->sf13, shx->sf13, tm_a, tm_a32,
+                               a_sf_atoms, h->ws.tiles, h->ws.n_tiles, max_tiles, E_groups_shared_index, d, f,
+                               h->cfg.swiglu_limit, h->ws.h_q, h->ws.h_sf, h->status, h->budget_ns, h->stall_loads,
+                               tile_rows, fp4, h->num_sms, s),
            "gate-up GEMM");
   if (timed) mark_stage(h, 3, s);
-  MOE_CUDA(launch_gemm_down(h->tm2, shx->tm2, h->sf2, shx->sf2, tm_h, tm_h32, h->ws.h_sf, h->ws.tiles, h->ws.n_tiles, max_tiles,
-                            E_groups_shared_index, d, f, row_w, y_f32, y_bf16, h->status, h->budget_ns,
-                            h->stall_loads, tile_rows, h->num_sms, s),
+  MOE_CUDA(launch_gemm_down(fp4 ? h->tm2p : h->tm2, fp4 ? shx->tm2p : shx->tm2, h->sf2, shx->sf2, tm_h, tm_h32,
+                            h->ws.h_sf, h->ws.tiles, h->ws.n_tiles, max_tiles, E_groups_shared_index, d, f, row_w, y_f32,
+                            y_bf16, h->status, h->budget_ns, h->stall_loads, tile_rows, fp4, h->num_sms, s),
            "down GEMM");
   return MOE_OK;
 }
@@ -449,6 +489,7 @@ moe_status_t moe_expert_ffn(moe_experts_t h, int32_t n_rows, const int32_t* offs
            "tile list");
   MOE_CUDA(launch_rows_sf_to_atoms(a_s, h->ws.tiles, h->ws.n_tiles, h->cfg.d_model, dm.max_tiles, h->ws.a_sf, s),
            "scale atoms");
+  h->last_rows = n_rows;
   return run_ffn(h, nullptr, n_rows, h->n, a_q, h->ws.a_sf, row_w, nullptr, static_cast<__nv_bfloat16*>(y_bf16),
                  dm.max_tiles, bn, false, s);
 }
@@ -481,6 +522,8 @@ moe_status_t forward_impl(const moe_input_t* x, const float* router_w, const flo
     if (sh->n != 1) return fail(MOE_ERR_INVALID_ARG, "shared set must hold exactly one expert");
     if (sh->cfg.d_model != h->cfg.d_model || sh->cfg.d_ff != h->cfg.d_ff)
       return fail(MOE_ERR_INVALID_ARG, "shared expert shape differs from the routed experts");
+    if (sh->act_fp4 != h->act_fp4)
+      return fail(MOE_ERR_INVALID_ARG, "shared and routed experts use different activation formats");
   }
   if (x->T > 0 && !out_bf16) return fail(MOE_ERR_INVALID_ARG, "out is NULL");
   if (out_bf16 && !aligned(out_bf16, 16)) return fail(MOE_ERR_INVALID_ARG, "out must be 16-byte aligned");
@@ -509,11 +552,12 @@ moe_status_t forward_impl(const moe_input_t* x, const float* router_w, const flo
            "scan");
   MOE_CUDA(launch_gather(static_cast<const __nv_bfloat16*>(x->x_bf16), h->ws.topk_ids, h->ws.topk_w, h->ws.chunk_hist,
                          h->ws.offsets, h->ws.tile_off, T, d, k, E, G, has_shared, bn, h->ws.a_q, h->ws.a_sf,
-                         nullptr, h->ws.perm_tok, h->ws.inv_pos, h->ws.row_w, s),
+                         nullptr, h->ws.perm_tok, h->ws.inv_pos, h->ws.row_w, h->act_fp4, s),
            "gather");
   mark_stage(h, 2, s);
   st = run_ffn(h, sh, rows, E, h->ws.a_q, h->ws.a_sf, h->ws.row_w, h->ws.y_rows, nullptr, dm.max_tiles, bn, true, s);
   if (st != MOE_OK) return st;
+  h->last_rows = rows;
   mark_stage(h, 4, s);
   MOE_CUDA(launch_combine(h->ws.y_rows, h->ws.inv_pos, T, d, k, R, has_shared,
                           static_cast<const __nv_bfloat16*>(residual_bf16), static_cast<__nv_bfloat16*>(out_bf16), s),
@@ -536,6 +580,21 @@ moe_status_t moe_get_routing(moe_experts_t h, const int32_t** ids, const float**
   *ids = h->ws.topk_ids;
   *w = h->ws.topk_w;
   *T = h->last_T;
+  return MOE_OK;
+}
+
+moe_status_t moe_testing_read_h(moe_experts_t h, uint8_t* h_q, uint8_t* h_s, int32_t* n_rows, moe_stream_t stream) {
+  if (!h || !n_rows) return fail(MOE_ERR_INVALID_ARG, "NULL argument");
+  if (!h->ws_base) return fail(MOE_ERR_WORKSPACE, "no workspace attached");
+  *n_rows = h->last_rows;
+  if (h->last_rows == 0 || (!h_q && !h_s)) return MOE_OK;  // a query of the row count
+  if (!h_q || !h_s || !aligned(h_s, 4)) return fail(MOE_ERR_INVALID_ARG, "h_q / h_s NULL or h_s not 4-byte aligned");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int f = h->cfg.d_ff;
+  const Dims dm = dims_for(h->ws_max_T, h->cfg.n_experts, h->cfg.top_k);
+  const size_t row_bytes = h->act_fp4 ? (size_t)f / 2 : (size_t)f;
+  MOE_CUDA(cudaMemcpyAsync(h_q, h->ws.h_q, row_bytes * h->last_rows, cudaMemcpyDeviceToDevice, s), "h codes");
+  MOE_CUDA(launch_atoms_to_rows_sf(h->ws.h_sf, h->ws.tiles, h->ws.n_tiles, f, dm.max_tiles, h_s, s), "h scales");
   return MOE_OK;
 }
 

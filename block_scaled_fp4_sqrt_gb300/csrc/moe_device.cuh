@@ -190,7 +190,7 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
 // ------------------------------------------------------------------------- tcgen05
 // Shared-memory matrix descriptor (tcgen05 format): start address, leading / stride byte offsets
 // (all >> 4), fixed version bits 46..47 = 1, swizzle mode in bits 61..63 (2 = 128-byte swizzle,
-// 0 = none).
+// 4 = 64-byte swizzle, 0 = none).
 __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo, uint32_t swizzle) {
   uint64_t d = 0;
   d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
@@ -204,6 +204,10 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
 // Instruction descriptor of kind::mxf8f6f4 with E8M0 block scales.
 // Formats: 0 = E4M3, 5 = E2M1.  M in {128}, N multiple of 16 up to 256.  sf ids pick the byte of
 // the 32-bit scale word (the 32-element K block inside a 128-element group).
+// kind::mxf4 (both operands E2M1, packed two per byte in shared memory, K = 64 per MMA): the E2M1
+// format code of this kind is 1.
+constexpr uint32_t kMxf4E2M1 = 1;
+
 __host__ __device__ __forceinline__ constexpr uint32_t mma_idesc(uint32_t a_fmt, uint32_t b_fmt, uint32_t M,
                                                                  uint32_t N, uint32_t a_sf_id, uint32_t b_sf_id) {
   return ((b_sf_id & 3u) << 4) | ((a_fmt & 7u) << 7) | ((b_fmt & 7u) << 10) | (((N >> 3) & 63u) << 17) |
@@ -270,6 +274,33 @@ __device__ __forceinline__ bool tc_stage4_mx_commit_poll(uint32_t d_tmem, uint64
   return ok != 0;
 }
 
+// The MXFP4-activation variant's stage: two block-scaled MMAs of kind::mxf4 (E2M1 x E2M1, K = 64 each,
+// scale_vec::2X: two E8M0 scales per row and MMA), fused with the commit and a barrier test as above.
+// A stage holds K = 128 packed in 64-byte rows: MMA k reads bytes 32k.. of each row (descriptor
+// address + 2k) and scale bytes 2k, 2k+1 of the 32-bit scale word (sf id 2k).
+__device__ __forceinline__ bool tc_stage2_mxf4_commit_poll(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                                           uint32_t idesc0, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                                           uint32_t accumulate, uint64_t* commit_bar,
+                                                           uint64_t* poll_bar, uint32_t poll_parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p, q, t;\n .reg .b64 a1, b1;\n .reg .b32 i1;\n"
+      " mbarrier.test_wait.parity.shared::cta.b64 q, [%8], %9;\n"
+      " setp.ne.b32 p, %4, 0;\n"
+      " setp.eq.b32 t, 0, 0;\n"
+      " add.s64 a1, %2, 2;\n add.s64 b1, %3, 2;\n"
+      " or.b32 i1, %5, 0x40000020;\n"
+      " tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%1], %2, %3, %5, [%6], [%7], p;\n"
+      " tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%1], a1, b1, i1, [%6], [%7], t;\n"
+      " tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%10];\n"
+      " selp.u32 %0, 1, 0, q;\n}\n"
+      : "=r"(ok)
+      : "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(accumulate), "r"(idesc0), "r"(sfa_tmem), "r"(sfb_tmem),
+        "r"(smem_addr(poll_bar)), "r"(poll_parity), "r"(smem_addr(commit_bar))
+      : "memory");
+  return ok != 0;
+}
+
 __device__ __forceinline__ void tc_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
                : "memory");
@@ -308,6 +339,13 @@ __device__ __forceinline__ int mxfp8_block_exp(float amax) {
   return s < -127 ? -127 : (s > 127 ? 127 : s);
 }
 
+// E8M0 block exponent for an MXFP4 (E2M1, emax 2) block with maximum magnitude amax.
+__device__ __forceinline__ int mxfp4_block_exp(float amax) {
+  if (!(amax > 0.0f)) return -127;
+  int s = floor_log2_f32(amax) - 2;
+  return s < -127 ? -127 : (s > 127 ? 127 : s);
+}
+
 // 2^-s as fp32 for s in [-127, 127] (2^127 is representable; 2^-127 is subnormal, built from bits).
 __device__ __forceinline__ float exp2_neg_int(int s) {
   int e = 127 - s;  // biased exponent of 2^-s
@@ -320,6 +358,32 @@ __device__ __forceinline__ uint16_t e4m3x2(float lo, float hi) {
   uint16_t r;
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
   return r;
+}
+
+// Round-to-nearest-even, saturating E2M1 conversion of eight values (hardware cvt); value i in bits
+// 4i..4i+3, i.e. element 2j in the low nibble of byte j.
+__device__ __forceinline__ uint32_t e2m1x8(float v0, float v1, float v2, float v3, float v4, float v5, float v6,
+                                           float v7) {
+  uint32_t r;
+  asm("{\n .reg .b8 b0, b1, b2, b3;\n"
+      " cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n"
+      " cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n"
+      " cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n"
+      " cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n"
+      " mov.b32 %0, {b0, b1, b2, b3};\n}"
+      : "=r"(r)
+      : "f"(v0), "f"(v1), "f"(v2), "f"(v3), "f"(v4), "f"(v5), "f"(v6), "f"(v7));
+  return r;
+}
+
+// One MX block of 32 values -> 16 bytes of packed E2M1 codes, each value multiplied by mul first.
+__device__ __forceinline__ uint4 e2m1_block(const float (&v)[32], float mul) {
+  uint32_t w[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    w[i] = e2m1x8(v[8 * i] * mul, v[8 * i + 1] * mul, v[8 * i + 2] * mul, v[8 * i + 3] * mul, v[8 * i + 4] * mul,
+                  v[8 * i + 5] * mul, v[8 * i + 6] * mul, v[8 * i + 7] * mul);
+  return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
 }  // namespace moe

@@ -185,6 +185,9 @@ __global__ void __launch_bounds__(1024) groupscan_kernel(const int32_t* __restri
 //    instructions of 512 contiguous bytes (lane l stores 16-byte chunk l of each half, moved there by
 //    shuffles); four consecutive threads (one 128-element K group) pack their scale bytes into one
 //    32-bit word, which is one word of a scale atom.
+//  * FP4 (the MXFP4-activation variant): the warp's 32 blocks are 512 bytes of packed E2M1 codes, and
+//    lane l's 16 bytes are chunk l of them: one store per destination row, no shuffles.
+template <bool FP4>
 __global__ void __launch_bounds__(128) gather_kernel(
     const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ ids, const float* __restrict__ wts,
     const int32_t* __restrict__ chunk_base, int n_chunks, const int32_t* __restrict__ offsets,
@@ -277,13 +280,21 @@ __global__ void __launch_bounds__(128) gather_kernel(
         float amax = 0.f;
 #pragma unroll
         for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
-        const int se = mxfp8_block_exp(amax);
+        const int se = FP4 ? mxfp4_block_exp(amax) : mxfp8_block_exp(amax);
         const float mul = exp2_neg_int(se);
+        if (FP4) {
+          const uint4 c = e2m1_block(v, mul);
+          packed[0] = c.x;
+          packed[1] = c.y;
+          packed[2] = c.z;
+          packed[3] = c.w;
+        } else {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const uint32_t lo = e4m3x2(v[4 * i] * mul, v[4 * i + 1] * mul);
-          const uint32_t hi = e4m3x2(v[4 * i + 2] * mul, v[4 * i + 3] * mul);
-          packed[i] = lo | (hi << 16);
+          for (int i = 0; i < 8; ++i) {
+            const uint32_t lo = e4m3x2(v[4 * i] * mul, v[4 * i + 1] * mul);
+            const uint32_t hi = e4m3x2(v[4 * i + 2] * mul, v[4 * i + 3] * mul);
+            packed[i] = lo | (hi << 16);
+          }
         }
         byte = (uint32_t)(se + 127);
       } else {
@@ -299,7 +310,7 @@ __global__ void __launch_bounds__(128) gather_kernel(
       const int wb0 = b - lane;  // the warp's first MX block
       uint4 outv[2];
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
+      for (int h = 0; h < (FP4 ? 0 : 2); ++h) {
         const int src_lane = 16 * h + (lane >> 1);
         uint32_t w4[4];
 #pragma unroll
@@ -313,11 +324,16 @@ __global__ void __launch_bounds__(128) gather_kernel(
       const int grp = b >> 2;
       for (int q = 0; q < n_dst; ++q) {
         const int row = s_row[q];
-        uint8_t* rowp = a_q + (size_t)row * d;
+        if (FP4) {
+          if (on) reinterpret_cast<uint4*>(a_q + (size_t)row * (d / 2))[b] =
+              make_uint4(packed[0], packed[1], packed[2], packed[3]);
+        } else {
+          uint8_t* rowp = a_q + (size_t)row * d;
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int blk = wb0 + 16 * h + (lane >> 1);  // MX block whose half this lane stores
-          if (blk < nb) reinterpret_cast<uint4*>(rowp + (size_t)blk * 32)[lane & 1] = outv[h];
+          for (int h = 0; h < 2; ++h) {
+            const int blk = wb0 + 16 * h + (lane >> 1);  // MX block whose half this lane stores
+            if (blk < nb) reinterpret_cast<uint4*>(rowp + (size_t)blk * 32)[lane & 1] = outv[h];
+          }
         }
         if (on && (b & 3) == 0) {
           if (a_sf_atoms) {
@@ -439,14 +455,18 @@ cudaError_t launch_tiles_from_offsets(const int32_t* offsets, int G, int n_rows,
 cudaError_t launch_gather(const __nv_bfloat16* x, const int32_t* ids, const float* wts, const int32_t* chunk_hist,
                           const int32_t* offsets, const int32_t* tile_off, int T, int d, int k, int E, int G,
                           int has_shared, int bn, uint8_t* a_q, uint8_t* a_sf_atoms, uint8_t* a_s_rows,
-                          int32_t* perm_tok, int32_t* inv_pos, float* row_w, cudaStream_t s) {
+                          int32_t* perm_tok, int32_t* inv_pos, float* row_w, int act_fp4, cudaStream_t s) {
   (void)G;
   const int n_chunks = (T + 31) / 32;
   const int nb = d / 32;
   const int threads = nb >= 128 ? 128 : ((nb + 31) / 32) * 32;
   const int blocks = T < 152 * 16 ? T : 152 * 16;
-  return launch_pdl(gather_kernel, dim3(blocks), dim3(threads), 0, s, x, ids, wts, chunk_hist, n_chunks, offsets,
-                    tile_off, T, d, k, E, has_shared, bn, a_q, a_sf_atoms, a_s_rows, perm_tok, inv_pos, row_w);
+  if (act_fp4)
+    return launch_pdl(gather_kernel<true>, dim3(blocks), dim3(threads), 0, s, x, ids, wts, chunk_hist, n_chunks,
+                      offsets, tile_off, T, d, k, E, has_shared, bn, a_q, a_sf_atoms, a_s_rows, perm_tok, inv_pos,
+                      row_w);
+  return launch_pdl(gather_kernel<false>, dim3(blocks), dim3(threads), 0, s, x, ids, wts, chunk_hist, n_chunks,
+                    offsets, tile_off, T, d, k, E, has_shared, bn, a_q, a_sf_atoms, a_s_rows, perm_tok, inv_pos, row_w);
 }
 
 cudaError_t launch_combine(const float* y_rows, const int32_t* inv_pos, int T, int d, int k, int R,

@@ -27,6 +27,12 @@
 // four warps per 32-lane TMEM quadrant, each owning a quarter of the 256 columns, so one thread holds
 // one token row of one MX block and needs no shuffles.  The accumulator is released as soon as it is
 // in registers.  Every wait is bounded; on timeout the kernel records DEV_TIMEOUT and unwinds.
+//
+// MXFP4-activation variant (FP4 = true): activations and h are MXFP4 too, and the MMA is kind::mxf4
+// (E2M1 x E2M1, K = 64, two scales per row and MMA).  Both operands stay packed in shared memory: a
+// stage's K = 128 is one 64-byte row per operand row (64-byte swizzle), two MMAs per stage, so the
+// weight ring takes half the shared memory and the tensor pipe does twice the work per instruction.
+// The weights, their scale atoms and the activation scale atoms are the same as in the MXFP8 path.
 #include "moe_device.cuh"
 
 namespace moe {
@@ -47,10 +53,14 @@ constexpr int kStageFloats = 32 * kStageStride;
 
 // EPI = 1: the down projection's fp32 rows leave through a per-warp shared-memory transpose (full
 // 128-byte lines per quarter warp) instead of 16-byte stores to 32 different rows per instruction.
-template <int STAGES, int AROWS, int EPI = 0>
+// FP4: packed MXFP4 operands (64-byte rows, kind::mxf4) instead of E4M3 x byte-expanded E2M1.
+template <int STAGES, int AROWS, int EPI = 0, bool FP4 = false>
 struct Cfg {
-  static constexpr int kASlot = AROWS * 128;         // activation rows x 128 FP8
-  static constexpr int kBSlot = kN * 128;            // 256 weight rows x 128 FP4, padded to bytes
+  static constexpr int kRowBytes = FP4 ? 64 : 128;   // one operand row of a stage (K = 128) in smem
+  static constexpr uint32_t kSwizzle = FP4 ? 4 : 2;  // descriptor layout: 64- or 128-byte swizzle
+  static constexpr uint32_t kSbo = 8 * kRowBytes;    // stride of the 8-row core groups
+  static constexpr int kASlot = AROWS * kRowBytes;   // activation rows x 128 FP8 (or FP4)
+  static constexpr int kBSlot = kN * kRowBytes;      // 256 weight rows x 128 FP4 (padded to bytes, or packed)
   static constexpr int kSfSlot = 3 * kSfAtomBytes;   // activation atom + two weight atoms
   static constexpr int kAOff = 0;                    // [activation ring | weight ring | scale ring]
   static constexpr int kBOff = STAGES * kASlot;
@@ -67,7 +77,7 @@ struct Cfg {
   // warps that drain the accumulator: with rows only in TMEM lanes 0..31, the four warps of quadrant 0
   static constexpr int kDrainWarps = AROWS == kSmallRows ? kEpiWarps / 4 : kEpiWarps;
   static_assert(kBOff % 1024 == 0 && kSfOff % 1024 == 0, "swizzled tiles need 1024-byte alignment");
-  static_assert(AROWS == kBM || kBOff >= (kBM - AROWS) * 128, "M = 128 reads past a short activation slot");
+  static_assert(AROWS == kBM || kBOff >= (kBM - AROWS) * kRowBytes, "M = 128 reads past a short activation slot");
   static_assert(kAccCols + STAGES * kSfCols <= kTmemCols, "TMEM budget");
   static_assert(kEpiOff % 16 == 0, "staging rows are float4-aligned");
   static_assert(kSmem <= 232448 - 64, "shared memory budget");
@@ -101,12 +111,12 @@ struct GemmArgs {
 
 __device__ __forceinline__ float silu_f(float z) { return z / (1.0f + expf(-z)); }
 
-template <int STAGES, int AROWS, int EPI>
+template <int STAGES, int AROWS, int EPI, bool FP4>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_mx_gemm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_w_shared,
                            const __grid_constant__ CUtensorMap tm_act, const __grid_constant__ CUtensorMap tm_act_small,
                            const GemmArgs a) {
-  using C = Cfg<STAGES, AROWS, EPI>;
+  using C = Cfg<STAGES, AROWS, EPI, FP4>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
@@ -166,7 +176,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int e = sh ? 0 : rt.group;
         const bool small = AROWS == kSmallRows || rt.nrows <= kSmallRows;
         const CUtensorMap* ta = small ? &tm_act_small : &tm_act;
-        const uint32_t tx = C::kTxB + (small ? kSmallRows : kBM) * 128 + kSfAtomBytes;
+        const uint32_t tx = C::kTxB + (small ? kSmallRows : kBM) * C::kRowBytes + kSfAtomBytes;
         // packed weights are [expert][K group][output tile][256 rows]: slab (e, kg, mt)
         const int wrow0 = (e * a.KG * a.m_tiles + mt) * kN;
         const int wrow_kg = a.m_tiles * kN;
@@ -180,7 +190,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           mbar_arrive_expect_tx(&full[stage], tx);
           tma_load_2d(smem + C::kBOff + stage * C::kBSlot, tw, 0, wrow0 + kg * wrow_kg, &full[stage], pol_w);
-          tma_load_2d(smem + C::kAOff + stage * C::kASlot, ta, kg * kKGroup, rt.row0, &full[stage], pol_a);
+          tma_load_2d(smem + C::kAOff + stage * C::kASlot, ta, kg * C::kRowBytes, rt.row0, &full[stage], pol_a);
           uint8_t* sf = smem + C::kSfOff + stage * C::kSfSlot;
           bulk_load(sf, sfa + kg * kSfAtomBytes, kSfAtomBytes, &full[stage]);
           bulk_load(sf + kSfAtomBytes, sfw + kg * sfw_kg, 2 * kSfAtomBytes, &full[stage]);
@@ -203,7 +213,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------------------------------------------------------- MMA issuer
-      // A = activations (E4M3), B = weights (E2M1).  The tensor pipe queues only a couple of MMAs, so
+      // A = activations (E4M3, or E2M1), B = weights (E2M1).  The tensor pipe queues only a couple of MMAs, so
       // this thread's instruction stream is on the critical path: descriptors are precomputed,
       // slots and phases advance incrementally (the same stage sequence as the producer's), and the
       // stage's four MMAs, its commit and a barrier test are one fused instruction block.  A scale
@@ -211,11 +221,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       // so the scale atoms of a stage are copied into TMEM as soon as the stage is seen to have
       // landed (tested inside the MMA block of an earlier stage, up to kAhead stages ahead); only a
       // stage that has not landed by the time its MMAs are due is waited for in front of them.
-      constexpr uint32_t kIdesc0 = mma_idesc(0, 5, kBM, kN, 0, 0);
+      constexpr uint32_t kIdesc0 = FP4 ? mma_idesc(kMxf4E2M1, kMxf4E2M1, kBM, kN, 0, 0) : mma_idesc(0, 5, kBM, kN, 0, 0);
       constexpr int kAhead = 2;
       static_assert(STAGES > kAhead, "scale copies run up to kAhead stages ahead of the MMAs");
-      const uint64_t a_desc0 = smem_desc(smem_addr(smem + C::kAOff), 16, 1024, 2);
-      const uint64_t b_desc0 = smem_desc(smem_addr(smem + C::kBOff), 16, 1024, 2);
+      const uint64_t a_desc0 = smem_desc(smem_addr(smem + C::kAOff), 16, C::kSbo, C::kSwizzle);
+      const uint64_t b_desc0 = smem_desc(smem_addr(smem + C::kBOff), 16, C::kSbo, C::kSwizzle);
       const uint64_t sf_desc0 = smem_desc(smem_addr(smem + C::kSfOff), 128, 128, 0);
       const uint32_t sf_tmem0 = tbase + (uint32_t)C::kAccCols;
       auto copy_sf = [&](int slot) {  // activation atom, then the two weight atoms (512 B apart)
@@ -257,10 +267,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const bool look = lg < n_st && lg <= g + kAhead;
           // with nothing to look ahead for, the test re-reads this stage's own (completed) barrier
-          const bool landed = tc_stage4_mx_commit_poll(
-              tbase, a_desc0 + (uint64_t)((cs * C::kASlot) >> 4), b_desc0 + (uint64_t)((cs * C::kBSlot) >> 4),
-              kIdesc0, sf_tmem0 + (uint32_t)(cs * C::kSfCols), sf_tmem0 + (uint32_t)(cs * C::kSfCols + 4),
-              kg != 0 ? 1u : 0u, &empty[cs], look ? &full[ls] : &full[cs], look ? lph : cph);
+          const uint64_t ad = a_desc0 + (uint64_t)((cs * C::kASlot) >> 4);
+          const uint64_t bd = b_desc0 + (uint64_t)((cs * C::kBSlot) >> 4);
+          const uint32_t sfa = sf_tmem0 + (uint32_t)(cs * C::kSfCols);
+          const bool landed =
+              FP4 ? tc_stage2_mxf4_commit_poll(tbase, ad, bd, kIdesc0, sfa, sfa + 4, kg != 0 ? 1u : 0u, &empty[cs],
+                                               look ? &full[ls] : &full[cs], look ? lph : cph)
+                  : tc_stage4_mx_commit_poll(tbase, ad, bd, kIdesc0, sfa, sfa + 4, kg != 0 ? 1u : 0u, &empty[cs],
+                                             look ? &full[ls] : &full[cs], look ? lph : cph);
           any = true;
           if (kg == a.KG - 1) tc_commit(acc_full);
           if (look && landed) {
@@ -359,18 +373,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           h[j] = silu_f(gc) * uc;
           amax = fmaxf(amax, fabsf(h[j]));
         }
-        const int se = mxfp8_block_exp(amax);
+        const int se = FP4 ? mxfp4_block_exp(amax) : mxfp8_block_exp(amax);
         const float mul = exp2_neg_int(se);
-        uint32_t packed[8];
+        if (FP4) {  // 32 E2M1 codes: 16 bytes at h column mt * 128 + 32 c of a row of f / 2 bytes
+          *reinterpret_cast<uint4*>(a.h_q + (size_t)r * (a.f / 2) + mt * (kKGroup / 2) + 16 * c) = e2m1_block(v0, mul);
+        } else {
+          uint32_t packed[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const uint32_t lo = e4m3x2(h[4 * i] * mul, h[4 * i + 1] * mul);
-          const uint32_t hi = e4m3x2(h[4 * i + 2] * mul, h[4 * i + 3] * mul);
-          packed[i] = lo | (hi << 16);
+          for (int i = 0; i < 8; ++i) {
+            const uint32_t lo = e4m3x2(h[4 * i] * mul, h[4 * i + 1] * mul);
+            const uint32_t hi = e4m3x2(h[4 * i + 2] * mul, h[4 * i + 3] * mul);
+            packed[i] = lo | (hi << 16);
+          }
+          uint4* dst = reinterpret_cast<uint4*>(a.h_q + (size_t)r * a.f + mt * kKGroup + 32 * c);
+          dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+          dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
         }
-        uint4* dst = reinterpret_cast<uint4*>(a.h_q + (size_t)r * a.f + mt * kKGroup + 32 * c);
-        dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-        dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
         a.h_sf[((size_t)ti * (a.f / kKGroup) + mt) * kSfAtomBytes + (lr & 31) * 16 + (lr >> 5) * 4 + c] =
             (uint8_t)(se + 127);
       } else {
@@ -406,31 +424,37 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc(tbase, C::kTmemCols);
 }
 
-template <int STAGES, int AROWS, int EPI>
+template <int STAGES, int AROWS, int EPI, bool FP4>
 cudaError_t launch_shape(const CUtensorMap& w, const CUtensorMap& w_sh, const CUtensorMap& act,
                          const CUtensorMap& act_small, const GemmArgs& a, int num_sms, cudaStream_t s) {
-  using C = Cfg<STAGES, AROWS, EPI>;
+  using C = Cfg<STAGES, AROWS, EPI, FP4>;
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(grouped_mx_gemm_kernel<STAGES, AROWS, EPI>,
+    cudaError_t e = cudaFuncSetAttribute(grouped_mx_gemm_kernel<STAGES, AROWS, EPI, FP4>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  return launch_pdl(grouped_mx_gemm_kernel<STAGES, AROWS, EPI>, dim3(num_sms), dim3(kThreads), C::kSmem, s, w, w_sh,
-                    act, act_small, a);
+  return launch_pdl(grouped_mx_gemm_kernel<STAGES, AROWS, EPI, FP4>, dim3(num_sms), dim3(kThreads), C::kSmem, s, w,
+                    w_sh, act, act_small, a);
 }
 
 // tile_rows 32: 6 stages of 32-row activation slots.  tile_rows 128: 4 stages of 128-row slots, or for
 // the down projection's fp32 rows 3 stages plus the epilogue's staging buffers (the 16-byte scattered
 // stores of the direct epilogue bound that GEMM at the 8192-token shape: 835 us with them, 373 us
 // without any stores).
+// FP4: the packed weight ring is half as large, so every shape holds more stages.
 cudaError_t launch_grouped(const CUtensorMap& w, const CUtensorMap& w_sh, const CUtensorMap& act,
-                           const CUtensorMap& act_small, const GemmArgs& a, int tile_rows, int num_sms,
+                           const CUtensorMap& act_small, const GemmArgs& a, int tile_rows, int act_fp4, int num_sms,
                            cudaStream_t s) {
-  if (tile_rows == kSmallRows) return launch_shape<6, kSmallRows, 0>(w, w_sh, act, act_small, a, num_sms, s);
-  if (!a.gate_up && a.y_f32) return launch_shape<3, kBM, 1>(w, w_sh, act, act_small, a, num_sms, s);
-  return launch_shape<4, kBM, 0>(w, w_sh, act, act_small, a, num_sms, s);
+  if (act_fp4) {
+    if (tile_rows == kSmallRows) return launch_shape<8, kSmallRows, 0, true>(w, w_sh, act, act_small, a, num_sms, s);
+    if (!a.gate_up && a.y_f32) return launch_shape<6, kBM, 1, true>(w, w_sh, act, act_small, a, num_sms, s);
+    return launch_shape<8, kBM, 0, true>(w, w_sh, act, act_small, a, num_sms, s);
+  }
+  if (tile_rows == kSmallRows) return launch_shape<6, kSmallRows, 0, false>(w, w_sh, act, act_small, a, num_sms, s);
+  if (!a.gate_up && a.y_f32) return launch_shape<3, kBM, 1, false>(w, w_sh, act, act_small, a, num_sms, s);
+  return launch_shape<4, kBM, 0, false>(w, w_sh, act, act_small, a, num_sms, s);
 }
 
 }  // namespace
@@ -439,7 +463,8 @@ cudaError_t launch_gemm_gate_up(const CUtensorMap& w_routed, const CUtensorMap& 
                                 const uint8_t* sf_shared, const CUtensorMap& act, const CUtensorMap& act_small,
                                 const uint8_t* act_sf, const RowTile* tiles, const int32_t* n_tiles, int max_tiles,
                                 int E, int d, int f, float limit, uint8_t* h_q, uint8_t* h_sf, int* status,
-                                uint64_t wait_budget_ns, int stall_loads, int tile_rows, int num_sms, cudaStream_t s) {
+                                uint64_t wait_budget_ns, int stall_loads, int tile_rows, int act_fp4, int num_sms,
+                                cudaStream_t s) {
   GemmArgs a{};
   a.sf_routed = sf_routed;
   a.sf_shared = sf_shared ? sf_shared : sf_routed;
@@ -459,14 +484,15 @@ cudaError_t launch_gemm_gate_up(const CUtensorMap& w_routed, const CUtensorMap& 
   a.status = status;
   a.budget_ns = wait_budget_ns;
   a.stall_loads = stall_loads;
-  return launch_grouped(w_routed, w_shared, act, act_small, a, tile_rows, num_sms, s);
+  return launch_grouped(w_routed, w_shared, act, act_small, a, tile_rows, act_fp4, num_sms, s);
 }
 
 cudaError_t launch_gemm_down(const CUtensorMap& w_routed, const CUtensorMap& w_shared, const uint8_t* sf_routed,
                              const uint8_t* sf_shared, const CUtensorMap& act, const CUtensorMap& act_small,
                              const uint8_t* act_sf, const RowTile* tiles, const int32_t* n_tiles, int max_tiles, int E,
                              int d, int f, const float* row_w, float* y_f32, __nv_bfloat16* y_bf16, int* status,
-                             uint64_t wait_budget_ns, int stall_loads, int tile_rows, int num_sms, cudaStream_t s) {
+                             uint64_t wait_budget_ns, int stall_loads, int tile_rows, int act_fp4, int num_sms,
+                             cudaStream_t s) {
   GemmArgs a{};
   a.sf_routed = sf_routed;
   a.sf_shared = sf_shared ? sf_shared : sf_routed;
@@ -486,7 +512,7 @@ cudaError_t launch_gemm_down(const CUtensorMap& w_routed, const CUtensorMap& w_s
   a.status = status;
   a.budget_ns = wait_budget_ns;
   a.stall_loads = stall_loads;
-  return launch_grouped(w_routed, w_shared, act, act_small, a, tile_rows, num_sms, s);
+  return launch_grouped(w_routed, w_shared, act, act_small, a, tile_rows, act_fp4, num_sms, s);
 }
 
 }  // namespace moe

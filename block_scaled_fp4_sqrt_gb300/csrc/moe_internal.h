@@ -121,15 +121,19 @@ cudaError_t launch_histogram(const int32_t* ids, int T, int k, int E, int G, int
 cudaError_t launch_scan(int32_t* chunk_hist, int n_chunks, int T, int E, int G, int has_shared, int bn, int max_tiles,
                         int32_t* counts, int32_t* offsets, int32_t* tile_off, int32_t* n_tiles, RowTile* tiles,
                         int* status, cudaStream_t s);
-// Quantise x to MXFP8 and scatter each token row to its k routed rows (+ its shared row).
-// a_sf_atoms / a_s_rows may each be null (kernel-layout scale atoms / canonical [rows, d/32]).
+// Quantise x to MXFP8 (act_fp4: MXFP4, rows of d/2 bytes) and scatter each token row to its k routed
+// rows (+ its shared row).  a_sf_atoms / a_s_rows may each be null (kernel-layout scale atoms /
+// canonical [rows, d/32]).
 cudaError_t launch_gather(const __nv_bfloat16* x, const int32_t* ids, const float* wts, const int32_t* chunk_hist,
                           const int32_t* offsets, const int32_t* tile_off, int T, int d, int k, int E, int G,
                           int has_shared, int bn, uint8_t* a_q, uint8_t* a_sf_atoms, uint8_t* a_s_rows,
-                          int32_t* perm_tok, int32_t* inv_pos, float* row_w, cudaStream_t s);
+                          int32_t* perm_tok, int32_t* inv_pos, float* row_w, int act_fp4, cudaStream_t s);
 // Canonical [rows, d/32] scales -> per-tile atoms (for moe_expert_ffn on caller buffers).
 cudaError_t launch_rows_sf_to_atoms(const uint8_t* a_s_rows, const RowTile* tiles, const int32_t* n_tiles, int d,
                                     int max_tiles, uint8_t* atoms, cudaStream_t s);
+// Per-tile atoms -> canonical [rows, K/32] (reads back the h scales for tests).
+cudaError_t launch_atoms_to_rows_sf(const uint8_t* atoms, const RowTile* tiles, const int32_t* n_tiles, int K,
+                                    int max_tiles, uint8_t* rows_sf, cudaStream_t s);
 cudaError_t launch_tiles_from_offsets(const int32_t* offsets, int G, int n_rows, int bn, int max_tiles,
                                       int32_t* tile_off, int32_t* n_tiles, RowTile* tiles, int* status,
                                       cudaStream_t s);
@@ -143,19 +147,24 @@ cudaError_t launch_pack_weights(const uint8_t* codes, int n, int rows, int K, in
 cudaError_t launch_pack_weight_sf(const uint8_t* sc, int n, int rows, int K, int mode, uint8_t* atoms,
                                   cudaStream_t s);
 
+// Grouped GEMMs.  act_fp4 = 0: MXFP8 activations (E4M3 rows of K bytes) x MXFP4 weights on
+// kind::mxf8f6f4, weight maps of 16U4_ALIGN16B type (K = 128 elements expanded to 128-byte rows);
+// act_fp4 = 1: MXFP4 activations (rows of K/2 bytes) on kind::mxf4, every map 8-bit over packed bytes
+// with 64-byte rows and 64-byte swizzle.  The gate-up epilogue writes h in the same format.
 cudaError_t launch_gemm_gate_up(const CUtensorMap& w_routed, const CUtensorMap& w_shared, const uint8_t* sf_routed,
                                 const uint8_t* sf_shared, const CUtensorMap& act, const CUtensorMap& act_small,
                                 const uint8_t* act_sf,
                                 const RowTile* tiles, const int32_t* n_tiles, int max_tiles, int E, int d, int f,
                                 float limit,
                                 uint8_t* h_q, uint8_t* h_sf, int* status, uint64_t wait_budget_ns, int stall_loads,
-                                int tile_rows, int num_sms, cudaStream_t s);
+                                int tile_rows, int act_fp4, int num_sms, cudaStream_t s);
 cudaError_t launch_gemm_down(const CUtensorMap& w_routed, const CUtensorMap& w_shared, const uint8_t* sf_routed,
                              const uint8_t* sf_shared, const CUtensorMap& act, const CUtensorMap& act_small,
                              const uint8_t* act_sf,
                              const RowTile* tiles, const int32_t* n_tiles, int max_tiles, int E, int d, int f,
                              const float* row_w, float* y_f32, __nv_bfloat16* y_bf16, int* status,
-                             uint64_t wait_budget_ns, int stall_loads, int tile_rows, int num_sms, cudaStream_t s);
+                             uint64_t wait_budget_ns, int stall_loads, int tile_rows, int act_fp4, int num_sms,
+                             cudaStream_t s);
 
 cudaError_t launch_combine(const float* y_rows, const int32_t* inv_pos, int T, int d, int k, int R, int has_shared,
                            const __nv_bfloat16* residual, __nv_bfloat16* out, cudaStream_t s);

@@ -26,6 +26,23 @@ __global__ void rows_sf_to_atoms_kernel(const uint8_t* __restrict__ a_s_rows, co
   }
 }
 
+// the inverse: per-tile atoms [tile, K/128, 512] -> canonical [rows, K/32] scale bytes
+__global__ void atoms_to_rows_sf_kernel(const uint8_t* __restrict__ atoms, const RowTile* __restrict__ tiles,
+                                        const int32_t* __restrict__ n_tiles, int K, int max_tiles,
+                                        uint8_t* __restrict__ rows_sf) {
+  const int nt = min(*n_tiles, max_tiles);
+  const int groups = K / kKGroup;
+  for (int ti = blockIdx.x; ti < nt; ti += gridDim.x) {
+    const RowTile rt = tiles[ti];
+    for (int idx = threadIdx.x; idx < rt.nrows * groups; idx += blockDim.x) {
+      const int n = idx / groups, grp = idx - n * groups;
+      const uint32_t word = *reinterpret_cast<const uint32_t*>(atoms + ((size_t)ti * groups + grp) * kSfAtomBytes +
+                                                               (n & 31) * 16 + ((n >> 5) & 3) * 4);
+      *reinterpret_cast<uint32_t*>(rows_sf + (size_t)(rt.row0 + n) * (K / 32) + grp * 4) = word;
+    }
+  }
+}
+
 // Output tile and row inside its 256-row slab of canonical weight row `row` (see launch_pack_weights).
 __device__ __forceinline__ void slab_of_row(int row, int rows, int mode, int* tile, int* rr) {
   if (mode == 0) {
@@ -87,6 +104,12 @@ __global__ void pack_weight_sf_kernel(const uint8_t* __restrict__ s, int n, int 
 cudaError_t launch_rows_sf_to_atoms(const uint8_t* a_s_rows, const RowTile* tiles, const int32_t* n_tiles, int d,
                                     int max_tiles, uint8_t* atoms, cudaStream_t s) {
   rows_sf_to_atoms_kernel<<<296, 256, 0, s>>>(a_s_rows, tiles, n_tiles, d, max_tiles, atoms);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_atoms_to_rows_sf(const uint8_t* atoms, const RowTile* tiles, const int32_t* n_tiles, int K,
+                                    int max_tiles, uint8_t* rows_sf, cudaStream_t s) {
+  atoms_to_rows_sf_kernel<<<296, 256, 0, s>>>(atoms, tiles, n_tiles, K, max_tiles, rows_sf);
   return cudaGetLastError();
 }
 

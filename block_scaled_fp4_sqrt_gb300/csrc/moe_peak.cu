@@ -1,9 +1,10 @@
-// Measured peak of the block-scaled tensor-core MMA the grouped GEMMs use (tcgen05.mma
-// kind::mxf8f6f4.block_scale.scale_vec::1X, E4M3 x E2M1, M = 128, N = 256, K = 32): the denominator
-// of the tensor-bound roofline.  One CTA per SM issues MMAs back to back with its operands rotating
-// through six shared-memory stages laid out like the GEMM's (so the tensor pipe reads fresh operands
-// every stage) and the scale atoms copied into TMEM two stages ahead.  The operands are fixed
-// pseudo-random finite codes; the result is discarded.
+// Measured peaks of the block-scaled tensor-core MMAs the grouped GEMMs use -- tcgen05.mma
+// kind::mxf8f6f4.block_scale.scale_vec::1X (E4M3 x E2M1, M = 128, N = 256, K = 32) and, for the
+// MXFP4-activation variant, kind::mxf4.block_scale.scale_vec::2X (E2M1 x E2M1, K = 64): the
+// denominators of the tensor-bound roofline.  One CTA per SM issues MMAs back to back with its
+// operands rotating through six shared-memory stages laid out like the GEMM's (so the tensor pipe
+// reads fresh operands every stage) and the scale atoms copied into TMEM two stages ahead.  The
+// operands are fixed pseudo-random finite codes; the result is discarded.
 #include <algorithm>
 #include <vector>
 
@@ -14,18 +15,31 @@ namespace moe {
 
 namespace {
 
-constexpr int kPS = 6;                 // stages
-constexpr int kPASlot = 4096;          // activation slot (the MMA's 128 rows read on into the next slots)
-constexpr int kPBSlot = 256 * 128;     // weight slot: 256 rows x 128 padded FP4
-constexpr int kPSfSlot = 3 * 512;      // scale atoms
-constexpr int kPAOff = 0, kPBOff = kPS * kPASlot, kPSfOff = kPBOff + kPS * kPBSlot;
-constexpr int kPUsed = kPSfOff + kPS * kPSfSlot;
-constexpr int kPSmem = kPUsed + 1024;
-static_assert(kPAOff + (kPS - 1) * kPASlot + 128 * 128 <= kPBOff + kPS * kPBSlot, "activation reads stay in smem");
-static_assert(kPSmem <= 232448 - 64, "shared memory budget");
+constexpr int kPS = 6;  // stages
 
+// FP4 = false: E4M3 rows of 128 bytes and byte-expanded E2M1 weights (128-byte swizzle);
+// FP4 = true: packed E2M1 rows of 64 bytes for both operands (64-byte swizzle).
+template <bool FP4>
+struct PeakCfg {
+  static constexpr int kRowBytes = FP4 ? 64 : 128;
+  static constexpr int kASlot = 4096;  // activation slot (the MMA's 128 rows read on into the next slots)
+  static constexpr int kBSlot = 256 * kRowBytes;
+  static constexpr int kSfSlot = 3 * 512;  // scale atoms
+  static constexpr int kAOff = 0, kBOff = kPS * kASlot, kSfOff = kBOff + kPS * kBSlot;
+  static constexpr int kUsed = kSfOff + kPS * kSfSlot;
+  static constexpr int kSmem = kUsed + 1024;
+  static_assert(kAOff + (kPS - 1) * kASlot + 128 * kRowBytes <= kBOff + kPS * kBSlot, "activation reads stay in smem");
+  static_assert(kSmem <= 232448 - 64, "shared memory budget");
+  // per stage: four K = 32 MMAs, or two K = 64 MMAs; either way K = 128
+  static constexpr double kFlopsPerStage = 2.0 * 128 * 256 * 128;
+};
+
+template <bool FP4>
 __global__ void __launch_bounds__(128, 1) mma_peak_kernel(int n_stages, uint64_t budget_ns,
                                                           unsigned long long* ns_out, int* status) {
+  using P = PeakCfg<FP4>;
+  constexpr int kPAOff = P::kAOff, kPBOff = P::kBOff, kPSfOff = P::kSfOff, kPUsed = P::kUsed;
+  constexpr int kPASlot = P::kASlot, kPBSlot = P::kBSlot, kPSfSlot = P::kSfSlot;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ uint64_t done, sink;
@@ -35,7 +49,7 @@ __global__ void __launch_bounds__(128, 1) mma_peak_kernel(int n_stages, uint64_t
     h ^= h >> 15;
     h *= 2246822519u;
     h ^= h >> 13;
-    // operand bytes: positive E4M3 codes below 0x78 (finite), any E2M1 nibble pair without sign;
+    // operand bytes: positive E4M3 codes below 0x78 (finite), or E2M1 nibble pairs without sign;
     // scale bytes 126..129
     reinterpret_cast<uint32_t*>(smem)[i] = i >= kPSfOff / 4 ? 0x7E7F8081u : (h & 0x77777777u);
   }
@@ -52,9 +66,10 @@ __global__ void __launch_bounds__(128, 1) mma_peak_kernel(int n_stages, uint64_t
   tc_fence_after();
   const uint32_t tbase = tmem_slot;
   if (threadIdx.x == 0) {
-    constexpr uint32_t kIdesc0 = mma_idesc(0, 5, 128, 256, 0, 0);
-    const uint64_t a0 = smem_desc(smem_addr(smem + kPAOff), 16, 1024, 2);
-    const uint64_t b0 = smem_desc(smem_addr(smem + kPBOff), 16, 1024, 2);
+    constexpr uint32_t kIdesc0 = FP4 ? mma_idesc(kMxf4E2M1, kMxf4E2M1, 128, 256, 0, 0) : mma_idesc(0, 5, 128, 256, 0, 0);
+    constexpr uint32_t kSwz = FP4 ? 4 : 2, kSbo = 8 * P::kRowBytes;
+    const uint64_t a0 = smem_desc(smem_addr(smem + kPAOff), 16, kSbo, kSwz);
+    const uint64_t b0 = smem_desc(smem_addr(smem + kPBOff), 16, kSbo, kSwz);
     const uint64_t sf0 = smem_desc(smem_addr(smem + kPSfOff), 128, 128, 0);
     const uint32_t sft = tbase + 256;
     auto copy_sf = [&](int s) {
@@ -69,9 +84,12 @@ __global__ void __launch_bounds__(128, 1) mma_peak_kernel(int n_stages, uint64_t
     const uint64_t t0 = globaltimer_ns();
     for (int g = 0; g < n_stages; ++g) {
       const int s = g % kPS;
-      (void)tc_stage4_mx_commit_poll(tbase, a0 + (uint64_t)((s * kPASlot) >> 4), b0 + (uint64_t)((s * kPBSlot) >> 4),
-                                     kIdesc0, sft + (uint32_t)(s * 12), sft + (uint32_t)(s * 12 + 4), g ? 1u : 0u,
-                                     &sink, &done, 1u);
+      const uint64_t ad = a0 + (uint64_t)((s * kPASlot) >> 4), bd = b0 + (uint64_t)((s * kPBSlot) >> 4);
+      const uint32_t sfa = sft + (uint32_t)(s * 12);
+      if (FP4)
+        (void)tc_stage2_mxf4_commit_poll(tbase, ad, bd, kIdesc0, sfa, sfa + 4, g ? 1u : 0u, &sink, &done, 1u);
+      else
+        (void)tc_stage4_mx_commit_poll(tbase, ad, bd, kIdesc0, sfa, sfa + 4, g ? 1u : 0u, &sink, &done, 1u);
       if (g + 2 < n_stages) copy_sf((g + 2) % kPS);
     }
     tc_commit(&done);
@@ -84,12 +102,10 @@ __global__ void __launch_bounds__(128, 1) mma_peak_kernel(int n_stages, uint64_t
   if (threadIdx.x < 32) tmem_dealloc(tbase, 512);
 }
 
-}  // namespace
-
-}  // namespace moe
-
-extern "C" MOE_API moe_status_t moe_measure_mxf8f6f4_peak(int32_t n_stages, double* tflops) {
-  using namespace moe;
+template <bool FP4>
+moe_status_t measure_peak(int32_t n_stages, double* tflops) {
+  using P = PeakCfg<FP4>;
+  constexpr int kPSmem = P::kSmem;
   if (n_stages < 8 || n_stages > (1 << 18) || !tflops) {
     set_last_error("n_stages must be in [8, 262144] and tflops non-NULL");
     return MOE_ERR_INVALID_ARG;
@@ -105,7 +121,7 @@ extern "C" MOE_API moe_status_t moe_measure_mxf8f6f4_peak(int32_t n_stages, doub
     if (d_ns) cudaFree(d_ns);
     if (d_status) cudaFree(d_status);
   };
-  if (cudaFuncSetAttribute(mma_peak_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPSmem) != cudaSuccess ||
+  if (cudaFuncSetAttribute(mma_peak_kernel<FP4>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPSmem) != cudaSuccess ||
       cudaMalloc(&d_ns, sizeof(unsigned long long) * sms) != cudaSuccess ||
       cudaMalloc(&d_status, sizeof(int)) != cudaSuccess || cudaMemset(d_status, 0, sizeof(int)) != cudaSuccess) {
     cleanup();
@@ -113,8 +129,8 @@ extern "C" MOE_API moe_status_t moe_measure_mxf8f6f4_peak(int32_t n_stages, doub
     return MOE_ERR_CUDA;
   }
   // warm-up launch, then the timed one (per-CTA globaltimer spans; the slowest CTA counts)
-  mma_peak_kernel<<<sms, 128, kPSmem>>>(16, 2000000000ull, d_ns, d_status);
-  mma_peak_kernel<<<sms, 128, kPSmem>>>(n_stages, 2000000000ull, d_ns, d_status);
+  mma_peak_kernel<FP4><<<sms, 128, kPSmem>>>(16, 2000000000ull, d_ns, d_status);
+  mma_peak_kernel<FP4><<<sms, 128, kPSmem>>>(n_stages, 2000000000ull, d_ns, d_status);
   std::vector<unsigned long long> ns(sms);
   int status = 0;
   if (cudaDeviceSynchronize() != cudaSuccess ||
@@ -130,7 +146,18 @@ extern "C" MOE_API moe_status_t moe_measure_mxf8f6f4_peak(int32_t n_stages, doub
     return MOE_ERR_TIMEOUT;
   }
   const double t = (double)*std::max_element(ns.begin(), ns.end()) * 1e-9;
-  const double flops = 2.0 * 128 * 256 * 32 * 4 * (double)n_stages * sms;
+  const double flops = P::kFlopsPerStage * (double)n_stages * sms;
   *tflops = t > 0 ? flops / t / 1e12 : 0.0;
   return MOE_OK;
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" MOE_API moe_status_t moe_measure_mxf8f6f4_peak(int32_t n_stages, double* tflops) {
+  return moe::measure_peak<false>(n_stages, tflops);
+}
+
+extern "C" MOE_API moe_status_t moe_measure_mxf4_peak(int32_t n_stages, double* tflops) {
+  return moe::measure_peak<true>(n_stages, tflops);
 }

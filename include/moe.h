@@ -103,6 +103,23 @@ MOE_API moe_status_t moe_experts_create(const moe_config_t* cfg, int32_t n, cons
  */
 MOE_API moe_status_t moe_experts_set_hash_table(moe_experts_t experts, const int32_t* table, int32_t V);
 
+/*
+ * Activation format of an expert set (default MOE_ACT_MXFP8).  MOE_ACT_MXFP8: x and the SwiGLU output
+ * h are quantised to MXFP8 (E4M3 codes, one E8M0 scale per 32 along the reduction dimension) and the
+ * grouped GEMMs run tcgen05 kind::mxf8f6f4 (E4M3 x E2M1).  MOE_ACT_MXFP4: x and h are quantised to
+ * MXFP4 with the weights' own rule (E2M1 codes packed two per byte, element 2i in the low nibble of
+ * byte i; scale exponent floor(log2(amax)) - 2; round to nearest even, saturating at +-6) and the
+ * GEMMs run kind::mxf4 (E2M1 x E2M1): twice the tensor-core rate at a coarser activation precision.
+ * This is the MXFP4-activation prefill variant; the pages quantise only the weights to MXFP4 (model
+ * card "Preprocessing"; TensorSharp page "Getting a drafter").  It changes the layouts of moe_permute's
+ * a_q output and moe_expert_ffn's a_q input to [rows, d_model/2] packed codes.  In moe_forward the
+ * routed set and the shared expert must use the same format.  Takes effect on later calls.
+ * Errors: MOE_ERR_INVALID_ARG (NULL handle, unknown format).
+ */
+#define MOE_ACT_MXFP8 0
+#define MOE_ACT_MXFP4 1
+MOE_API moe_status_t moe_experts_set_activation_format(moe_experts_t experts, int32_t format);
+
 /* Bytes of workspace a routed set needs for batches of up to max_T rows (with a shared expert). */
 MOE_API size_t moe_workspace_size(const moe_config_t* cfg, int32_t max_T);
 
@@ -129,7 +146,8 @@ MOE_API moe_status_t moe_route(moe_experts_t experts, const moe_input_t* x, cons
  *   a_q [R, d_model] E4M3 codes of x[perm_tok[r]] (round-to-nearest-even, saturating at +-448),
  *   a_s [R, d_model/32] E8M0 bytes, exponent floor(log2(amax of the 32-block)) - 8 (0 for a zero block).
  * a_q / a_s may be NULL (not written).  Uses the workspace.  Ids outside [0, E) are reported by
- * moe_check and treated as expert 0.
+ * moe_check and treated as expert 0.  With MOE_ACT_MXFP4 set on the handle a_q is [R, d_model/2]
+ * packed E2M1 codes and the a_s exponent is floor(log2(amax)) - 2.
  */
 MOE_API moe_status_t moe_permute(moe_experts_t experts, const moe_input_t* x, const int32_t* topk_ids, int32_t* counts,
                          int32_t* offsets, int32_t* perm_tok, int32_t* inv_pos, uint8_t* a_q, uint8_t* a_s,
@@ -141,7 +159,9 @@ MOE_API moe_status_t moe_permute(moe_experts_t experts, const moe_input_t* x, co
  * (offsets int32 [n+1] of the handle's n experts, offsets[0] = 0, offsets[n] = n_rows; NULL = every
  * row uses expert 0).  y[r] = row_w[r] * W2_g . q8(silu(min(W1_g a_r, L)) * clamp(W3_g a_r, -L, L)),
  * with q8 the MXFP8 quantisation along d_ff; row_w fp32 [n_rows] or NULL (= 1); y bf16
- * [n_rows, d_model].  Uses the workspace of the handle (n_rows <= max_T * (top_k + 1)).
+ * [n_rows, d_model].  Uses the workspace of the handle (n_rows <= max_T * (top_k + 1)).  With
+ * MOE_ACT_MXFP4 set on the handle a_q is [n_rows, d_model/2] packed E2M1 codes and h is quantised to
+ * MXFP4 instead (q8 becomes q4).
  */
 MOE_API moe_status_t moe_expert_ffn(moe_experts_t experts, int32_t n_rows, const int32_t* offsets, const uint8_t* a_q,
                             const uint8_t* a_s, const float* row_w, void* y_bf16, moe_stream_t stream);

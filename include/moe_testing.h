@@ -24,6 +24,19 @@ extern "C" {
 MOE_API moe_status_t moe_testing_stall_loads(moe_experts_t experts, int32_t enable);
 
 /*
+ * Reads back the SwiGLU output h of the last moe_forward / moe_expert_ffn on this handle, as the
+ * down projection consumed it: *n_rows receives its row count (the call's routed rows in permuted
+ * order, then one shared row per token in token order; 0 if there was none), h_q [n_rows, d_ff]
+ * E4M3 codes (or [n_rows, d_ff/2] packed E2M1 codes with MOE_ACT_MXFP4) and h_s [n_rows, d_ff/32]
+ * E8M0 bytes, both device buffers (h_s 4-byte aligned) that the caller sizes for n_rows; pass NULL
+ * for both to learn n_rows only.  Asynchronous on `stream`; valid until the next call on the handle.
+ * Tests use it to compare the kernels' h codes with the oracle's and to check the down projection on
+ * the kernels' own h.  Errors: MOE_ERR_INVALID_ARG, MOE_ERR_WORKSPACE, MOE_ERR_CUDA.
+ */
+MOE_API moe_status_t moe_testing_read_h(moe_experts_t experts, uint8_t* h_q, uint8_t* h_s, int32_t* n_rows,
+                                        moe_stream_t stream);
+
+/*
  * Measures the throughput of the block-scaled MMA the grouped GEMMs are built on (tcgen05.mma
  * kind::mxf8f6f4.block_scale.scale_vec::1X, E4M3 activations x E2M1 weights with E8M0 scales,
  * M = 128, N = 256, K = 32) on the current device: one CTA per SM issues n_stages x 4 MMAs back to
@@ -35,6 +48,14 @@ MOE_API moe_status_t moe_testing_stall_loads(moe_experts_t experts, int32_t enab
  * Returns MOE_ERR_INVALID_ARG, MOE_ERR_CUDA, or MOE_ERR_TIMEOUT if the kernel's bounded wait ran out.
  */
 MOE_API moe_status_t moe_measure_mxf8f6f4_peak(int32_t n_stages, double* tflops);
+
+/*
+ * The same measurement for the MMA of the MXFP4-activation variant (moe_experts_set_activation_format
+ * with MOE_ACT_MXFP4): tcgen05.mma kind::mxf4.block_scale.scale_vec::2X, E2M1 x E2M1 with E8M0
+ * scales, M = 128, N = 256, K = 64; n_stages x 2 MMAs per SM, operands packed in 64-byte rows.
+ * Arguments, result and errors as moe_measure_mxf8f6f4_peak.
+ */
+MOE_API moe_status_t moe_measure_mxf4_peak(int32_t n_stages, double* tflops);
 
 #ifdef __cplusplus
 }

@@ -292,6 +292,15 @@ def expert_ffn(aq, as_, weights: "synth.ExpertWeights", offsets=None, row_w=None
     return y, hq, hs
 
 
+def down_from_h(hq, hs, w2, s2, act: str = "mxfp8") -> np.ndarray:
+    """The down projection of given h rows through one expert: dequantise h (codes [n, f] or packed
+    [n, f/2], scales [n, f/32]) and the expert's W2 (codes [d, f/2], scales [d, f/32]) exactly, then
+    one fp64 matmul.  Returns [n, d].  For checking a device path on its own h codes."""
+    hd = act_dequantize(_c(hq, np.uint8), _c(hs, np.uint8), act)
+    w = mxfp4_dequantize(_c(w2, np.uint8), _c(s2, np.uint8))
+    return hd @ w.T
+
+
 def layer(x_bf16, ids, wts, experts: "synth.ExpertWeights", shared: "synth.ExpertWeights | None",
           limit: float = 10.0, tokens=None, mode: int = 1, act: str = "mxfp8"):
     """y fp64 [n_sel, d] for the listed tokens (None: all), given the routing (ids, wts).

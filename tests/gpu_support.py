@@ -40,14 +40,15 @@ def x_to_device(x_bits: np.ndarray) -> torch.Tensor:
 
 
 @functools.lru_cache(maxsize=1)
-def case(name: str, T: int | None = None, seed: int = 0):
-    """(workload, inputs, oracle ids, oracle weights, device layer) for a named workload."""
+def case(name: str, T: int | None = None, seed: int = 0, act: str = "mxfp8"):
+    """(workload, inputs, oracle ids, oracle weights, device layer) for a named workload; act is the
+    layer's activation format ("mxfp4": the MXFP4-activation variant)."""
     from block_scaled_fp4_sqrt_gb300 import MoELayer
     wl = WORKLOADS[name]
     if T is not None:
         wl = wl.with_T(T)
     inp, ids, wts, _ = oracle.margin_filtered_layer(wl, seed)
-    layer = MoELayer.from_host(inp, device=device(), max_T=max(wl.T, 1))
+    layer = MoELayer.from_host(inp, device=device(), max_T=max(wl.T, 1), act=act)
     return wl, inp, ids, wts, layer
 
 
@@ -58,9 +59,18 @@ def compare_outputs(y: np.ndarray, y_ref: np.ndarray):
     return max_err, rms, mean_rel
 
 
+# The outputs compared here are bf16: each element carries one rounding to bf16 (8 significant bits,
+# at most 2^-8 of its magnitude) on top of the arithmetic the tolerance above bounds.  A layer output
+# of 2M elements reaches 7 rms in its tail, where that rounding alone is 2.7e-2 rms; so the
+# element-wise bound is TOL_MAX_RMS * rms + 2^-8 |y_ref|.
+BF16_HALF_ULP_REL = 2.0 ** -8
+
+
 def assert_close(y: np.ndarray, y_ref: np.ndarray, what: str = "output"):
     max_err, rms, mean_rel = compare_outputs(y, y_ref)
-    assert max_err <= TOL_MAX_RMS * rms, f"{what}: max |dy| {max_err:.4e} > {TOL_MAX_RMS} rms ({rms:.4e})"
+    excess = np.abs(y - y_ref) - (TOL_MAX_RMS * rms + BF16_HALF_ULP_REL * np.abs(y_ref)) if y.size else np.zeros(1)
+    assert np.all(excess <= 0), (f"{what}: max |dy| {max_err:.4e} exceeds {TOL_MAX_RMS} rms ({rms:.4e}) plus the bf16 "
+                                 f"rounding of y_ref by {float(excess.max()):.4e}")
     assert mean_rel <= TOL_MEAN_REL, f"{what}: mean relative error {mean_rel:.4e} > {TOL_MEAN_REL}"
     return max_err / max(rms, 1e-300), mean_rel
 

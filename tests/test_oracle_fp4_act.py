@@ -130,6 +130,17 @@ def test_down_projection_and_h_codes():
         assert np.allclose(y[rows], want, rtol=1e-12, atol=1e-12 * np.abs(want).max())
 
 
+def test_down_from_h_equals_the_ffn_down_projection():
+    """oracle.down_from_h on the oracle's own h reproduces expert_ffn's y (both formats)."""
+    wl, inp = _tiny()
+    ex = synth.ExpertWeights(*(getattr(inp.experts, n)[:1] for n in ("w13", "s13", "w2", "s2")))
+    for act in ("mxfp8", "mxfp4"):
+        q, s = oracle.quantize_x(inp.x, act=act)
+        y, hq, hs = oracle.expert_ffn(q, s, ex, act=act)
+        y2 = oracle.down_from_h(hq, hs, ex.w2[0], ex.s2[0], act=act)
+        assert np.allclose(y2, y, rtol=1e-12, atol=1e-12 * np.abs(y).max())
+
+
 def test_dense_equals_permuted_bitwise_mxfp4():
     wl, inp = _tiny()
     ids, wts, _ = oracle.route_inputs(inp)
