@@ -274,10 +274,10 @@ def run_reference(args, wl):
 
 
 def layer_launches(wl) -> int:
-    """Kernels one layer forward launches.  Route: the hash-table kernel, or the router weight split then
-    the fused cluster router (up to 256 experts; above that tensor-core logits + a top-k kernel).
+    """Kernels one layer forward launches with the router resident on the handle.  Route: the hash-table
+    kernel, or the fused cluster router (up to 256 experts; above that tensor-core logits + a top-k kernel).
     Dispatch: histogram, column scan, group scan, gather.  The two grouped GEMMs, then the combine."""
-    route = 1 if wl.hashed else (2 if wl.E <= 256 else 3)
+    route = 1 if wl.hashed else (1 if wl.E <= 256 else 2)  # router weights resident: no per-call split
     return route + 4 + 2 + 1
 
 
@@ -307,7 +307,8 @@ def run_ours(args, wl):
     inp = synth.gen_layer(wl, args.seed)
     if world > 1:  # each replica gets its own batch of token rows
         inp.x = replica_x(args.seed, rank, world, wl.T, wl.d)
-    layer = moe.MoELayer.from_host(inp, device=dev, max_T=wl.T, act=args.act)
+    # the router weights are made resident once, like the expert weights (moe_experts_set_router)
+    layer = moe.MoELayer.from_host(inp, device=dev, max_T=wl.T, act=args.act, resident_router=True)
     x = torch.from_numpy(inp.x.view(np.int16)).to(dev).view(torch.bfloat16)
     out = torch.empty((wl.T, wl.d), dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -403,6 +404,7 @@ def run_ours(args, wl):
     pk = peaks()
     dom = max(stage_ms, key=stage_ms.get)
     sb = stage_bytes(wl, touched, rows, args.act)
+    traffic_key = wl.name + (":mxfp4" if fp4 else "")  # rows of profiles/dram_traffic.txt
     fl = gemm_flops(wl, rows)
     # verify shapes stream the expert weights (HBM bound); with >= 64 rows per expert (the prefill
     # chunk) the grouped GEMMs are dense block-scaled contractions (tensor bound)
@@ -410,7 +412,7 @@ def run_ours(args, wl):
     if compute_bound:
         achieved = fl[dom] / (stage_ms[dom] * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": mx_peak, "unit": "TFLOP/s", "frac": achieved / mx_peak,
-                "traffic": None if fp4 else measured_traffic(dom, wl.name), "kernel": dom,
+                "traffic": measured_traffic(dom, traffic_key), "kernel": dom,
                 "peak_source": "measured in this run: back-to-back " + mma_name,
                 "nominal_alt_peak": {"value": (6 if fp4 else 2) * pk["bf16_tflops_sustained"],
                                      "source": f"{pk['source']} bf16 sustained x {6 if fp4 else 2} (nominal "
@@ -419,8 +421,7 @@ def run_ours(args, wl):
     else:
         achieved = sb[dom] / (stage_ms[dom] * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved / pk["hbm_gbs"], "traffic": None if fp4 else measured_traffic(dom, wl.name),
-                "kernel": dom,
+                "frac": achieved / pk["hbm_gbs"], "traffic": measured_traffic(dom, traffic_key), "kernel": dom,
                 "peak_source": f"{pk['source']} HBM copy bandwidth", "algorithmic_bytes_per_launch": sb[dom]}
     lb = layer_bytes(wl, touched)
     kernels_per_step = layer_launches(wl)
@@ -493,7 +494,7 @@ def run_stack(args, wl):
             rw, rb, _ = synth.gen_router(args.seed + l, wl.E, wl.d, wl.n_hot, wl.hot_bias)
             layers.append(moe.MoELayer(wl.d, wl.f, wl.E, wl.k, dex, dsh, torch.from_numpy(rw).to(dev),
                                        torch.from_numpy(rb).to(dev), None, wl.T, wl.route_scale, wl.swiglu_limit, dev,
-                                       args.act))
+                                       args.act, resident_router=True))
         layers[-1].workspace = None  # the stacks below give every layer one shared workspace
     del dex, dsh
     torch.cuda.empty_cache()

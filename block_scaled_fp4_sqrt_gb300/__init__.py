@@ -27,7 +27,8 @@ EXPORTED = ("moe_experts_create", "moe_experts_set_hash_table", "moe_workspace_s
             "moe_set_wait_budget", "moe_experts_destroy", "moe_status_string", "moe_last_error",
             "moe_testing_stall_loads", "moe_set_stage_events", "moe_route_noalloc", "moe_measure_mxf8f6f4_peak",
             "moe_stack_create", "moe_stack_forward", "moe_stack_destroy", "moe_mx_blocks_unpack",
-            "moe_experts_set_activation_format", "moe_measure_mxf4_peak", "moe_testing_read_h")
+            "moe_experts_set_activation_format", "moe_measure_mxf4_peak", "moe_testing_read_h",
+            "moe_experts_set_router")
 
 MOE_MX_NIBBLES_PAIRED, MOE_MX_NIBBLES_SPLIT = 0, 1
 MOE_ACT_MXFP8, MOE_ACT_MXFP4 = 0, 1
@@ -85,6 +86,7 @@ def lib() -> ctypes.CDLL:
         L.moe_measure_mxf4_peak.argtypes = [i32, ctypes.POINTER(ctypes.c_double)]
         L.moe_experts_set_activation_format.argtypes = [vp, i32]
         L.moe_testing_read_h.argtypes = [vp, vp, vp, ctypes.POINTER(i32), vp]
+        L.moe_experts_set_router.argtypes = [vp, vp, vp, vp]
         L.moe_stack_create.argtypes = [ctypes.POINTER(moe_stack_layer_t), i32, i32, ctypes.POINTER(vp)]
         L.moe_stack_forward.argtypes = [vp, inp, vp, vp, vp]
         L.moe_stack_destroy.argtypes = [vp]
@@ -141,6 +143,10 @@ def moe_experts_create(cfg: moe_config_t, n: int, w13: torch.Tensor, s13: torch.
 def moe_experts_set_hash_table(h, table: torch.Tensor | None) -> None:
     _ok("moe_experts_set_hash_table",
         lib().moe_experts_set_hash_table(h, _p(table), 0 if table is None else int(table.shape[0])))
+
+
+def moe_experts_set_router(h, router_w: torch.Tensor | None, router_bias: torch.Tensor | None, stream=None) -> None:
+    _ok("moe_experts_set_router", lib().moe_experts_set_router(h, _p(router_w), _p(router_bias), _stream(stream)))
 
 
 def moe_workspace_size(cfg: moe_config_t, max_T: int) -> int:
@@ -308,9 +314,10 @@ class MoELayer:
     def __init__(self, d_model, d_ff, n_experts, top_k, experts: DeviceExperts, shared: DeviceExperts | None,
                  router_w: torch.Tensor | None, router_bias: torch.Tensor | None,
                  hash_table: torch.Tensor | None = None, max_T: int = 512, route_scale: float = 1.5,
-                 swiglu_limit: float = 10.0, device=None, act: str = "mxfp8"):
+                 swiglu_limit: float = 10.0, device=None, act: str = "mxfp8", resident_router: bool = False):
         self.device = torch.device(device or "cuda")
         self.act = act
+        self.resident_router = resident_router and router_w is not None
         self.cfg = make_config(d_model, d_ff, n_experts, top_k, route_scale, swiglu_limit)
         self.d, self.f, self.E, self.k, self.max_T = d_model, d_ff, n_experts, top_k, max_T
         self.experts, self.shared_w = experts, shared
@@ -327,6 +334,8 @@ class MoELayer:
                 moe_experts_set_hash_table(self.h, hash_table)
             for h in self._handles:
                 moe_experts_set_activation_format(h, act)
+            if self.resident_router:  # split once here; forward passes no router weights
+                moe_experts_set_router(self.h, router_w, router_bias)
             nbytes = moe_workspace_size(self.cfg, max_T)
             self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=self.device)
             moe_set_workspace(self.h, self.workspace, max_T)
@@ -334,7 +343,7 @@ class MoELayer:
 
     @classmethod
     def from_host(cls, inp, device=None, max_T: int | None = None, with_shared: bool = True,
-                  act: str = "mxfp8") -> "MoELayer":
+                  act: str = "mxfp8", resident_router: bool = False) -> "MoELayer":
         """Build from host arrays (an object with the fields of ``synth.LayerInputs``); act is the
         activation format ("mxfp8", or "mxfp4" for the MXFP4-activation variant)."""
         dev = torch.device(device or "cuda")
@@ -347,7 +356,7 @@ class MoELayer:
         rb = None if inp.router_bias is None else _to_dev(inp.router_bias, dev)
         tab = None if inp.hash_table is None else _to_dev(inp.hash_table, dev)
         layer = cls(wl.d, wl.f, wl.E, wl.k, ex, sh, rw, rb, tab, max_T or wl.T, wl.route_scale, wl.swiglu_limit, dev,
-                    act)
+                    act, resident_router)
         layer.token_ids = None if inp.token_ids is None else _to_dev(inp.token_ids, dev)
         return layer
 
@@ -357,7 +366,8 @@ class MoELayer:
             token_ids = self.token_ids
         if out is None:
             out = torch.empty((x.shape[0], self.d), dtype=torch.bfloat16, device=self.device)
-        moe_forward(x, self.router_w, self.router_bias, self.h, self.h_shared, out, token_ids, stream)
+        rw, rb = (None, None) if self.resident_router else (self.router_w, self.router_bias)
+        moe_forward(x, rw, rb, self.h, self.h_shared, out, token_ids, stream)
         return out
 
     def route(self, x: torch.Tensor, token_ids: torch.Tensor | None = None):
@@ -366,7 +376,8 @@ class MoELayer:
         T = x.shape[0]
         ids = torch.empty((T, self.k), dtype=torch.int32, device=self.device)
         w = torch.empty((T, self.k), dtype=torch.float32, device=self.device)
-        moe_route(self.h, x, self.router_w, self.router_bias, ids, w, token_ids)
+        rw, rb = (None, None) if self.resident_router else (self.router_w, self.router_bias)
+        moe_route(self.h, x, rw, rb, ids, w, token_ids)
         return ids, w
 
     def permute(self, x: torch.Tensor, ids: torch.Tensor):
@@ -446,7 +457,9 @@ class MoEStack:
             for i, ly in enumerate(self.layers):
                 moe_set_workspace(ly.h, self.workspaces[i % n_ws], max_T)
             self.scratch = torch.empty((max_T, self.d), dtype=torch.bfloat16, device=self.device)
-            self.stack = moe_stack_create([(ly.h, ly.h_shared, ly.router_w, ly.router_bias) for ly in self.layers],
+            self.stack = moe_stack_create([(ly.h, ly.h_shared, *((None, None) if ly.resident_router else
+                                                                 (ly.router_w, ly.router_bias)))
+                                           for ly in self.layers],
                                           use_graph)
 
     def forward(self, x: torch.Tensor, token_ids: torch.Tensor | None = None, out: torch.Tensor | None = None,

@@ -27,6 +27,9 @@ struct moe_experts_s {
   CUtensorMap tm13p;  // ... and for kind::mxf4 (packed 64-byte rows, 64-byte swizzle)
   CUtensorMap tm2p;
   int act_fp4 = 0;    // activation format: 0 = MXFP8, 1 = MXFP4 (moe_experts_set_activation_format)
+  __nv_bfloat16* router_split = nullptr;  // owned: resident router weight planes (moe_experts_set_router)
+  float* router_bias = nullptr;           // owned: its bias [E]
+  CUtensorMap tm_router;                  // map over router_split
   const int32_t* hash_table = nullptr;
   int32_t hash_V = 0;
   void* ws_base = nullptr;
@@ -299,7 +302,43 @@ void moe_experts_destroy(moe_experts_t h) {
   if (h->sf13) cudaFree(h->sf13);
   if (h->sf2) cudaFree(h->sf2);
   if (h->status) cudaFree(h->status);
+  if (h->router_split) cudaFree(h->router_split);
+  if (h->router_bias) cudaFree(h->router_bias);
   delete h;
+}
+
+moe_status_t moe_experts_set_router(moe_experts_t h, const float* router_w, const float* router_bias,
+                                    moe_stream_t stream) {
+  if (!h) return fail(MOE_ERR_INVALID_ARG, "handle is NULL");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (!router_w && !router_bias) {  // drop the resident router
+    MOE_CUDA(cudaStreamSynchronize(s), "stream synchronize");
+    if (h->router_split) cudaFree(h->router_split);
+    if (h->router_bias) cudaFree(h->router_bias);
+    h->router_split = nullptr;
+    h->router_bias = nullptr;
+    return MOE_OK;
+  }
+  if (!router_w || !router_bias) return fail(MOE_ERR_INVALID_ARG, "router_w and router_bias go together");
+  const int E = h->cfg.n_experts, d = h->cfg.d_model;
+  if (E > 512) return fail(MOE_ERR_UNSUPPORTED, "the learned router supports up to 512 experts");
+  if (!aligned(router_w, 16)) return fail(MOE_ERR_INVALID_ARG, "router_w must be 16-byte aligned");
+  const int Epad = router_tc_epad(E);
+  if (!h->router_split) {
+    MOE_CUDA(cudaMalloc(&h->router_split, (size_t)3 * Epad * d * sizeof(__nv_bfloat16)), "router planes");
+    const cudaError_t e = cudaMalloc(&h->router_bias, (size_t)E * sizeof(float));
+    if (e != cudaSuccess) {
+      cudaFree(h->router_split);
+      h->router_split = nullptr;
+      return cuda_fail(e, "router bias");
+    }
+    const moe_status_t st = make_map_bf16(&h->tm_router, h->router_split, 64, (uint64_t)3 * Epad * (d / 64), 256);
+    if (st != MOE_OK) return st;
+  }
+  MOE_CUDA(launch_split_router(router_w, E, d, h->router_split, s), "router weight split");
+  MOE_CUDA(cudaMemcpyAsync(h->router_bias, router_bias, (size_t)E * sizeof(float), cudaMemcpyDeviceToDevice, s),
+           "router bias copy");
+  return MOE_OK;
 }
 
 moe_status_t moe_experts_set_hash_table(moe_experts_t h, const int32_t* table, int32_t V) {
@@ -360,18 +399,27 @@ static moe_status_t route_into(moe_experts_s* h, const moe_input_t* x, const flo
              "hash route");
     return MOE_OK;
   }
-  if (!router_w || !router_bias) return fail(MOE_ERR_INVALID_ARG, "router_w / router_bias is NULL");
+  // router_w = router_bias = NULL: the handle's resident router (moe_experts_set_router), split once
+  const bool resident = !router_w && !router_bias && h->router_split;
+  if (!resident && (!router_w || !router_bias))
+    return fail(MOE_ERR_INVALID_ARG, "router_w / router_bias is NULL and the handle has no resident router");
   if (x->token_ids) return fail(MOE_ERR_INVALID_ARG, "token_ids given but no hash table is set");
   if (E > 512) return fail(MOE_ERR_UNSUPPORTED, "the learned router supports up to 512 experts");
-  if (!aligned(router_w, 16)) return fail(MOE_ERR_INVALID_ARG, "router_w must be 16-byte aligned");
+  if (!resident && !aligned(router_w, 16)) return fail(MOE_ERR_INVALID_ARG, "router_w must be 16-byte aligned");
   if (T == 0) return MOE_OK;
   CUtensorMap tm_x, tm_w;
   const int Epad = router_tc_epad(E);
   moe_status_t st = make_map_bf16(&tm_x, x->x_bf16, (uint64_t)d, (uint64_t)T, 128);
-  // the split planes are tile-contiguous [256 x 64] blocks: viewed as a [3 * Epad * d / 64, 64] matrix
-  if (st == MOE_OK) st = make_map_bf16(&tm_w, h->ws.w_split, 64, (uint64_t)3 * Epad * (d / 64), 256);
   if (st != MOE_OK) return st;
-  MOE_CUDA(launch_split_router(router_w, E, d, h->ws.w_split, s), "router weight split");
+  if (resident) {
+    tm_w = h->tm_router;
+    router_bias = h->router_bias;
+  } else {
+    // the split planes are tile-contiguous [256 x 64] blocks: viewed as a [3 * Epad * d / 64, 64] matrix
+    st = make_map_bf16(&tm_w, h->ws.w_split, 64, (uint64_t)3 * Epad * (d / 64), 256);
+    if (st != MOE_OK) return st;
+    MOE_CUDA(launch_split_router(router_w, E, d, h->ws.w_split, s), "router weight split");
+  }
   if (E <= 256) {  // logits, split-K reduction and top-k in one cluster kernel
     MOE_CUDA(launch_router_fused(tm_x, tm_w, router_bias, T, E, d, k, h->cfg.route_scale, router_fused_split(T, d), ids,
                                  wts, h->status, h->budget_ns, s),
@@ -569,6 +617,8 @@ moe_status_t forward_impl(const moe_input_t* x, const float* router_w, const flo
 int experts_d_model(moe_experts_t h) { return h ? h->cfg.d_model : 0; }
 
 int experts_has_hash_table(moe_experts_t h) { return h && h->hash_table ? 1 : 0; }
+
+int experts_has_resident_router(moe_experts_t h) { return h && h->router_split ? 1 : 0; }
 
 }  // namespace moe
 

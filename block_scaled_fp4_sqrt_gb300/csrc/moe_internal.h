@@ -76,6 +76,7 @@ moe_status_t forward_impl(const moe_input_t* x, const float* router_w, const flo
                           moe_experts_t sh, void* out_bf16, const void* residual_bf16, moe_stream_t stream);
 int experts_d_model(moe_experts_t h);
 int experts_has_hash_table(moe_experts_t h);
+int experts_has_resident_router(moe_experts_t h);
 
 // Launch with programmatic stream serialization: the kernel may be scheduled before the previous kernel
 // in the stream has finished (it must call pdl_wait() before touching global memory, see moe_device.cuh).

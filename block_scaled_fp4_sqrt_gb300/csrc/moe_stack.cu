@@ -70,8 +70,10 @@ moe_status_t moe_stack_create(const moe_stack_layer_t* layers, int32_t n_layers,
     if (layers[l].shared && moe::experts_d_model(layers[l].shared) != d)
       return stack_fail(MOE_ERR_INVALID_ARG, "a shared expert differs in d_model");
     const bool hashed = moe::experts_has_hash_table(layers[l].experts) != 0;
-    if (hashed != (layers[l].router_w == nullptr))
-      return stack_fail(MOE_ERR_INVALID_ARG, "a layer needs either a hash table or router weights, not both");
+    const bool given = layers[l].router_w != nullptr;
+    if (hashed ? given : !(given || moe::experts_has_resident_router(layers[l].experts)))
+      return stack_fail(MOE_ERR_INVALID_ARG,
+                        "a layer needs either a hash table or router weights (given, or resident), not both");
   }
   moe_stack_s* st = new moe_stack_s();
   st->layers.assign(layers, layers + n_layers);

@@ -120,6 +120,21 @@ MOE_API moe_status_t moe_experts_set_hash_table(moe_experts_t experts, const int
 #define MOE_ACT_MXFP4 1
 MOE_API moe_status_t moe_experts_set_activation_format(moe_experts_t experts, int32_t format);
 
+/*
+ * Make the learned router resident on a routed set: router_w fp32 [E, d_model] (16-byte aligned) and
+ * router_bias fp32 [E], both device buffers, are converted once into the form the router kernels read
+ * (three bf16 planes whose sum is router_w exactly, in the tile order of the tensor-core router), into
+ * memory the handle allocates and owns (6 * E_pad * d_model bytes + 4 * E; E_pad = E rounded up to 256).
+ * The copy is enqueued on `stream`; the inputs may be released once `stream` has passed the call.  Later
+ * moe_route / moe_forward calls (and stack layers) with router_w = router_bias = NULL use it and skip
+ * the per-call conversion; calls that pass router weights still use those.  Calling it again replaces
+ * the contents; router_w = router_bias = NULL frees it (after synchronising `stream`).  A hash table, when
+ * set, takes precedence.  Errors: MOE_ERR_INVALID_ARG (NULL handle, one of the two NULL, misaligned),
+ * MOE_ERR_UNSUPPORTED (E > 512), MOE_ERR_CUDA.
+ */
+MOE_API moe_status_t moe_experts_set_router(moe_experts_t experts, const float* router_w, const float* router_bias,
+                                            moe_stream_t stream);
+
 /* Bytes of workspace a routed set needs for batches of up to max_T rows (with a shared expert). */
 MOE_API size_t moe_workspace_size(const moe_config_t* cfg, int32_t max_T);
 
@@ -131,6 +146,7 @@ MOE_API moe_status_t moe_set_workspace(moe_experts_t experts, void* workspace, s
  * s = sqrt(softplus(l)), the top_k experts by s + router_bias (fp32 [E]; ties to the lower id),
  * weights route_scale * s_j / sum of the selected s (the bias steers selection only).
  * Hash layer (a table is set): router_w and router_bias must be NULL, x->token_ids non-NULL.
+ * Learned layer with router_w = router_bias = NULL: the handle's resident router (moe_experts_set_router).
  * Outputs: topk_ids int32 [T, top_k] ascending per row, topk_w fp32 [T, top_k].
  * Uses the workspace.  Errors: MOE_ERR_INVALID_ARG, MOE_ERR_WORKSPACE, MOE_ERR_CUDA.
  */
@@ -229,7 +245,8 @@ MOE_API moe_status_t moe_route_noalloc(const moe_config_t* cfg, const moe_input_
  * moe_stack_layer_t (one layer)
  *   experts      required; its hash table (moe_experts_set_hash_table) makes the layer hash-routed.
  *   shared       may be NULL.
- *   router_w     required exactly when the layer has no hash table; NULL on hash layers.
+ *   router_w     NULL on hash layers; on the others required unless the handle has a resident router
+ *                (moe_experts_set_router), which NULL selects.
  *   router_bias  likewise.
  * The stack keeps these pointers; the caller owns the handles and buffers and keeps them alive.  Every
  * layer handle needs a workspace (moe_set_workspace).  Layers may share one workspace: they run one after

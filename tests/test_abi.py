@@ -62,6 +62,7 @@ def test_host_side_validation_without_gpu(libmoe):
     assert L.moe_stack_create(None, 0, 0, ctypes.byref(st)) == 1 and not st.value
     assert L.moe_stack_forward(None, None, None, None, None) == 1
     assert L.moe_experts_set_activation_format(None, libmoe.MOE_ACT_MXFP4) == 1
+    assert L.moe_experts_set_router(None, None, None, None) == 1
     n = ctypes.c_int32(-1)
     assert L.moe_testing_read_h(None, None, None, ctypes.byref(n), None) == 1
 

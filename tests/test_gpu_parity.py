@@ -114,6 +114,31 @@ def test_expert_ffn_stage(name):
     assert_close(bf16_to_f64(ys), ys_ref, f"{name} shared FFN")
 
 
+@pytest.mark.parametrize("name", ["tiny", "wide", "verify8", "verify512"])
+def test_resident_router_matches_per_call_router(name):
+    """moe_experts_set_router (weights split once on the handle) gives the per-call router's ids,
+    weights and layer output bit for bit, through moe_route and moe_forward."""
+    from block_scaled_fp4_sqrt_gb300 import moe_experts_set_router, moe_forward, moe_route
+    wl, inp, ids_ref, wts_ref, layer = case(name)
+    x = x_to_device(inp.x)
+    y_call = layer.forward(x)
+    ids_call, w_call = layer.route(x)
+    moe_experts_set_router(layer.h, layer.router_w, layer.router_bias)
+    try:
+        ids = torch.empty_like(ids_call)
+        w = torch.empty_like(w_call)
+        moe_route(layer.h, x, None, None, ids, w)
+        y = torch.empty_like(y_call)
+        moe_forward(x, None, None, layer.h, layer.h_shared, y)
+        torch.cuda.synchronize()
+        layer.check()
+        assert torch.equal(ids, ids_call) and torch.equal(w, w_call)
+        assert np.array_equal(ids.cpu().numpy(), ids_ref)
+        assert torch.equal(y, y_call)
+    finally:
+        moe_experts_set_router(layer.h, None, None)
+
+
 @pytest.mark.parametrize("T", [1, 2, 31, 33, 100, 256])
 def test_tiny_ragged_sizes(T):
     """Chunk / tile edges: one token, partial 32-token chunks, expert groups longer than a 32-row tile."""

@@ -118,3 +118,33 @@ def test_stack_rejects_aliased_buffers(stack_layers):
             st.forward(x, token_ids=tok, out=x)
     finally:
         st.close()
+
+
+def test_stack_with_resident_routers(stack_layers):
+    """Learned layers whose router is resident on the handle (moe_experts_set_router): the same output
+    as the stack that passes router weights, directly and replayed from a graph."""
+    from block_scaled_fp4_sqrt_gb300 import moe_experts_set_router
+    inputs, layers = stack_layers
+    tok = torch.from_numpy(inputs[0].token_ids).to(device())
+    x = x_to_device(synth.gen_x(9, T, 256))
+    ref_st = _stack(layers)
+    ref = ref_st.forward(x, token_ids=tok).clone()
+    ref_st.close()
+    learned = [ly for ly in layers if ly.hash_table is None]
+    try:
+        for ly in learned:
+            moe_experts_set_router(ly.h, ly.router_w, ly.router_bias)
+            ly.resident_router = True
+        for use_graph in (False, True):
+            st = _stack(layers, use_graph=use_graph)
+            out = torch.empty_like(x)
+            st.forward(x, token_ids=tok, out=out)
+            st.forward(x, token_ids=tok, out=out)
+            torch.cuda.synchronize()
+            st.check()
+            assert torch.equal(out, ref)
+            st.close()
+    finally:
+        for ly in learned:
+            ly.resident_router = False
+            moe_experts_set_router(ly.h, None, None)
