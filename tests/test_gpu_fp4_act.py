@@ -228,3 +228,47 @@ def test_shared_expert_must_match_the_format():
         moe_experts_set_activation_format(layer.h_shared, ACT)
     with pytest.raises(ValueError):
         moe_experts_set_activation_format(layer.h, "fp6")
+
+
+def test_fp4_hash_layer_and_graph_replayed_stack():
+    """The variant on a hash-routed layer (64 tokens, 32 experts), against the oracle on the kernel's h;
+    and a two-layer stack of MXFP4 layers replayed from a CUDA graph, bit-identical to its direct launches."""
+    from block_scaled_fp4_sqrt_gb300 import MoELayer, MoEStack
+    wl = synth.Workload("fp4_hash", 64, 512, 256, 32, 4, hash_vocab=1000)
+    inp = synth.gen_layer(wl, 4)
+    ids_ref, wts_ref = oracle.hash_route(inp.token_ids, inp.hash_table, wl.k, wl.route_scale)
+    layer = MoELayer.from_host(inp, device=device(), max_T=wl.T, act=ACT)
+    try:
+        y, hq, hs = _forward_and_h(layer, x_to_device(inp.x))
+        assert np.array_equal(layer.last_topk_ids().cpu().numpy(), ids_ref)
+        counts, offsets, perm, inv = oracle.permute(ids_ref, wl.E)
+        R = wl.T * wl.k
+        q, s = oracle.quantize_x(inp.x, act=ACT)
+        _, hq_r, hs_r, hpre_r = oracle.expert_ffn(q[perm], s[perm], inp.experts, offsets=offsets, act=ACT,
+                                                  want_hpre=True)
+        _, hq_s, hs_s, hpre_s = oracle.expert_ffn(q, s, inp.shared, act=ACT, want_hpre=True)
+        check_h(hq, hs, np.concatenate([hq_r, hq_s]), np.concatenate([hs_r, hs_s]),
+                np.concatenate([hpre_r, hpre_s]), "hash FP4 h")
+        row_w = np.empty(R)
+        row_w[inv.reshape(-1)] = wts_ref.reshape(-1)
+        y_ref = y_on_gpu_h(hq, hs, np.repeat(np.arange(wl.E), counts), row_w, inp.experts, inp.shared, inv, wl.T, R)
+        assert_close(bf16_to_f64(y), y_ref, "hash FP4 forward")
+        tok = layer.token_ids
+        learned = synth.gen_layer(synth.Workload("fp4_learned", 64, wl.d, wl.f, wl.E, wl.k), 5)
+        layer2 = MoELayer.from_host(learned, device=device(), max_T=wl.T, act=ACT, resident_router=True)
+        try:
+            x = x_to_device(inp.x)
+            direct, graph = (MoEStack([layer, layer2], max_T=wl.T, use_graph=g) for g in (False, True))
+            ref = direct.forward(x, token_ids=tok).clone()
+            out = torch.empty_like(ref)
+            graph.forward(x, token_ids=tok, out=out)
+            graph.forward(x, token_ids=tok, out=out)
+            torch.cuda.synchronize()
+            graph.check()
+            assert torch.equal(out, ref)
+            direct.close()
+            graph.close()
+        finally:
+            layer2.close()
+    finally:
+        layer.close()

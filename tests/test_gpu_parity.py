@@ -139,6 +139,21 @@ def test_resident_router_matches_per_call_router(name):
         moe_experts_set_router(layer.h, None, None)
 
 
+def test_resident_router_argument_checks():
+    from block_scaled_fp4_sqrt_gb300 import MoEError, moe_experts_set_router, moe_forward
+    wl, inp, ids_ref, wts_ref, layer = case("tiny")
+    x = x_to_device(inp.x)
+    y = torch.empty((wl.T, wl.d), dtype=torch.bfloat16, device=device())
+    with pytest.raises(MoEError):  # no resident router and no weights given
+        moe_forward(x, None, None, layer.h, layer.h_shared, y)
+    with pytest.raises(MoEError):  # weights without a bias
+        moe_experts_set_router(layer.h, layer.router_w, None)
+    mis = torch.empty(layer.router_w.numel() + 4, dtype=torch.float32, device=device())[1:1 + layer.router_w.numel()]
+    with pytest.raises(MoEError):  # not 16-byte aligned
+        moe_experts_set_router(layer.h, mis, layer.router_bias)
+    moe_experts_set_router(layer.h, None, None)  # nothing resident: dropping is a no-op
+
+
 @pytest.mark.parametrize("T", [1, 2, 31, 33, 100, 256])
 def test_tiny_ragged_sizes(T):
     """Chunk / tile edges: one token, partial 32-token chunks, expert groups longer than a 32-row tile."""
