@@ -84,6 +84,23 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64
   }
 }
 
+// Polling wait for the phase with the given parity: mbarrier.test_wait never suspends the thread, so it
+// sees the phase complete at once.  For waiters with no other warps to steal issue slots from (the handoff
+// of the accumulator in the verify-batch GEMM shape); bounded by budget_ns like mbar_wait.
+__device__ __forceinline__ bool mbar_spin(uint64_t* bar, uint32_t parity, uint64_t budget_ns) {
+  const uint64_t t0 = globaltimer_ns();
+  for (int i = 0;; ++i) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    if (ok) return true;
+    if ((i & 255) == 255 && globaltimer_ns() - t0 > budget_ns) return false;
+  }
+}
+
 // ------------------------------------------------------------------------- routing
 __device__ __forceinline__ float softplus_f(float l) { return fmaxf(l, 0.f) + log1pf(expf(-fabsf(l))); }
 

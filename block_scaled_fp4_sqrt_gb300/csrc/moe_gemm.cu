@@ -117,6 +117,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                            const __grid_constant__ CUtensorMap tm_act, const __grid_constant__ CUtensorMap tm_act_small,
                            const GemmArgs a) {
   using C = Cfg<STAGES, AROWS, EPI, FP4>;
+  // The accumulator handoff (acc_full / acc_empty) is polled in the 32-row shape: there only the issuer and
+  // four epilogue warps run, and polling took 4 % off the T = 8 step (measured).  With 128-row tiles the 16
+  // polling epilogue warps took issue slots from the producer and issuer (the T = 8192 step 2 % slower).
+  constexpr bool kPollHandoff = AROWS == kSmallRows;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
@@ -259,7 +263,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           if (kg == 0) {  // a new work item: the epilogue must have drained the accumulator
-            if (abort_flag || !mbar_wait(acc_empty, ((uint32_t)item & 1u) ^ 1u, a.budget_ns)) {
+            const uint32_t par = ((uint32_t)item & 1u) ^ 1u;
+            if (abort_flag || !(kPollHandoff ? mbar_spin(acc_empty, par, a.budget_ns)
+                                             : mbar_wait(acc_empty, par, a.budget_ns))) {
               ok = false;
               break;
             }
@@ -310,7 +316,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // 32-row tiles keep their rows in TMEM lanes 0..31: the other quadrants' warps have nothing to do
     const int my_total = (AROWS == kSmallRows && q != 0) ? 0 : total;
     for (int w = blockIdx.x; w < my_total; w += gridDim.x, ++it) {
-      bool got = !abort_flag && mbar_wait(acc_full, (uint32_t)it & 1u, a.budget_ns);
+      bool got = !abort_flag && (kPollHandoff ? mbar_spin(acc_full, (uint32_t)it & 1u, a.budget_ns)
+                                              : mbar_wait(acc_full, (uint32_t)it & 1u, a.budget_ns));
       got = __all_sync(0xFFFFFFFFu, got);
       if (!got) {
         if (lane == 0) {
