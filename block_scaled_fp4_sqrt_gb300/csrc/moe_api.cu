@@ -28,6 +28,7 @@ struct moe_experts_s {
   CUtensorMap tm2p;
   int act_fp4 = 0;    // activation format: 0 = MXFP8, 1 = MXFP4 (moe_experts_set_activation_format)
   __nv_bfloat16* router_split = nullptr;  // owned: resident router weight planes (moe_experts_set_router)
+  float* router_w32 = nullptr;            // owned: the resident router weights in fp32 (small batches)
   float* router_bias = nullptr;           // owned: its bias [E]
   CUtensorMap tm_router;                  // map over router_split
   const int32_t* hash_table = nullptr;
@@ -209,6 +210,7 @@ size_t workspace_layout(int max_T, int d, int f, int E, int k, Workspace* ws, vo
   w.h_q = (uint8_t*)take((size_t)dm.rows * f);
   w.h_sf = (uint8_t*)take((size_t)dm.max_tiles * (f / 128) * kSfAtomBytes);
   w.y_rows = (float*)take((size_t)dm.rows * d * 4);
+  w.route_done = (int32_t*)take(4);
   if (ws) *ws = w;
   return align_up(off, 256);
 }
@@ -303,6 +305,7 @@ void moe_experts_destroy(moe_experts_t h) {
   if (h->sf2) cudaFree(h->sf2);
   if (h->status) cudaFree(h->status);
   if (h->router_split) cudaFree(h->router_split);
+  if (h->router_w32) cudaFree(h->router_w32);
   if (h->router_bias) cudaFree(h->router_bias);
   delete h;
 }
@@ -314,8 +317,10 @@ moe_status_t moe_experts_set_router(moe_experts_t h, const float* router_w, cons
   if (!router_w && !router_bias) {  // drop the resident router
     MOE_CUDA(cudaStreamSynchronize(s), "stream synchronize");
     if (h->router_split) cudaFree(h->router_split);
+    if (h->router_w32) cudaFree(h->router_w32);
     if (h->router_bias) cudaFree(h->router_bias);
     h->router_split = nullptr;
+    h->router_w32 = nullptr;
     h->router_bias = nullptr;
     return MOE_OK;
   }
@@ -326,16 +331,21 @@ moe_status_t moe_experts_set_router(moe_experts_t h, const float* router_w, cons
   const int Epad = router_tc_epad(E);
   if (!h->router_split) {
     MOE_CUDA(cudaMalloc(&h->router_split, (size_t)3 * Epad * d * sizeof(__nv_bfloat16)), "router planes");
-    const cudaError_t e = cudaMalloc(&h->router_bias, (size_t)E * sizeof(float));
+    cudaError_t e = cudaMalloc(&h->router_bias, (size_t)E * sizeof(float));
+    if (e == cudaSuccess) e = cudaMalloc(&h->router_w32, (size_t)E * d * sizeof(float));
     if (e != cudaSuccess) {
       cudaFree(h->router_split);
+      if (h->router_bias) cudaFree(h->router_bias);
       h->router_split = nullptr;
-      return cuda_fail(e, "router bias");
+      h->router_bias = nullptr;
+      return cuda_fail(e, "router bias / fp32 copy");
     }
     const moe_status_t st = make_map_bf16(&h->tm_router, h->router_split, 64, (uint64_t)3 * Epad * (d / 64), 256);
     if (st != MOE_OK) return st;
   }
   MOE_CUDA(launch_split_router(router_w, E, d, h->router_split, s), "router weight split");
+  MOE_CUDA(cudaMemcpyAsync(h->router_w32, router_w, (size_t)E * d * sizeof(float), cudaMemcpyDeviceToDevice, s),
+           "router weight copy");
   MOE_CUDA(cudaMemcpyAsync(h->router_bias, router_bias, (size_t)E * sizeof(float), cudaMemcpyDeviceToDevice, s),
            "router bias copy");
   return MOE_OK;
@@ -357,6 +367,8 @@ moe_status_t moe_set_workspace(moe_experts_t h, void* ws, size_t bytes, int32_t 
                                        nullptr);
   if (bytes < need) return fail(MOE_ERR_WORKSPACE, "workspace of %zu bytes, %zu needed for max_T %d", bytes, need, max_T);
   workspace_layout(max_T, h->cfg.d_model, h->cfg.d_ff, h->cfg.n_experts, h->cfg.top_k, &h->ws, ws);
+  // the small-batch router's CTA count starts at zero (and every call leaves it there)
+  MOE_CUDA(cudaMemset(h->ws.route_done, 0, sizeof(int32_t)), "router counter");
   h->ws_base = ws;
   h->ws_bytes = bytes;
   h->ws_max_T = max_T;
@@ -407,6 +419,13 @@ static moe_status_t route_into(moe_experts_s* h, const moe_input_t* x, const flo
   if (E > 512) return fail(MOE_ERR_UNSUPPORTED, "the learned router supports up to 512 experts");
   if (!resident && !aligned(router_w, 16)) return fail(MOE_ERR_INVALID_ARG, "router_w must be 16-byte aligned");
   if (T == 0) return MOE_OK;
+  if (T <= kRouterSmallMaxT) {  // small batches: fp32 logits over the whole GPU and top-k, one kernel
+    MOE_CUDA(launch_router_small(static_cast<const __nv_bfloat16*>(x->x_bf16), resident ? h->router_w32 : router_w,
+                                 resident ? h->router_bias : router_bias, T, d, E, k, h->cfg.route_scale, h->ws.logits,
+                                 h->ws.route_done, ids, wts, resident ? 1 : 0, s),
+             "router");
+    return MOE_OK;
+  }
   CUtensorMap tm_x, tm_w;
   const int Epad = router_tc_epad(E);
   moe_status_t st = make_map_bf16(&tm_x, x->x_bf16, (uint64_t)d, (uint64_t)T, 128);

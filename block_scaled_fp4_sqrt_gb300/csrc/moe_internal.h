@@ -66,6 +66,7 @@ struct Workspace {
   uint8_t* h_q;         // [rows, f]
   uint8_t* h_sf;        // [max_tiles, f/128, 512]
   float* y_rows;         // [rows, d] weighted expert outputs (fp32)
+  int32_t* route_done;   // [1] CTA count of the small-batch router (zero between calls)
 };
 
 // Text returned by moe_last_error() on this thread.
@@ -114,6 +115,13 @@ cudaError_t launch_router_tc(const CUtensorMap& tm_x, const CUtensorMap& tm_w, i
                              float* partial, int* status, uint64_t budget_ns, cudaStream_t s);
 cudaError_t launch_router_topk(const float* partial, int ksplit, const float* bias, int T, int E, int k,
                                float route_scale, int32_t* ids, float* wts, cudaStream_t s);
+// Small-batch router (T <= kRouterSmallMaxT, E <= 512): fp32 logits spread over the GPU, then top-k in the
+// last CTA; logits [T, E] scratch, done = a zeroed counter the kernel leaves at zero.  early_params: w and
+// bias are the handle's resident copies and may be read before the programmatic-dependency wait.
+constexpr int kRouterSmallMaxT = 32;
+cudaError_t launch_router_small(const __nv_bfloat16* x, const float* w, const float* bias, int T, int d, int E, int k,
+                                float route_scale, float* logits, int* done, int32_t* ids, float* wts,
+                                int early_params, cudaStream_t s);
 cudaError_t launch_hash_route(const int32_t* tok, const int32_t* table, int V, int T, int E, int k, float route_scale,
                               int32_t* ids, float* wts, int* status, cudaStream_t s);
 

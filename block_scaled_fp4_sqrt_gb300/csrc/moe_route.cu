@@ -138,6 +138,144 @@ __global__ void __launch_bounds__(512) router_topk_kernel(const float* __restric
   warp_route_topk<NPL>(sc, sel, E, k, route_scale, ids + (size_t)t * k, wts + (size_t)t * k);
 }
 
+// Router for small batches (T <= 32), one kernel.  A 128-token tensor-core tile would leave most of
+// the GPU idle while one cluster streams the weights; here every CTA takes two experts and computes their
+// full fp32 dot products with all T tokens, so the 4 * E * d bytes of router weights are read by E / 2
+// SMs at once.  Warp w sums K range [w d/8, (w+1) d/8) (lane-strided, then a shuffle tree), the CTA adds
+// the eight warp sums in order and stores the logits; the last CTA to finish (an atomic count, fenced on
+// both sides) computes s = sqrt(softplus(l)) and runs the same warp top-k as the other routers for every
+// token, and resets the count for the next call.
+// early_params: the weights and bias are the handle's resident copies (written only by
+// moe_experts_set_router's copies, never by the kernel this one may overlap), so a lane loads its first
+// weight vectors and its bias values before the programmatic-dependency wait, hiding their HBM latency
+// behind the previous kernel's tail; only x waits.
+template <int TMAX, int NPL>
+__global__ void __launch_bounds__(256) router_small_kernel(const __nv_bfloat16* __restrict__ x,
+                                                           const float* __restrict__ w, const float* __restrict__ bias,
+                                                           int T, int d, int E, int k, float route_scale,
+                                                           float* __restrict__ logits, int* __restrict__ done,
+                                                           int32_t* __restrict__ ids, float* __restrict__ wts,
+                                                           int early_params) {
+  pdl_trigger();
+  __shared__ float red[8][2][TMAX];
+  __shared__ int s_last;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int e0 = 2 * blockIdx.x;
+  const bool has1 = e0 + 1 < E;
+  const int kw = d / 8, kb = warp * kw;
+  const float* w0p = w + (size_t)e0 * d;
+  const float* w1p = w + (size_t)(has1 ? e0 + 1 : e0) * d;
+  float acc0[TMAX], acc1[TMAX];
+#pragma unroll
+  for (int t = 0; t < TMAX; ++t) acc0[t] = acc1[t] = 0.f;
+  float4 wa[4], wb[4];
+  auto load_w = [&](int base) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int kk = base + 128 * j + 4 * lane;
+      const bool in = kk < kb + kw;
+      wa[j] = in ? __ldg(reinterpret_cast<const float4*>(w0p + kk)) : make_float4(0.f, 0.f, 0.f, 0.f);
+      wb[j] = in ? __ldg(reinterpret_cast<const float4*>(w1p + kk)) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  };
+  float bv[NPL];  // the bias values this lane's selection reads, if this CTA turns out to be the last
+  auto load_bias = [&]() {
+#pragma unroll
+    for (int i = 0; i < NPL; ++i) bv[i] = lane + 32 * i < E ? __ldg(&bias[lane + 32 * i]) : 0.f;
+  };
+  if (early_params) {
+    load_w(kb);
+    load_bias();
+  }
+  pdl_wait();
+  if (!early_params) {
+    load_w(kb);
+    load_bias();
+  }
+  // the warp's K range in pieces of 4 x 128: a lane holds its 4 weight vectors of both experts, then loads
+  // all tokens' activation vectors of the piece, so that a piece costs one memory round trip
+  for (int base = kb; base < kb + kw; base += 4 * 128) {
+    if (base != kb) load_w(base);
+    // tokens in groups of 8: all 32 activation vectors of a group are loaded before their FMAs
+#pragma unroll
+    for (int tg = 0; tg < TMAX; tg += 8) {
+      uint2 raw[8][4];
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int kk = base + 128 * j + 4 * lane;
+          raw[u][j] = (tg + u < T && kk < kb + kw)
+                          ? __ldg(reinterpret_cast<const uint2*>(x + (size_t)(tg + u) * d + kk))
+                          : make_uint2(0u, 0u);
+        }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int t = tg + u;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw[u][j].x));
+          const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw[u][j].y));
+          acc0[t] = fmaf(wa[j].x, lo.x, acc0[t]);
+          acc0[t] = fmaf(wa[j].y, lo.y, acc0[t]);
+          acc0[t] = fmaf(wa[j].z, hi.x, acc0[t]);
+          acc0[t] = fmaf(wa[j].w, hi.y, acc0[t]);
+          acc1[t] = fmaf(wb[j].x, lo.x, acc1[t]);
+          acc1[t] = fmaf(wb[j].y, lo.y, acc1[t]);
+          acc1[t] = fmaf(wb[j].z, hi.x, acc1[t]);
+          acc1[t] = fmaf(wb[j].w, hi.y, acc1[t]);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int t = 0; t < TMAX; ++t) {
+    float v0 = acc0[t], v1 = acc1[t];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      v0 += __shfl_xor_sync(0xFFFFFFFFu, v0, off);
+      v1 += __shfl_xor_sync(0xFFFFFFFFu, v1, off);
+    }
+    if (lane == 0) {
+      red[warp][0][t] = v0;
+      red[warp][1][t] = v1;
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x < 2 * TMAX) {
+    const int e = threadIdx.x / TMAX, t = threadIdx.x - e * TMAX;
+    if (t < T && (e == 0 || has1)) {
+      float l = 0.f;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) l += red[q][e][t];
+      logits[(size_t)t * E + e0 + e] = l;
+    }
+  }
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) s_last = atomicAdd(done, 1) == (int)gridDim.x - 1;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  if (threadIdx.x == 0) *done = 0;  // every CTA of this call has counted
+  for (int t = warp; t < T; t += 8) {
+    float sc[NPL], sel[NPL];
+#pragma unroll
+    for (int i = 0; i < NPL; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E) {
+        const float sv = sqrtf(softplus_f(__ldcg(&logits[(size_t)t * E + e])));
+        sc[i] = sv;
+        sel[i] = sv + bv[i];
+      } else {
+        sc[i] = 0.f;
+        sel[i] = -FLT_MAX;
+      }
+    }
+    warp_route_topk<NPL>(sc, sel, E, k, route_scale, ids + (size_t)t * k, wts + (size_t)t * k);
+  }
+}
+
 // Hash routing: ids = the token's table row (ascending), weights route_scale / k.  Out-of-range token
 // ids or table entries raise a device status bit and are replaced by valid values so that no later
 // kernel indexes out of bounds.
@@ -210,6 +348,19 @@ cudaError_t launch_router_topk(const float* partial, int ksplit, const float* bi
     default:
       return cudaErrorInvalidValue;
   }
+}
+
+cudaError_t launch_router_small(const __nv_bfloat16* x, const float* w, const float* bias, int T, int d, int E, int k,
+                                float route_scale, float* logits, int* done, int32_t* ids, float* wts,
+                                int early_params, cudaStream_t s) {
+  if (T < 1 || T > kRouterSmallMaxT || E > 512) return cudaErrorInvalidValue;
+  const dim3 grid((E + 1) / 2), block(256);
+#define MOE_SMALL(TM, NP) \
+  launch_pdl(router_small_kernel<TM, NP>, grid, block, 0, s, x, w, bias, T, d, E, k, route_scale, logits, done, ids, wts, \
+             early_params)
+  if (E <= 256) return T <= 8 ? MOE_SMALL(8, 8) : (T <= 16 ? MOE_SMALL(16, 8) : MOE_SMALL(32, 8));
+  return T <= 8 ? MOE_SMALL(8, 16) : (T <= 16 ? MOE_SMALL(16, 16) : MOE_SMALL(32, 16));
+#undef MOE_SMALL
 }
 
 cudaError_t launch_hash_route(const int32_t* tok, const int32_t* table, int V, int T, int E, int k, float route_scale,

@@ -123,8 +123,9 @@ MOE_API moe_status_t moe_experts_set_activation_format(moe_experts_t experts, in
 /*
  * Make the learned router resident on a routed set: router_w fp32 [E, d_model] (16-byte aligned) and
  * router_bias fp32 [E], both device buffers, are converted once into the form the router kernels read
- * (three bf16 planes whose sum is router_w exactly, in the tile order of the tensor-core router), into
- * memory the handle allocates and owns (6 * E_pad * d_model bytes + 4 * E; E_pad = E rounded up to 256).
+ * (three bf16 planes whose sum is router_w exactly, in the tile order of the tensor-core router, plus an
+ * fp32 copy for batches of up to 32 rows), into memory the handle allocates and owns
+ * (6 * E_pad * d_model + 4 * E * d_model + 4 * E bytes; E_pad = E rounded up to 256).
  * The copy is enqueued on `stream`; the inputs may be released once `stream` has passed the call.  Later
  * moe_route / moe_forward calls (and stack layers) with router_w = router_bias = NULL use it and skip
  * the per-call conversion; calls that pass router weights still use those.  Calling it again replaces

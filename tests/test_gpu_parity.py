@@ -38,6 +38,20 @@ def test_route_parity(name):
     assert np.allclose(w.sum(axis=1), wl.route_scale, rtol=1e-5)
 
 
+@pytest.mark.parametrize("name,T", [("wide", 16), ("wide", 32), ("verify512", 32), ("verify512", 33)])
+def test_route_parity_small_batch_boundary(name, T):
+    """Batches of up to 32 rows take the small-batch router (fp32 logits over the whole GPU, top-k in its
+    last CTA), larger ones the tensor-core cluster router: both sides of the boundary, 256 and 384 experts."""
+    wl, inp, ids_ref, wts_ref, layer = case(name, T=T)
+    ids, w = _routing_on_gpu(layer, x_to_device(inp.x))
+    layer.check()
+    assert np.array_equal(ids, ids_ref)
+    assert np.max(np.abs(w - wts_ref) / np.abs(wts_ref)) <= TOL_WEIGHT_REL
+    # twice in a row: the kernel's CTA count is back at zero
+    ids2, w2 = _routing_on_gpu(layer, x_to_device(inp.x))
+    assert np.array_equal(ids2, ids) and np.array_equal(w2, w)
+
+
 @pytest.mark.parametrize("name", SMALL + FULL)
 def test_permute_parity(name):
     wl, inp, ids_ref, wts_ref, layer = case(name)
