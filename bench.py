@@ -276,9 +276,12 @@ def run_reference(args, wl):
 def layer_launches(wl) -> int:
     """Kernels one layer forward launches with the router resident on the handle.  Route: the hash-table
     kernel, or the fused cluster router (up to 256 experts; above that tensor-core logits + a top-k kernel).
-    Dispatch: histogram, column scan, group scan, gather.  The two grouped GEMMs, then the combine."""
-    route = 1 if wl.hashed else (1 if wl.E <= 256 else 2)  # router weights resident: no per-call split
-    return route + 4 + 2 + 1
+    Dispatch: histogram, column scan, group scan, gather -- for learned routing of up to 32 rows the router's
+    last CTA writes the dispatch state and only the gather remains.  The two grouped GEMMs, then the combine."""
+    small = not wl.hashed and wl.T <= 32
+    route = 1 if (wl.hashed or small or wl.E <= 256) else 2  # router weights resident: no per-call split
+    dispatch = 1 if small else 4
+    return route + dispatch + 2 + 1
 
 
 def workload_config(wl, act: str = "mxfp8"):

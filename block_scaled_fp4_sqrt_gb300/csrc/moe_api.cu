@@ -399,8 +399,9 @@ static moe_status_t check_input(const moe_experts_s* h, const moe_input_t* x) {
   return MOE_OK;
 }
 
+// disp: for learned routing with T <= kRouterSmallMaxT only (the small-batch router writes the dispatch state).
 static moe_status_t route_into(moe_experts_s* h, const moe_input_t* x, const float* router_w, const float* router_bias,
-                               int32_t* ids, float* wts, cudaStream_t s) {
+                               int32_t* ids, float* wts, cudaStream_t s, const SmallDispatch* disp = nullptr) {
   const int T = x->T, E = h->cfg.n_experts, k = h->cfg.top_k, d = h->cfg.d_model;
   if (h->hash_table) {
     if (router_w || router_bias) return fail(MOE_ERR_INVALID_ARG, "hash layer: router_w and router_bias must be NULL");
@@ -422,7 +423,7 @@ static moe_status_t route_into(moe_experts_s* h, const moe_input_t* x, const flo
   if (T <= kRouterSmallMaxT) {  // small batches: fp32 logits over the whole GPU and top-k, one kernel
     MOE_CUDA(launch_router_small(static_cast<const __nv_bfloat16*>(x->x_bf16), resident ? h->router_w32 : router_w,
                                  resident ? h->router_bias : router_bias, T, d, E, k, h->cfg.route_scale, h->ws.logits,
-                                 h->ws.route_done, ids, wts, resident ? 1 : 0, s),
+                                 h->ws.route_done, ids, wts, resident ? 1 : 0, disp, s),
              "router");
     return MOE_OK;
   }
@@ -597,15 +598,6 @@ moe_status_t forward_impl(const moe_input_t* x, const float* router_w, const flo
   if (residual_bf16 && !aligned(residual_bf16, 16)) return fail(MOE_ERR_INVALID_ARG, "residual must be 16-byte aligned");
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const int T = x->T, E = h->cfg.n_experts, k = h->cfg.top_k, d = h->cfg.d_model;
-  mark_stage(h, 0, s);
-  st = route_into(h, x, router_w, router_bias, h->ws.topk_ids, h->ws.topk_w, s);
-  if (st != MOE_OK) return st;
-  h->last_T = T;
-  mark_stage(h, 1, s);
-  if (T == 0) {
-    for (int i = 2; i <= MOE_N_STAGES; ++i) mark_stage(h, i, s);
-    return MOE_OK;
-  }
   const int has_shared = sh ? 1 : 0;
   const int G = E + has_shared;
   const int R = T * k;
@@ -613,10 +605,25 @@ moe_status_t forward_impl(const moe_input_t* x, const float* router_w, const flo
   const Dims dm = dims_for(h->ws_max_T, E, k);
   const int n_chunks = (T + 31) / 32;
   const int bn = tile_rows_for(R, E);
-  MOE_CUDA(launch_histogram(h->ws.topk_ids, T, k, E, G, h->ws.chunk_hist, h->status, s), "histogram");
-  MOE_CUDA(launch_scan(h->ws.chunk_hist, n_chunks, T, E, G, has_shared, bn, dm.max_tiles, h->ws.counts,
-                       h->ws.offsets, h->ws.tile_off, h->ws.n_tiles, h->ws.tiles, h->status, s),
-           "scan");
+  // learned routing of a small batch: the router's last CTA also writes the dispatch state
+  const bool router_dispatch = !h->hash_table && T >= 1 && T <= kRouterSmallMaxT && bn >= kRouterSmallMaxT;
+  SmallDispatch sd{G, has_shared, bn, dm.max_tiles, h->ws.chunk_hist, h->ws.counts, h->ws.offsets, h->ws.tile_off,
+                   h->ws.n_tiles, h->ws.tiles};
+  mark_stage(h, 0, s);
+  st = route_into(h, x, router_w, router_bias, h->ws.topk_ids, h->ws.topk_w, s, router_dispatch ? &sd : nullptr);
+  if (st != MOE_OK) return st;
+  h->last_T = T;
+  mark_stage(h, 1, s);
+  if (T == 0) {
+    for (int i = 2; i <= MOE_N_STAGES; ++i) mark_stage(h, i, s);
+    return MOE_OK;
+  }
+  if (!router_dispatch) {
+    MOE_CUDA(launch_histogram(h->ws.topk_ids, T, k, E, G, h->ws.chunk_hist, h->status, s), "histogram");
+    MOE_CUDA(launch_scan(h->ws.chunk_hist, n_chunks, T, E, G, has_shared, bn, dm.max_tiles, h->ws.counts,
+                         h->ws.offsets, h->ws.tile_off, h->ws.n_tiles, h->ws.tiles, h->status, s),
+             "scan");
+  }
   MOE_CUDA(launch_gather(static_cast<const __nv_bfloat16*>(x->x_bf16), h->ws.topk_ids, h->ws.topk_w, h->ws.chunk_hist,
                          h->ws.offsets, h->ws.tile_off, T, d, k, E, G, has_shared, bn, h->ws.a_q, h->ws.a_sf,
                          nullptr, h->ws.perm_tok, h->ws.inv_pos, h->ws.row_w, h->act_fp4, s),

@@ -118,10 +118,22 @@ cudaError_t launch_router_topk(const float* partial, int ksplit, const float* bi
 // Small-batch router (T <= kRouterSmallMaxT, E <= 512): fp32 logits spread over the GPU, then top-k in the
 // last CTA; logits [T, E] scratch, done = a zeroed counter the kernel leaves at zero.  early_params: w and
 // bias are the handle's resident copies and may be read before the programmatic-dependency wait.
+// disp (optional): the last CTA also writes the dispatch state that histogram_kernel + colscan_kernel +
+// groupscan_kernel would (one 32-token chunk: every chunk base is 0; at most 32 rows per group: one tile
+// per non-empty group).
 constexpr int kRouterSmallMaxT = 32;
+struct SmallDispatch {
+  int G, has_shared, bn, max_tiles;
+  int32_t* chunk_hist;  // [G] (one chunk)
+  int32_t* counts;      // [G]
+  int32_t* offsets;     // [G + 1]
+  int32_t* tile_off;    // [G + 1]
+  int32_t* n_tiles;     // [1]
+  RowTile* tiles;       // [max_tiles]
+};
 cudaError_t launch_router_small(const __nv_bfloat16* x, const float* w, const float* bias, int T, int d, int E, int k,
                                 float route_scale, float* logits, int* done, int32_t* ids, float* wts,
-                                int early_params, cudaStream_t s);
+                                int early_params, const SmallDispatch* disp, cudaStream_t s);
 cudaError_t launch_hash_route(const int32_t* tok, const int32_t* table, int V, int T, int E, int k, float route_scale,
                               int32_t* ids, float* wts, int* status, cudaStream_t s);
 

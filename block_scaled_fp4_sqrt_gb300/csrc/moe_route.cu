@@ -155,7 +155,7 @@ __global__ void __launch_bounds__(256) router_small_kernel(const __nv_bfloat16* 
                                                            int T, int d, int E, int k, float route_scale,
                                                            float* __restrict__ logits, int* __restrict__ done,
                                                            int32_t* __restrict__ ids, float* __restrict__ wts,
-                                                           int early_params) {
+                                                           int early_params, SmallDispatch disp) {
   pdl_trigger();
   __shared__ float red[8][2][TMAX];
   __shared__ int s_last;
@@ -274,6 +274,80 @@ __global__ void __launch_bounds__(256) router_small_kernel(const __nv_bfloat16* 
     }
     warp_route_topk<NPL>(sc, sel, E, k, route_scale, ids + (size_t)t * k, wts + (size_t)t * k);
   }
+  if (!disp.counts) return;
+  // Dispatch state of this batch (the ids above are this block's own global writes, visible after the
+  // barrier).  Rows per group <= T <= 32, so a non-empty group is one tile and the lone 32-token chunk's
+  // bases are all 0.  Groups are scanned in thread-contiguous runs of kGPer, then across the block.
+  constexpr int kGPer = 3;  // 256 threads x 3 >= 513 groups
+  __shared__ int s_cnt[256 * kGPer];
+  __shared__ int s_wsum[2][8];
+  const int G = disp.G;
+  __syncthreads();
+  for (int g = threadIdx.x; g < G; g += blockDim.x) s_cnt[g] = (disp.has_shared && g == E) ? T : 0;
+  __syncthreads();
+  for (int i = threadIdx.x; i < T * k; i += blockDim.x) atomicAdd(&s_cnt[ids[i]], 1);
+  __syncthreads();
+  int c[kGPer], nt[kGPer], run_r = 0, run_t = 0;
+#pragma unroll
+  for (int j = 0; j < kGPer; ++j) {
+    const int g = threadIdx.x * kGPer + j;
+    c[j] = g < G ? s_cnt[g] : 0;
+    nt[j] = (c[j] + disp.bn - 1) / disp.bn;
+    run_r += c[j];
+    run_t += nt[j];
+  }
+  // exclusive prefix of (run_r, run_t) over the block's threads
+  int ir = run_r, it = run_t;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int orr = __shfl_up_sync(0xFFFFFFFFu, ir, off), ott = __shfl_up_sync(0xFFFFFFFFu, it, off);
+    if (lane >= off) {
+      ir += orr;
+      it += ott;
+    }
+  }
+  if (lane == 31) {
+    s_wsum[0][warp] = ir;
+    s_wsum[1][warp] = it;
+  }
+  __syncthreads();
+  int br = 0, bt = 0, tot_r = 0, tot_t = 0;
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    if (q < warp) {
+      br += s_wsum[0][q];
+      bt += s_wsum[1][q];
+    }
+    tot_r += s_wsum[0][q];
+    tot_t += s_wsum[1][q];
+  }
+  int off_r = br + ir - run_r, off_t = bt + it - run_t;
+#pragma unroll
+  for (int j = 0; j < kGPer; ++j) {
+    const int g = threadIdx.x * kGPer + j;
+    if (g < G) {
+      disp.chunk_hist[g] = 0;
+      disp.counts[g] = c[j];
+      disp.offsets[g] = off_r;
+      disp.tile_off[g] = off_t;
+      for (int i = 0; i < nt[j]; ++i)
+        if (off_t + i < disp.max_tiles) {
+          RowTile rt;
+          rt.group = g;
+          rt.row0 = off_r + i * disp.bn;
+          rt.nrows = min(disp.bn, c[j] - i * disp.bn);
+          rt.pad = 0;
+          disp.tiles[off_t + i] = rt;
+        }
+    }
+    off_r += c[j];
+    off_t += nt[j];
+  }
+  if (threadIdx.x == 0) {
+    disp.offsets[G] = tot_r;
+    disp.tile_off[G] = tot_t;
+    *disp.n_tiles = min(tot_t, disp.max_tiles);
+  }
 }
 
 // Hash routing: ids = the token's table row (ascending), weights route_scale / k.  Out-of-range token
@@ -352,12 +426,15 @@ cudaError_t launch_router_topk(const float* partial, int ksplit, const float* bi
 
 cudaError_t launch_router_small(const __nv_bfloat16* x, const float* w, const float* bias, int T, int d, int E, int k,
                                 float route_scale, float* logits, int* done, int32_t* ids, float* wts,
-                                int early_params, cudaStream_t s) {
+                                int early_params, const SmallDispatch* disp, cudaStream_t s) {
   if (T < 1 || T > kRouterSmallMaxT || E > 512) return cudaErrorInvalidValue;
+  if (disp && (disp->G > 256 * 3 || disp->bn < kRouterSmallMaxT)) return cudaErrorInvalidValue;
+  SmallDispatch dd{};
+  if (disp) dd = *disp;
   const dim3 grid((E + 1) / 2), block(256);
 #define MOE_SMALL(TM, NP) \
   launch_pdl(router_small_kernel<TM, NP>, grid, block, 0, s, x, w, bias, T, d, E, k, route_scale, logits, done, ids, wts, \
-             early_params)
+             early_params, dd)
   if (E <= 256) return T <= 8 ? MOE_SMALL(8, 8) : (T <= 16 ? MOE_SMALL(16, 8) : MOE_SMALL(32, 8));
   return T <= 8 ? MOE_SMALL(8, 16) : (T <= 16 ? MOE_SMALL(16, 16) : MOE_SMALL(32, 16));
 #undef MOE_SMALL
