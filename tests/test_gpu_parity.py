@@ -181,6 +181,25 @@ def test_tiny_ragged_sizes(T):
     assert_close(bf16_to_f64(y), y_ref, f"tiny T={T}")
 
 
+@pytest.mark.parametrize("E,k,T", [(9, 2, 8), (9, 2, 40), (1, 1, 5), (1, 1, 37)])
+def test_odd_and_single_expert_counts(E, k, T):
+    """An odd expert count (the small-batch router's last CTA holds one expert) and a single expert with
+    top-1, on both sides of the 32-row boundary: routing bit for bit, output within the tolerance."""
+    wl = synth.Workload(f"e{E}k{k}", T, 256, 128, E, k)
+    inp, ids_ref, wts_ref, _ = oracle.margin_filtered_layer(wl, seed=6)
+    layer = _layer_from(inp)
+    try:
+        x = x_to_device(inp.x)
+        y = layer.forward(x)
+        torch.cuda.synchronize()
+        layer.check()
+        assert np.array_equal(layer.last_topk_ids().cpu().numpy(), ids_ref)
+        y_ref = oracle.layer(inp.x, ids_ref, wts_ref, inp.experts, inp.shared, wl.swiglu_limit)
+        assert_close(bf16_to_f64(y), y_ref, f"E={E} k={k} T={T}")
+    finally:
+        layer.close()
+
+
 def test_empty_batch():
     wl, inp, ids_ref, wts_ref, layer = case("tiny")
     x = torch.empty((0, wl.d), dtype=torch.bfloat16, device=device())
