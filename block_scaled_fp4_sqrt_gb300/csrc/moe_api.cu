@@ -341,7 +341,15 @@ moe_status_t moe_experts_set_router(moe_experts_t h, const float* router_w, cons
       return cuda_fail(e, "router bias / fp32 copy");
     }
     const moe_status_t st = make_map_bf16(&h->tm_router, h->router_split, 64, (uint64_t)3 * Epad * (d / 64), 256);
-    if (st != MOE_OK) return st;
+    if (st != MOE_OK) {  // leave the handle without a resident router
+      cudaFree(h->router_split);
+      cudaFree(h->router_w32);
+      cudaFree(h->router_bias);
+      h->router_split = nullptr;
+      h->router_w32 = nullptr;
+      h->router_bias = nullptr;
+      return st;
+    }
   }
   MOE_CUDA(launch_split_router(router_w, E, d, h->router_split, s), "router weight split");
   MOE_CUDA(cudaMemcpyAsync(h->router_w32, router_w, (size_t)E * d * sizeof(float), cudaMemcpyDeviceToDevice, s),
