@@ -366,6 +366,10 @@ __global__ void __launch_bounds__(kFThreads, 1) router_fused_kernel(const __grid
       }
     }
   }
+  // the selection's bias values, loaded before the cluster barrier so that their latency hides behind it
+  float bv[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) bv[i] = lane + 32 * i < a.E ? __ldg(&a.bias[lane + 32 * i]) : 0.f;
   __syncwarp();
   tc_fence_before();
   cluster_sync_all();  // every partial of the cluster is in shared memory
@@ -405,7 +409,7 @@ __global__ void __launch_bounds__(kFThreads, 1) router_fused_kernel(const __grid
       const int e = lane + 32 * i;
       const float sv = sqrtf(softplus_f(lrow[e]));
       sc[i] = e < a.E ? sv : 0.f;
-      sel[i] = e < a.E ? sv + __ldg(&a.bias[e]) : -FLT_MAX;
+      sel[i] = e < a.E ? sv + bv[i] : -FLT_MAX;
     }
     __syncwarp();
     warp_route_topk<8>(sc, sel, a.E, a.k, a.route_scale, a.ids + (size_t)t * a.k, a.wts + (size_t)t * a.k);
