@@ -14,7 +14,8 @@
  *     output stages"), the weighted sum being the moe_scatter_add epilogue (TensorSharp page, "DSpark
  *     and MoE CPU offload together").
  * Activations enter the expert GEMMs as MXFP8 (E4M3, one E8M0 scale per 32 along the reduction
- * dimension), as do the SwiGLU outputs before the down projection.
+ * dimension), as do the SwiGLU outputs before the down projection (MXFP4 in the variant that
+ * moe_experts_set_activation_format selects).
  *
  * Conventions for every call:
  *   - All tensor pointers are DEVICE pointers unless stated otherwise; row-major; the caller owns
@@ -23,8 +24,9 @@
  *     returned status covers host-side argument checks and launch errors only.  Conditions found on
  *     the device (an out-of-range expert or token id, a bounded wait that ran out) are recorded in a
  *     sticky per-handle status word and reported by moe_check().
- *   - No call allocates device memory except moe_experts_create (its copy of the weights); per-call
- *     scratch lives in a caller-provided workspace (moe_workspace_size / moe_set_workspace).
+ *   - No per-call path allocates device memory: moe_experts_create (its copy of the weights) and
+ *     moe_experts_set_router (its resident router) allocate once at set-up; per-call scratch lives in a
+ *     caller-provided workspace (moe_workspace_size / moe_set_workspace).
  *   - Shapes: d_model a multiple of 256, d_ff of 128; n_experts in [1, 1024]; top_k in [1, min(16,
  *     n_experts)]; n_experts <= 512 for the learned router (hash routing has no such limit).
  *   - Nothing is thread-safe per handle: calls on one handle must be ordered by the caller (one
@@ -51,7 +53,7 @@ typedef struct CUstream_st* moe_stream_t; /* identical to cudaStream_t */
 typedef enum {
   MOE_OK = 0,
   MOE_ERR_INVALID_ARG = 1, /* null pointer, bad size, misaligned pointer, wrong mode */
-  MOE_ERR_UNSUPPORTED = 2, /* shape outside the supported set, or no sm_100-family GPU */
+  MOE_ERR_UNSUPPORTED = 2, /* shape outside the supported set, or the GPU is not sm_103 */
   MOE_ERR_WORKSPACE = 3,   /* workspace missing or smaller than the call needs */
   MOE_ERR_CUDA = 4,        /* a CUDA runtime / driver call failed (text in moe_last_error()) */
   MOE_ERR_DEVICE_CHECK = 5, /* moe_check: a device-side range check failed */
