@@ -45,6 +45,11 @@ def parse_args():
     p.add_argument("--layers", type=int, default=1,
                    help="> 1: time a stack of this many MoE layers (moe_stack_forward) instead of one layer")
     p.add_argument("--hash-layers", type=int, default=3, help="hash-routed layers at the bottom of the stack")
+    p.add_argument("--workloads", default="all",
+                   help="after the headline, also measure these workloads into the line's 'workloads' object: "
+                        "'all' (the five layer configurations), 'none', or a comma-separated list (one GPU only)")
+    p.add_argument("--cpu-seconds-other", type=float, default=4.0,
+                   help="target CPU time of the oracle baseline sample of each extra workload")
     return p.parse_args()
 
 
@@ -291,25 +296,15 @@ def workload_config(wl, act: str = "mxfp8"):
             "l2": "no flush: expert weights read per step exceed the 129 MB L2"}
 
 
-def run_ours(args, wl):
+def measure_layer(args, wl, inp, dev, world, rank, mx_peak, mma_name, cpu_target_s, headline):
+    """Time one layer workload: device-timed steps, a staged pass, end-to-end legs and (one GPU) the oracle
+    on the host cores.  Returns the record of this workload (the keys of the benchmark's JSON line)."""
     import numpy as np
     import torch
 
-    import __graft_entry__ as g
-    import synth
-
-    rank, local_rank, world = dist_env()
-    g.build()
     import block_scaled_fp4_sqrt_gb300 as moe
 
-    if world > 1:
-        init_replicas("nccl")
-    torch.cuda.set_device(local_rank)
-    dev = torch.device("cuda", local_rank)
-
-    inp = synth.gen_layer(wl, args.seed)
-    if world > 1:  # each replica gets its own batch of token rows
-        inp.x = replica_x(args.seed, rank, world, wl.T, wl.d)
+    fp4 = args.act == "mxfp4"
     # the router weights are made resident once, like the expert weights (moe_experts_set_router)
     layer = moe.MoELayer.from_host(inp, device=dev, max_T=wl.T, act=args.act, resident_router=True)
     x = torch.from_numpy(inp.x.view(np.int16)).to(dev).view(torch.bfloat16)
@@ -327,15 +322,9 @@ def run_ours(args, wl):
     touched = int(torch.unique(ids).numel()) + 1  # + shared expert
     rows = wl.T * wl.k + wl.T
 
-    # block-scaled MMA peak of this GPU (the tensor roofline's denominator), before the timed region
-    fp4 = args.act == "mxfp4"
-    mx_peak = moe.moe_measure_mxf4_peak(4096) if fp4 else moe.moe_measure_mxf8f6f4_peak(4096)
-    mma_name = ("tcgen05.mma kind::mxf4.block_scale (E2M1 x E2M1, M=128 N=256 K=64) on every SM (moe_measure_mxf4_peak)"
-                if fp4 else "tcgen05.mma kind::mxf8f6f4.block_scale (E4M3 x E2M1, M=128 N=256 K=32) on every SM "
-                "(moe_measure_mxf8f6f4_peak)")
-
-    # ---- device-timed steps: the headline value, plain steps back to back on the launching stream
+    # ---- device-timed steps: plain steps back to back on the launching stream
     cvd = [v for v in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if v.strip()]
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     clocks = ClockSampler(cvd[local_rank] if local_rank < len(cvd) else local_rank)
     t_begin = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
@@ -447,11 +436,8 @@ def run_ours(args, wl):
     # the last step's result reached the host and equals the device-timed path's output (same x)
     assert torch.equal(out_hosts[(args.steps - 1) % 2], out.cpu()), "pipelined end-to-end output differs"
     ms_e2e_serial = timed_e2e(lambda n: [serial_step() for _ in range(n)])
-
-    if rank != 0:
-        if world > 1:
-            torch.distributed.destroy_process_group()
-        return
+    layer.close()
+    del x_devs, out_devs, x, out
 
     pk = peaks()
     dom = max(stage_ms, key=stage_ms.get)
@@ -460,8 +446,8 @@ def run_ours(args, wl):
     fl = gemm_flops(wl, rows)
     # verify shapes stream the expert weights (HBM bound); with >= 64 rows per expert (the prefill
     # chunk) the grouped GEMMs are dense block-scaled contractions (tensor bound)
-    compute_bound = dom in fl and wl.T * wl.k / wl.E >= 64
-    if compute_bound:
+    compute_bound = wl.T * wl.k / wl.E >= 64
+    if compute_bound and dom in fl:
         achieved = fl[dom] / (stage_ms[dom] * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": mx_peak, "unit": "TFLOP/s", "frac": achieved / mx_peak,
                 "traffic": measured_traffic(dom, traffic_key), "kernel": dom,
@@ -476,21 +462,30 @@ def run_ours(args, wl):
                 "frac": achieved / pk["hbm_gbs"], "traffic": measured_traffic(dom, traffic_key), "kernel": dom,
                 "peak_source": f"{pk['source']} HBM copy bandwidth", "algorithmic_bytes_per_launch": sb[dom]}
     lb = layer_bytes(wl, touched)
-    kernels_per_step = layer_launches(wl)
-    line = {
-        "metric": METRIC, "value": job_tokens_per_s(world, wl.T, ms), "unit": "tokens/s", "n_gpus": world,
-        "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "mxfp4 x mxfp4 -> f32" if fp4 else "mxfp4 x mxfp8 -> f32",
-        "data": "synthetic",
+    layer_fl = fl["gemm_gate_up"] + fl["gemm_down"]
+    if compute_bound:
+        layer_roof = {"bound": "tensor", "algorithmic_flops": layer_fl, "achieved": layer_fl / (ms * 1e-3) / 1e12,
+                      "peak": mx_peak, "unit": "TFLOP/s", "frac": layer_fl / (ms * 1e-3) / 1e12 / mx_peak,
+                      "peak_source": "measured in this run: back-to-back " + mma_name,
+                      "how": "expert GEMM FLOPs of the whole layer (2 x 3 x d x f per routed and shared row) over "
+                             "the whole step's time"}
+        if fp4:
+            layer_roof["frac_of_3x_mxf8f6f4_peak"] = None  # filled in by the caller
+    elif lb < 64 << 20:  # a few launches over kilobytes to megabytes: bound by launch latency, not by HBM
+        layer_roof = {"bound": "latency", "algorithmic_bytes": lb, "achieved": lb / (ms * 1e-3) / 1e9,
+                      "peak": None, "unit": "GB/s", "frac": None,
+                      "how": f"{layer_launches(wl)} dependent kernel launches over {lb / 1e6:.2f} MB"}
+    else:
+        layer_roof = {"bound": "hbm", "algorithmic_bytes": lb, "achieved": lb / (ms * 1e-3) / 1e9,
+                      "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": lb / (ms * 1e-3) / 1e9 / pk["hbm_gbs"]}
+    rec = {
+        "ms_per_step": ms, "value": job_tokens_per_s(world, wl.T, ms), "unit": "tokens/s",
         "config": dict(workload_config(wl, args.act), touched_experts=touched, parallelism=f"replicas x{world}"),
         "roofline": roof,
-        "layer_roofline": {"bound": "hbm", "algorithmic_bytes": lb, "achieved": lb / (ms * 1e-3) / 1e9,
-                           "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": lb / (ms * 1e-3) / 1e9 / pk["hbm_gbs"]},
-        "gemm_tensor": {"achieved": (fl["gemm_gate_up"] + fl["gemm_down"]) /
-                        ((stage_ms["gemm_gate_up"] + stage_ms["gemm_down"]) * 1e-3) / 1e12,
+        "layer_roofline": layer_roof,
+        "gemm_tensor": {"achieved": layer_fl / ((stage_ms["gemm_gate_up"] + stage_ms["gemm_down"]) * 1e-3) / 1e12,
                         "peak": mx_peak, "unit": "TFLOP/s",
-                        "frac": (fl["gemm_gate_up"] + fl["gemm_down"]) /
-                        ((stage_ms["gemm_gate_up"] + stage_ms["gemm_down"]) * 1e-3) / 1e12 / mx_peak},
+                        "frac": layer_fl / ((stage_ms["gemm_gate_up"] + stage_ms["gemm_down"]) * 1e-3) / 1e12 / mx_peak},
         "stage_ms": stage_ms,
         "stage_timing": {"ms_per_step": ms_staged, "how": "second pass of the same steps with CUDA events "
                          "between the stages (events serialise the launches there)"},
@@ -501,12 +496,90 @@ def run_ours(args, wl):
                        "and i-1 overlap step i on their own streams (two device buffers)",
                 "serial": {"value": job_tokens_per_s(world, wl.T, ms_e2e_serial), "ms_per_step": ms_e2e_serial,
                            "how": "copy in, forward, copy out on one stream"}},
-        "gpu_launches": kernels_per_step * args.steps,
+        "gpu_launches": layer_launches(wl) * args.steps,
         "clocks": clk,
     }
-    if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(inp, wl, args.cpu_seconds, args.seed, args.act)
-    layer.close()
+    if world == 1 and cpu_target_s > 0:
+        rec["cpu_baseline"] = cpu_baseline(inp, wl, cpu_target_s, args.seed, args.act)
+    return rec
+
+
+# The five layer configurations the layer is specified on; the default run measures all of them after the
+# headline (verify512), reusing one draw of the full-size expert weights.
+ALL_WORKLOADS = ("verify512", "verify8", "hash512", "prefill8192", "tiny")
+
+
+def run_ours(args, wl):
+    import torch
+
+    import __graft_entry__ as g
+    import synth
+
+    rank, local_rank, world = dist_env()
+    g.build()
+    import block_scaled_fp4_sqrt_gb300 as moe
+
+    if world > 1:
+        init_replicas("nccl")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+
+    inp = synth.gen_layer(wl, args.seed)
+    if world > 1:  # each replica gets its own batch of token rows
+        inp.x = replica_x(args.seed, rank, world, wl.T, wl.d)
+
+    # block-scaled MMA peak of this GPU (the tensor roofline's denominator), before the timed region
+    fp4 = args.act == "mxfp4"
+    mx_peak = moe.moe_measure_mxf4_peak(4096) if fp4 else moe.moe_measure_mxf8f6f4_peak(4096)
+    mx8_peak = moe.moe_measure_mxf8f6f4_peak(4096) if fp4 else mx_peak
+    mma_name = ("tcgen05.mma kind::mxf4.block_scale (E2M1 x E2M1, M=128 N=256 K=64) on every SM (moe_measure_mxf4_peak)"
+                if fp4 else "tcgen05.mma kind::mxf8f6f4.block_scale (E4M3 x E2M1, M=128 N=256 K=32) on every SM "
+                "(moe_measure_mxf8f6f4_peak)")
+
+    def finish(rec):
+        if fp4 and rec["layer_roofline"]["bound"] == "tensor":
+            lr = rec["layer_roofline"]
+            lr["frac_of_3x_mxf8f6f4_peak"] = lr["achieved"] / (3 * mx8_peak)
+            rec["roofline"]["frac_of_3x_mxf8f6f4_peak"] = rec["roofline"]["achieved"] / (3 * mx8_peak)
+        return rec
+
+    rec = finish(measure_layer(args, wl, inp, dev, world, rank, mx_peak, mma_name,
+                               0 if args.no_cpu_baseline else args.cpu_seconds, True))
+    others = {}
+    names = [] if args.workloads == "none" or world > 1 or args.experts or args.tokens else (
+        [n for n in ALL_WORKLOADS if n != wl.name] if args.workloads == "all" else
+        [n for n in args.workloads.split(",") if n and n != wl.name])
+    for name in names:
+        owl = synth.WORKLOADS[name]
+        if (owl.E, owl.d, owl.f) == (wl.E, wl.d, wl.f):  # the same expert weights: draw only x and the router
+            oinp = synth.gen_layer(owl, args.seed, with_shared=False, experts=inp.experts)
+            oinp.shared = inp.shared
+        else:
+            oinp = synth.gen_layer(owl, args.seed)
+        torch.cuda.empty_cache()
+        others[name] = finish(measure_layer(args, owl, oinp, dev, world, rank, mx_peak, mma_name,
+                                            0 if args.no_cpu_baseline else args.cpu_seconds_other, False))
+
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+    line = {
+        "metric": METRIC, "value": rec["value"], "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": rec["ms_per_step"], "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "mxfp4 x mxfp4 -> f32" if fp4 else "mxfp4 x mxfp8 -> f32",
+        "data": "synthetic",
+    }
+    line.update({k: v for k, v in rec.items() if k not in ("ms_per_step", "value", "unit")})
+    if fp4:
+        line["mxf8f6f4_peak_tflops"] = mx8_peak
+    if others:
+        line["workloads"] = {wl.name: {"ms_per_step": rec["ms_per_step"], "tokens_per_s": rec["value"],
+                                       "note": "the headline above"}}
+        for name, r in others.items():
+            line["workloads"][name] = dict({"ms_per_step": r["ms_per_step"], "tokens_per_s": r["value"]},
+                                           **{k: v for k, v in r.items() if k not in ("ms_per_step", "value", "unit",
+                                                                                       "stage_timing")})
     print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()

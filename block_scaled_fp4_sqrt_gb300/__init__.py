@@ -28,7 +28,7 @@ EXPORTED = ("moe_experts_create", "moe_experts_set_hash_table", "moe_workspace_s
             "moe_testing_stall_loads", "moe_set_stage_events", "moe_route_noalloc", "moe_measure_mxf8f6f4_peak",
             "moe_stack_create", "moe_stack_forward", "moe_stack_destroy", "moe_mx_blocks_unpack",
             "moe_experts_set_activation_format", "moe_measure_mxf4_peak", "moe_testing_read_h",
-            "moe_experts_set_router")
+            "moe_experts_set_router", "moe_testing_read_y32")
 
 MOE_MX_NIBBLES_PAIRED, MOE_MX_NIBBLES_SPLIT = 0, 1
 MOE_ACT_MXFP8, MOE_ACT_MXFP4 = 0, 1
@@ -87,6 +87,7 @@ def lib() -> ctypes.CDLL:
         L.moe_experts_set_activation_format.argtypes = [vp, i32]
         L.moe_testing_read_h.argtypes = [vp, vp, vp, ctypes.POINTER(i32), vp]
         L.moe_experts_set_router.argtypes = [vp, vp, vp, vp]
+        L.moe_testing_read_y32.argtypes = [vp, vp, ctypes.POINTER(i32), vp]
         L.moe_stack_create.argtypes = [ctypes.POINTER(moe_stack_layer_t), i32, i32, ctypes.POINTER(vp)]
         L.moe_stack_forward.argtypes = [vp, inp, vp, vp, vp]
         L.moe_stack_destroy.argtypes = [vp]
@@ -221,6 +222,17 @@ def moe_testing_read_h(h, f: int, act: str, stream=None):
     if n.value:
         _ok("moe_testing_read_h", lib().moe_testing_read_h(h, _p(hq), _p(hs), ctypes.byref(n), _stream(stream)))
     return hq, hs
+
+
+def moe_testing_read_y32(h, d: int, stream=None) -> torch.Tensor:
+    """The fp32 sums of the last moe_forward on the handle before their rounding to bf16 ([T, d])."""
+    n = ctypes.c_int32(0)
+    _ok("moe_testing_read_y32", lib().moe_testing_read_y32(h, None, ctypes.byref(n), _stream(stream)))
+    dev = torch.device("cuda", torch.cuda.current_device())
+    y = torch.empty((n.value, d), dtype=torch.float32, device=dev)
+    if n.value:
+        _ok("moe_testing_read_y32", lib().moe_testing_read_y32(h, _p(y), ctypes.byref(n), _stream(stream)))
+    return y
 
 
 def moe_experts_set_activation_format(h, fmt: str) -> None:
@@ -417,6 +429,11 @@ class MoELayer:
         """(codes, scales) of h from the last forward / expert_ffn (test hook)."""
         with torch.cuda.device(self.device):
             return moe_testing_read_h(self.h_shared if shared else self.h, self.f, self.act)
+
+    def last_y32(self) -> torch.Tensor:
+        """The last forward's output before its rounding to bf16, fp32 [T, d] (test hook)."""
+        with torch.cuda.device(self.device):
+            return moe_testing_read_y32(self.h, self.d)
 
     def last_topk_ids(self) -> torch.Tensor:
         return self.last_routing()[0]

@@ -75,7 +75,7 @@ def build_library(force: bool = False, jobs: int | None = None) -> str:
                 fh.write(dig)
     if todo or force or not os.path.exists(LIB):
         tmp = LIB + ".tmp"
-        cmd = [nvcc()] + ARCH + ["-shared", "-cudart", "shared", "-o", tmp] + objs + ["-lcuda"] * 0
+        cmd = [nvcc()] + ARCH + ["-shared", "-cudart", "shared", "-o", tmp] + objs
         r = subprocess.run(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}")

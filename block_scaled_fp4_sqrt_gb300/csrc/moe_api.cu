@@ -3,6 +3,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -43,13 +44,24 @@ struct moe_experts_s {
   int device = 0;
   int32_t last_T = 0;
   int32_t last_rows = 0;  // rows of the last grouped FFN (its h stays in the workspace)
+  int32_t last_fwd_T = -1;     // T of the last moe_forward (its fp32 expert rows stay in the workspace), or -1
+  int32_t last_fwd_shared = 0;  // whether that forward had a shared expert
   int stall_loads = 0;
   void* const* stage_events = nullptr;  // MOE_N_STAGES + 1 caller-owned cudaEvent_t, or null
+  // Changes whenever something a recorded launch sequence depends on changes (workspace, router, hash
+  // table, activation format, wait budget, test hooks, stage events): a stack's cached graph compares it.
+  uint64_t generation = 0;
 };
 
 namespace {
 
 thread_local std::string g_last_error;
+
+// Source of handle generations: unique over the process, so a handle created at a destroyed one's
+// address never repeats its generation.
+std::atomic<uint64_t> g_generation{1};
+
+void bump(moe_experts_s* h) { h->generation = g_generation.fetch_add(1, std::memory_order_relaxed); }
 
 moe_status_t fail(moe_status_t st, const char* fmt, ...) {
   char buf[512];
@@ -265,6 +277,7 @@ moe_status_t moe_experts_create(const moe_config_t* cfg, int32_t n, const uint8_
   if (!h) return fail(MOE_ERR_CUDA, "host allocation failed");
   h->cfg = *cfg;
   h->n = n;
+  bump(h);
   h->num_sms = sms;
   h->device = dev;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -322,7 +335,8 @@ moe_status_t moe_experts_set_router(moe_experts_t h, const float* router_w, cons
     h->router_split = nullptr;
     h->router_w32 = nullptr;
     h->router_bias = nullptr;
-    return MOE_OK;
+    bump(h);
+  return MOE_OK;
   }
   if (!router_w || !router_bias) return fail(MOE_ERR_INVALID_ARG, "router_w and router_bias go together");
   const int E = h->cfg.n_experts, d = h->cfg.d_model;
@@ -356,6 +370,7 @@ moe_status_t moe_experts_set_router(moe_experts_t h, const float* router_w, cons
            "router weight copy");
   MOE_CUDA(cudaMemcpyAsync(h->router_bias, router_bias, (size_t)E * sizeof(float), cudaMemcpyDeviceToDevice, s),
            "router bias copy");
+  bump(h);
   return MOE_OK;
 }
 
@@ -364,6 +379,7 @@ moe_status_t moe_experts_set_hash_table(moe_experts_t h, const int32_t* table, i
   if (table && V < 1) return fail(MOE_ERR_INVALID_ARG, "hash table needs V >= 1");
   h->hash_table = table;
   h->hash_V = table ? V : 0;
+  bump(h);
   return MOE_OK;
 }
 
@@ -380,6 +396,7 @@ moe_status_t moe_set_workspace(moe_experts_t h, void* ws, size_t bytes, int32_t 
   h->ws_base = ws;
   h->ws_bytes = bytes;
   h->ws_max_T = max_T;
+  bump(h);
   return MOE_OK;
 }
 
@@ -387,12 +404,14 @@ moe_status_t moe_experts_set_activation_format(moe_experts_t h, int32_t format) 
   if (!h) return fail(MOE_ERR_INVALID_ARG, "handle is NULL");
   if (format != MOE_ACT_MXFP8 && format != MOE_ACT_MXFP4) return fail(MOE_ERR_INVALID_ARG, "unknown activation format");
   h->act_fp4 = format == MOE_ACT_MXFP4 ? 1 : 0;
+  bump(h);
   return MOE_OK;
 }
 
 moe_status_t moe_set_wait_budget(moe_experts_t h, uint64_t budget_ns) {
   if (!h || budget_ns == 0) return fail(MOE_ERR_INVALID_ARG, "handle NULL or zero budget");
   h->budget_ns = budget_ns;
+  bump(h);
   return MOE_OK;
 }
 
@@ -577,6 +596,7 @@ moe_status_t moe_set_stage_events(moe_experts_t h, void* const* events, int32_t 
     for (int i = 0; i <= MOE_N_STAGES; ++i)
       if (!events[i]) return fail(MOE_ERR_INVALID_ARG, "event %d is NULL", i);
   h->stage_events = events;
+  bump(h);
   return MOE_OK;
 }
 
@@ -621,6 +641,7 @@ moe_status_t forward_impl(const moe_input_t* x, const float* router_w, const flo
   st = route_into(h, x, router_w, router_bias, h->ws.topk_ids, h->ws.topk_w, s, router_dispatch ? &sd : nullptr);
   if (st != MOE_OK) return st;
   h->last_T = T;
+  h->last_fwd_T = -1;
   mark_stage(h, 1, s);
   if (T == 0) {
     for (int i = 2; i <= MOE_N_STAGES; ++i) mark_stage(h, i, s);
@@ -645,6 +666,8 @@ moe_status_t forward_impl(const moe_input_t* x, const float* router_w, const flo
                           static_cast<const __nv_bfloat16*>(residual_bf16), static_cast<__nv_bfloat16*>(out_bf16), s),
            "combine");
   mark_stage(h, 5, s);
+  h->last_fwd_T = T;
+  h->last_fwd_shared = has_shared;
   return MOE_OK;
 }
 
@@ -653,6 +676,8 @@ int experts_d_model(moe_experts_t h) { return h ? h->cfg.d_model : 0; }
 int experts_has_hash_table(moe_experts_t h) { return h && h->hash_table ? 1 : 0; }
 
 int experts_has_resident_router(moe_experts_t h) { return h && h->router_split ? 1 : 0; }
+
+uint64_t experts_generation(moe_experts_t h) { return h ? h->generation : 0; }
 
 }  // namespace moe
 
@@ -682,9 +707,25 @@ moe_status_t moe_testing_read_h(moe_experts_t h, uint8_t* h_q, uint8_t* h_s, int
   return MOE_OK;
 }
 
+moe_status_t moe_testing_read_y32(moe_experts_t h, float* y32, int32_t* T, moe_stream_t stream) {
+  if (!h || !T) return fail(MOE_ERR_INVALID_ARG, "NULL argument");
+  if (!h->ws_base) return fail(MOE_ERR_WORKSPACE, "no workspace attached");
+  if (h->last_fwd_T < 0) return fail(MOE_ERR_INVALID_ARG, "no moe_forward on this handle since its last other call");
+  *T = h->last_fwd_T;
+  if (h->last_fwd_T == 0 || !y32) return MOE_OK;  // a query of the row count
+  if (!aligned(y32, 16)) return fail(MOE_ERR_INVALID_ARG, "y32 must be 16-byte aligned");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int Tl = h->last_fwd_T, k = h->cfg.top_k;
+  MOE_CUDA(launch_combine(h->ws.y_rows, h->ws.inv_pos, Tl, h->cfg.d_model, k, Tl * k, h->last_fwd_shared, nullptr,
+                          nullptr, s, y32),
+           "fp32 combine");
+  return MOE_OK;
+}
+
 moe_status_t moe_testing_stall_loads(moe_experts_t h, int32_t enable) {
   if (!h) return fail(MOE_ERR_INVALID_ARG, "handle is NULL");
   h->stall_loads = enable ? 1 : 0;
+  bump(h);
   return MOE_OK;
 }
 

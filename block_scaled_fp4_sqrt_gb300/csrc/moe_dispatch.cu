@@ -1,7 +1,8 @@
 // Token <-> expert dispatch and combine (the single-GPU form of the pypto page's "dispatch /
 // combine" around expert_routed / expert_shared, "MoE and output stages"):
 //
-//  * histogram:  per 32-token chunk, how many (token, slot) pairs go to each expert group;
+//  * histogram:  per 32-token chunk, how many (token, slot) pairs go to each expert group (a warp vote,
+//                match.any + popc, per routing slot);
 //  * scans:      per group, exclusive sums over its chunks (one block per group); over groups, row
 //                offsets, tile offsets and a device-side list of row tiles for the grouped GEMMs (one
 //                block, warp-shuffle scans; no host round trip);
@@ -28,7 +29,10 @@ __device__ __forceinline__ int clamp_id(int e, int E, int* status) {
   return e;
 }
 
-// one warp per 32-token chunk; chunk_hist[g][c] = number of (t, j) in chunk c with ids[t, j] = g
+// One warp per 32-token chunk; chunk_hist[g][c] = number of (t, j) in chunk c with ids[t, j] = g.
+// Warp-vote histogram: for each routing slot j, match.any gives every lane the set of lanes whose token
+// chose the same expert, and the lowest lane of each set adds the set's population count.  Within one
+// slot the adding lanes hold distinct experts, so the warp's private histogram needs no atomics.
 __global__ void histogram_kernel(const int32_t* __restrict__ ids, int T, int k, int E, int G, int n_chunks,
                                  int32_t* __restrict__ chunk_hist, int* status) {
   pdl_trigger();
@@ -41,8 +45,12 @@ __global__ void histogram_kernel(const int32_t* __restrict__ ids, int T, int k, 
   __syncwarp();
   if (chunk < n_chunks) {
     const int t = chunk * 32 + lane;
-    if (t < T)
-      for (int j = 0; j < k; ++j) atomicAdd(&h[clamp_id(ids[(size_t)t * k + j], E, status)], 1);
+    for (int j = 0; j < k; ++j) {
+      const int e = t < T ? clamp_id(ids[(size_t)t * k + j], E, status) : -1;
+      const unsigned peers = __match_any_sync(0xFFFFFFFFu, e);
+      if (e >= 0 && (peers & ((1u << lane) - 1u)) == 0u) h[e] += __popc(peers);
+      __syncwarp();
+    }
   }
   __syncwarp();
   if (chunk < n_chunks)
@@ -349,10 +357,11 @@ __global__ void __launch_bounds__(128) gather_kernel(
   }
 }
 
-// out[t, c] = bf16( sum_j Yr[inv_pos[t, j], c] + Yr[R + t, c] ), fp32 rows, 8 columns per thread
+// out[t, c] = bf16( sum_j Yr[inv_pos[t, j], c] + Yr[R + t, c] ), fp32 rows, 8 columns per thread.
+// F32OUT writes the same fp32 sum without the final rounding (the test hook moe_testing_read_y32).
+template <bool F32OUT>
 __global__ void combine_kernel(const float* __restrict__ y_rows, const int32_t* __restrict__ inv_pos, int T, int d,
-                               int k, int R, int has_shared, const __nv_bfloat16* residual,
-                               __nv_bfloat16* out) {
+                               int k, int R, int has_shared, const __nv_bfloat16* residual, void* out_) {
   pdl_trigger();
   pdl_wait();
   const int vec_per_row = d / 8;
@@ -413,11 +422,17 @@ __global__ void combine_kernel(const float* __restrict__ y_rows, const int32_t* 
       for (int j = 0; j < k; ++j) add_row(__ldg(&inv_pos[(size_t)t * k + j]));
       if (has_shared) add_row(R + t);
     }
-    uint4 o;
-    __nv_bfloat16* ov = reinterpret_cast<__nv_bfloat16*>(&o);
+    if (F32OUT) {
+      float4* dst = reinterpret_cast<float4*>(static_cast<float*>(out_) + (size_t)t * d) + 2 * c8;
+      dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    } else {
+      uint4 o;
+      __nv_bfloat16* ov = reinterpret_cast<__nv_bfloat16*>(&o);
 #pragma unroll
-    for (int q = 0; q < 8; ++q) ov[q] = __float2bfloat16_rn(acc[q]);
-    reinterpret_cast<uint4*>(out + (size_t)t * d)[c8] = o;
+      for (int q = 0; q < 8; ++q) ov[q] = __float2bfloat16_rn(acc[q]);
+      reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out_) + (size_t)t * d)[c8] = o;
+    }
   }
 }
 
@@ -470,13 +485,17 @@ cudaError_t launch_gather(const __nv_bfloat16* x, const int32_t* ids, const floa
 }
 
 cudaError_t launch_combine(const float* y_rows, const int32_t* inv_pos, int T, int d, int k, int R,
-                           int has_shared, const __nv_bfloat16* residual, __nv_bfloat16* out, cudaStream_t s) {
+                           int has_shared, const __nv_bfloat16* residual, __nv_bfloat16* out, cudaStream_t s,
+                           float* out_f32) {
   const size_t total = (size_t)T * (d / 8);
   int blocks = (int)((total + 255) / 256);
   if (blocks > 152 * 16) blocks = 152 * 16;
   if (blocks < 1) blocks = 1;
-  return launch_pdl(combine_kernel, dim3(blocks), dim3(256), 0, s, y_rows, inv_pos, T, d, k, R, has_shared, residual,
-                    out);
+  if (out_f32)
+    return launch_pdl(combine_kernel<true>, dim3(blocks), dim3(256), 0, s, y_rows, inv_pos, T, d, k, R, has_shared,
+                      residual, static_cast<void*>(out_f32));
+  return launch_pdl(combine_kernel<false>, dim3(blocks), dim3(256), 0, s, y_rows, inv_pos, T, d, k, R, has_shared,
+                    residual, static_cast<void*>(out));
 }
 
 }  // namespace moe

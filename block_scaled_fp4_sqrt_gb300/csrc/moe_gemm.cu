@@ -435,13 +435,12 @@ template <int STAGES, int AROWS, int EPI, bool FP4>
 cudaError_t launch_shape(const CUtensorMap& w, const CUtensorMap& w_sh, const CUtensorMap& act,
                          const CUtensorMap& act_small, const GemmArgs& a, int num_sms, cudaStream_t s) {
   using C = Cfg<STAGES, AROWS, EPI, FP4>;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(grouped_mx_gemm_kernel<STAGES, AROWS, EPI, FP4>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static PerDeviceOnce smem_optin;
+  const cudaError_t e = smem_optin.run([] {
+    return cudaFuncSetAttribute(grouped_mx_gemm_kernel<STAGES, AROWS, EPI, FP4>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+  });
+  if (e != cudaSuccess) return e;
   return launch_pdl(grouped_mx_gemm_kernel<STAGES, AROWS, EPI, FP4>, dim3(num_sms), dim3(kThreads), C::kSmem, s, w,
                     w_sh, act, act_small, a);
 }

@@ -7,6 +7,7 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <utility>
 
 #include "moe.h"
@@ -78,6 +79,8 @@ moe_status_t forward_impl(const moe_input_t* x, const float* router_w, const flo
 int experts_d_model(moe_experts_t h);
 int experts_has_hash_table(moe_experts_t h);
 int experts_has_resident_router(moe_experts_t h);
+// Changes whenever a setter changes what the handle's launches depend on (unique over the process).
+uint64_t experts_generation(moe_experts_t h);
 
 // Launch with programmatic stream serialization: the kernel may be scheduled before the previous kernel
 // in the stream has finished (it must call pdl_wait() before touching global memory, see moe_device.cuh).
@@ -95,6 +98,27 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
+
+// Runs a set-up step once per device: kernel attributes such as the dynamic shared-memory opt-in and the
+// non-portable cluster size belong to the current device, so a process that drives several GPUs must
+// set them on each.  fn() returns cudaError_t; a failed step is retried on the next call.
+class PerDeviceOnce {
+ public:
+  template <typename F>
+  cudaError_t run(F&& fn) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const bool tracked = dev >= 0 && dev < 64;
+    if (tracked && ((done_.load(std::memory_order_acquire) >> dev) & 1ull)) return cudaSuccess;
+    e = fn();
+    if (e == cudaSuccess && tracked) done_.fetch_or(1ull << dev, std::memory_order_acq_rel);
+    return e;
+  }
+
+ private:
+  std::atomic<unsigned long long> done_{0};
+};
 
 size_t workspace_layout(int max_T, int d, int f, int E, int k, Workspace* ws, void* base);
 
@@ -187,7 +211,9 @@ cudaError_t launch_gemm_down(const CUtensorMap& w_routed, const CUtensorMap& w_s
                              uint64_t wait_budget_ns, int stall_loads, int tile_rows, int act_fp4, int num_sms,
                              cudaStream_t s);
 
+// out_f32 non-NULL: the fp32 sums go there instead, without the rounding to bf16 (out is then unused).
 cudaError_t launch_combine(const float* y_rows, const int32_t* inv_pos, int T, int d, int k, int R, int has_shared,
-                           const __nv_bfloat16* residual, __nv_bfloat16* out, cudaStream_t s);
+                           const __nv_bfloat16* residual, __nv_bfloat16* out, cudaStream_t s,
+                           float* out_f32 = nullptr);
 
 }  // namespace moe

@@ -1,11 +1,10 @@
 // moe_route_noalloc: the learned router (fp32 logits, sqrt-softplus scores, biased top-k) for callers
-// that cannot allocate device memory.  Some callers can't call cudaMalloc: code that runs while a
-// stream is being captured into a CUDA graph (an allocation there is not allowed in the default
-// capture mode), plug-ins whose host framework owns every device allocation, and latency-critical
-// paths that must never enter the allocator.  They have no expert handle and no workspace, so the
-// router's split-K partial sums live in a fixed array in the library's own device memory instead.
+// that cannot allocate device memory.  Some callers can't call cudaMalloc: plug-ins whose host
+// framework owns every device allocation, and latency-critical paths that must never enter the
+// allocator (an allocation may synchronise the device or wait on a lock).  They have no expert handle
+// and no workspace, so the router's split-K partial sums live in a fixed array in the library's own
+// device memory instead.
 #include <cstdio>
-#include <mutex>
 
 #include "moe.h"
 #include "moe_internal.h"
@@ -17,25 +16,16 @@ namespace {
 constexpr size_t kScratchFloats = size_t(1) << 20;
 static __device__ __align__(256) float g_router_scratch[kScratchFloats];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_mutex;
-float* g_scratch_addr[kMaxDevices] = {};
-
-// Device address of the scratch array on the current device, looked up once per device.  The name
-// g_router_scratch in host code is only a host-side stand-in: a kernel must receive this address.
+// Device address of the scratch array in the current context.  The name g_router_scratch in host code
+// is only a host-side stand-in: a kernel must receive this address.  It is looked up on every call
+// rather than cached: the lookup is a host-side table read once the library's device code is loaded,
+// and a cached address would go stale when the context is destroyed and recreated (cudaDeviceReset,
+// or a released primary context), which may load the device code at another address.
 cudaError_t scratch_on_current_device(float** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_router_scratch);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(g_mutex);
-  if (!g_scratch_addr[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_router_scratch);
-    if (e != cudaSuccess) return e;
-    g_scratch_addr[dev] = static_cast<float*>(p);
-  }
-  *out = g_scratch_addr[dev];
+  *out = static_cast<float*>(p);
   return cudaSuccess;
 }
 

@@ -435,18 +435,20 @@ int router_tc_epad(int E) { return (E + kRN - 1) / kRN * kRN; }
 // (a non-portable size; checked once with the occupancy query) and 8 otherwise.
 template <int S>
 static cudaError_t configure_fused() {
-  static bool done = false;
-  if (done) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(router_fused_kernel<S>, cudaFuncAttributeMaxDynamicSharedMemorySize, kRSmem);
-  if (e == cudaSuccess && S > 8)
-    e = cudaFuncSetAttribute(router_fused_kernel<S>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-  done = e == cudaSuccess;
-  return e;
+  static PerDeviceOnce once;
+  return once.run([] {
+    cudaError_t e = cudaFuncSetAttribute(router_fused_kernel<S>, cudaFuncAttributeMaxDynamicSharedMemorySize, kRSmem);
+    if (e == cudaSuccess && S > 8)
+      e = cudaFuncSetAttribute(router_fused_kernel<S>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    return e;
+  });
 }
 
 static int max_fused_cluster() {
-  static int cached = 0;
-  if (cached) return cached;
+  static std::atomic<int> cached[64];  // per device; 0 = not queried yet
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 8;
+  if (const int c = cached[dev].load(std::memory_order_relaxed)) return c;
   int best = 8;
   if (configure_fused<16>() == cudaSuccess) {
     cudaLaunchConfig_t cfg = {};
@@ -464,8 +466,8 @@ static int max_fused_cluster() {
     if (cudaOccupancyMaxActiveClusters(&n, router_fused_kernel<16>, &cfg) == cudaSuccess && n >= 1) best = 16;
   }
   (void)cudaGetLastError();
-  cached = best;
-  return cached;
+  cached[dev].store(best, std::memory_order_relaxed);
+  return best;
 }
 
 int router_fused_split(int T, int d) {
@@ -522,12 +524,10 @@ cudaError_t launch_split_router(const float* w, int E, int d, __nv_bfloat16* out
 
 cudaError_t launch_router_tc(const CUtensorMap& tm_x, const CUtensorMap& tm_w, int T, int E, int d, int split,
                              float* partial, int* status, uint64_t budget_ns, cudaStream_t s) {
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(router_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kRSmem);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static PerDeviceOnce smem_optin;
+  const cudaError_t e =
+      smem_optin.run([] { return cudaFuncSetAttribute(router_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kRSmem); });
+  if (e != cudaSuccess) return e;
   RouterArgs a{partial, T, E, router_tc_epad(E), d, d / split, status, budget_ns};
   dim3 grid((T + kRM - 1) / kRM, a.Epad / kRN, split);
   return launch_pdl(router_tc_kernel, grid, dim3(192), kRSmem, s, tm_x, tm_w, a);

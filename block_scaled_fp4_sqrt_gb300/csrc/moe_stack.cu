@@ -8,10 +8,12 @@
 // ping-pong between the caller's output and scratch so that the last layer writes the output.
 //
 // With graph mode on, the first call (and any call whose pointers or batch size differ from the
-// captured ones) records every layer's launches on a private stream into one CUDA graph; later calls
-// replay it on the caller's stream, which removes the host work of L x 9 launches and their tensor-map
-// encodes.  The captured kernels read the buffers named at capture time, whose contents may change
-// freely between calls.
+// captured ones, or after a setter changed a layer handle) records every layer's launches on a private
+// stream into one CUDA graph; later calls replay it on the caller's stream, which removes the host work
+// of L x 9 launches and their tensor-map encodes.  The captured kernels read the buffers named at
+// capture time, whose contents may change freely between calls.  A handle setter (a new workspace,
+// router, hash table, activation format, wait budget, stage events) changes the handle's generation,
+// which is part of the graph's key, so a replay never reaches a buffer the handle no longer uses.
 #include <vector>
 
 #include "moe_internal.h"
@@ -28,6 +30,7 @@ struct moe_stack_s {
   void* key_out = nullptr;
   void* key_scratch = nullptr;
   int32_t key_T = -1;
+  std::vector<uint64_t> key_gen;  // generations of every layer's routed and shared handles
 };
 
 namespace {
@@ -51,6 +54,16 @@ moe_status_t run_layers(moe_stack_s* st, const moe_input_t* x, void* out, void* 
     in = dst;
   }
   return MOE_OK;
+}
+
+std::vector<uint64_t> generations(const moe_stack_s* st) {
+  std::vector<uint64_t> g;
+  g.reserve(2 * st->layers.size());
+  for (const moe_stack_layer_t& ly : st->layers) {
+    g.push_back(moe::experts_generation(ly.experts));
+    g.push_back(moe::experts_generation(ly.shared));
+  }
+  return g;
 }
 
 }  // namespace
@@ -96,8 +109,9 @@ moe_status_t moe_stack_forward(moe_stack_t st, const moe_input_t* x, void* out_b
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (!st->use_graph) return run_layers(st, x, out_bf16, scratch_bf16, s);
 
+  std::vector<uint64_t> gen = generations(st);
   const bool hit = st->exec && st->key_x == x->x_bf16 && st->key_tok == x->token_ids && st->key_out == out_bf16 &&
-                   st->key_scratch == scratch_bf16 && st->key_T == x->T;
+                   st->key_scratch == scratch_bf16 && st->key_T == x->T && st->key_gen == gen;
   if (!hit) {
     if (!st->capture && cudaStreamCreateWithFlags(&st->capture, cudaStreamNonBlocking) != cudaSuccess)
       return stack_fail(MOE_ERR_CUDA, "could not create the capture stream");
@@ -127,6 +141,7 @@ moe_status_t moe_stack_forward(moe_stack_t st, const moe_input_t* x, void* out_b
     st->key_out = out_bf16;
     st->key_scratch = scratch_bf16;
     st->key_T = x->T;
+    st->key_gen = std::move(gen);
     // the direct pass ran on the capture stream: order the caller's stream after it
     if (cudaStreamSynchronize(st->capture) != cudaSuccess) return stack_fail(MOE_ERR_CUDA, "capture stream failed");
     return MOE_OK;

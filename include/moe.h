@@ -91,6 +91,11 @@ typedef struct {
  * buffers 4-byte aligned.  A routed set uses n = cfg->n_experts; a shared expert is a set with n = 1.
  * Errors: MOE_ERR_INVALID_ARG (null / misaligned / n < 1), MOE_ERR_UNSUPPORTED (shape or GPU),
  * MOE_ERR_CUDA.  *out is NULL on error.
+ * Passages: the expert FFN runs as a fused dequantisation + GEMM over the MXFP4 payload, 13.4 MB per
+ * expert (FaStar README, "Features" and "Expert virtual memory"); the experts are FP4 with one E8M0
+ * scale per 32 weights (model card, "Preprocessing" and its glossary; TensorSharp page, "Getting a
+ * drafter"); a layer holds experts.{0..255}.{w1,w2,w3} and shared_experts.{w1,w2,w3} (ds4 issue,
+ * "Resolved questions").
  */
 MOE_API moe_status_t moe_experts_create(const moe_config_t* cfg, int32_t n, const uint8_t* w13_fp4, const uint8_t* w13_e8m0,
                                 const uint8_t* w2_fp4, const uint8_t* w2_e8m0, moe_stream_t stream,
@@ -152,6 +157,11 @@ MOE_API moe_status_t moe_set_workspace(moe_experts_t experts, void* workspace, s
  * Learned layer with router_w = router_bias = NULL: the handle's resident router (moe_experts_set_router).
  * Outputs: topk_ids int32 [T, top_k] ascending per row, topk_w fp32 [T, top_k].
  * Uses the workspace.  Errors: MOE_ERR_INVALID_ARG, MOE_ERR_WORKSPACE, MOE_ERR_CUDA.
+ * Passages: routed experts chosen by sqrt-softplus routing, with hash routing on hash layers
+ * (TensorSharp page, "How TensorSharp runs it"); top-6 of 256, route_scale 1.5, hash routing over the
+ * first layers (model card, "Speeds, Sizes, Times"); the router is ffn.gate.weight with ffn.gate.bias
+ * (ds4 issue, "Resolved questions").  The bias steering selection only, the normalisation over the
+ * selected scores and the ascending id order are readings of those passages.
  */
 MOE_API moe_status_t moe_route(moe_experts_t experts, const moe_input_t* x, const float* router_w, const float* router_bias,
                        int32_t* topk_ids, float* topk_w, moe_stream_t stream);
@@ -167,6 +177,10 @@ MOE_API moe_status_t moe_route(moe_experts_t experts, const moe_input_t* x, cons
  * a_q / a_s may be NULL (not written).  Uses the workspace.  Ids outside [0, E) are reported by
  * moe_check and treated as expert 0.  With MOE_ACT_MXFP4 set on the handle a_q is [R, d_model/2]
  * packed E2M1 codes and the a_s exponent is floor(log2(amax)) - 2.
+ * Passage: the gate's top-6 routing feeds a dispatch to the routed expert FFNs and a combine back
+ * (pypto page, "MoE and output stages"), here one GPU's permutation instead of an EP collective.  The
+ * MXFP8 element rules (E4M3 round-to-nearest-even, saturating; E8M0 = floor(log2 amax) - 8) are the OCP
+ * MX ones the layer contract names; the pages' own kernels quantise activations per token to INT8.
  */
 MOE_API moe_status_t moe_permute(moe_experts_t experts, const moe_input_t* x, const int32_t* topk_ids, int32_t* counts,
                          int32_t* offsets, int32_t* perm_tok, int32_t* inv_pos, uint8_t* a_q, uint8_t* a_s,
@@ -181,6 +195,10 @@ MOE_API moe_status_t moe_permute(moe_experts_t experts, const moe_input_t* x, co
  * [n_rows, d_model].  Uses the workspace of the handle (n_rows <= max_T * (top_k + 1)).  With
  * MOE_ACT_MXFP4 set on the handle a_q is [n_rows, d_model/2] packed E2M1 codes and h is quantised to
  * MXFP4 instead (q8 becomes q4).
+ * Passages: the expert FFN is a fused dequantisation + GEMM (FaStar README, "Features"); the linear
+ * layers end in a SiLU-times-up op with clamp (SiLUMulClamp, TensorSharp page, "How TensorSharp runs it")
+ * with swiglu_limit = 10 (model card, "Model Architecture and Objective"); w1 = gate, w3 = up, w2 =
+ * down (ds4 issue, "Resolved questions").
  */
 MOE_API moe_status_t moe_expert_ffn(moe_experts_t experts, int32_t n_rows, const int32_t* offsets, const uint8_t* a_q,
                             const uint8_t* a_s, const float* row_w, void* y_bf16, moe_stream_t stream);
@@ -191,6 +209,11 @@ MOE_API moe_status_t moe_expert_ffn(moe_experts_t experts, int32_t n_rows, const
  * moe_route (hash layers: router_w = router_bias = NULL).  The routing of the last call stays in
  * the workspace (moe_get_routing).  Everything stays on the device: the call never waits for the
  * GPU and copies nothing to or from the host.
+ * Passages: gate -> top-6 -> dispatch -> routed and shared expert FFNs -> combine (pypto page, "MoE and
+ * output stages"; 64 requests x 8 verify rows = 512 rows per step, its "Deployment configuration"); the
+ * combine is a weighted-sum scatter epilogue after the expert FFNs (moe_scatter_add, TensorSharp page,
+ * "DSpark and MoE CPU offload together" and "Fitting the model"); one always-on shared expert (model
+ * card, "Speeds, Sizes, Times").
  */
 MOE_API moe_status_t moe_forward(const moe_input_t* x, const float* router_w, const float* router_bias,
                          moe_experts_t experts, moe_experts_t shared, void* out_bf16, moe_stream_t stream);
@@ -218,18 +241,19 @@ MOE_API moe_status_t moe_check(moe_experts_t experts, moe_stream_t stream);
 MOE_API moe_status_t moe_set_wait_budget(moe_experts_t experts, uint64_t budget_ns);
 
 /*
- * Learned router that allocates nothing -- for callers that can't call cudaMalloc: code running
- * while a stream is captured into a CUDA graph (allocation is not allowed there in the default capture
- * mode), plug-ins whose host framework owns all device memory, and latency-critical paths that must
- * not enter an allocator.  It needs no expert handle and no workspace.  (The pages have no
- * counterpart; it is the same router as moe_route.)
+ * Learned router that allocates nothing -- for callers that can't call cudaMalloc: plug-ins whose host
+ * framework owns all device memory, and latency-critical paths that must not enter an allocator (an
+ * allocation may synchronise the device or take a lock).  It needs no expert handle and no workspace.
+ * (The pages have no counterpart; it is the same router as moe_route.)
  * Computes exactly what moe_route computes for a learned (not hash) layer: cfg gives d_model,
  * n_experts (<= 512), top_k and route_scale; x, router_w, router_bias, topk_ids, topk_w as there.
  * Its split-K partial sums live in one fixed 4 MiB array of library device memory (1,048,576 fp32),
  * which every GPU that loads the library holds until the process exits; batches with
  * T * n_experts > 1,048,576 (T > 4096 at 256 experts) are rejected with MOE_ERR_WORKSPACE.
- * The first call on a device looks up that array's device address (with that device current); make
- * that first call before any stream capture.  All calls share the array and it keeps the last call's
+ * Every call looks up that array's device address in the current context (so the address follows a
+ * context that was destroyed and recreated); the first call on a device also loads the library's
+ * device code there, so make that first call before any stream capture.  All calls share the array
+ * and it keeps the last call's
  * contents (every call overwrites what it reads), so calls that overlap on the GPU -- on different
  * streams, or from several host threads -- race: order them.
  */
@@ -267,9 +291,12 @@ MOE_API moe_status_t moe_route_noalloc(const moe_config_t* cfg, const moe_input_
  *   x, out and scratch must be distinct and 16-byte aligned.
  *   Without graph mode: enqueues L moe_forward-equivalent launch sequences on the stream.
  *   With graph mode:
- *     - On the first call, or when x, token_ids, out, scratch or T differ from the captured ones, it runs
- *       the layers once directly on a private stream, captures them into a graph there, and synchronises.
- *       The call returns with the result already in out.
+ *     - On the first call, or when x, token_ids, out, scratch or T differ from the captured ones, or when
+ *       a setter (moe_set_workspace, moe_experts_set_router, moe_experts_set_hash_table,
+ *       moe_experts_set_activation_format, moe_set_wait_budget, moe_set_stage_events) has been called on
+ *       one of the layers' handles since the capture, it runs the layers once directly on a private
+ *       stream, captures them into a graph there, and synchronises.  The call returns with the result
+ *       already in out.
  *     - Otherwise it launches the cached graph on the stream.
  *   Device-side status is reported per layer handle by moe_check.  Host-side validation and CUDA errors
  *   are returned.

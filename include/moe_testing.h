@@ -37,6 +37,19 @@ MOE_API moe_status_t moe_testing_read_h(moe_experts_t experts, uint8_t* h_q, uin
                                         moe_stream_t stream);
 
 /*
+ * Reads back the layer output of the last moe_forward on this handle before its rounding to bf16:
+ * y32 fp32 [T, d_model] (device, 16-byte aligned, sized by the caller) receives, per token, the same
+ * fixed-order fp32 sum that the combine rounds once to bf16 (routing slots 0..top_k-1, then the shared
+ * row; a stack layer's residual is not included).  *T receives the forward's row count; y32 = NULL
+ * asks for it only.  It re-runs the sum from the expert rows the forward left in the workspace, so it
+ * is valid until the next moe_forward on the handle.  Tests use it to check the arithmetic before the
+ * output rounding against the layer's tolerance, and that the bf16 output is exactly that sum rounded
+ * to nearest even.  Asynchronous on `stream`.  Errors: MOE_ERR_INVALID_ARG (NULL handle or T, no
+ * forward since the last one started, misaligned y32), MOE_ERR_WORKSPACE, MOE_ERR_CUDA.
+ */
+MOE_API moe_status_t moe_testing_read_y32(moe_experts_t experts, float* y32, int32_t* T, moe_stream_t stream);
+
+/*
  * Measures the throughput of the block-scaled MMA the grouped GEMMs are built on (tcgen05.mma
  * kind::mxf8f6f4.block_scale.scale_vec::1X, E4M3 activations x E2M1 weights with E8M0 scales,
  * M = 128, N = 256, K = 32) on the current device: one CTA per SM issues n_stages x 4 MMAs back to

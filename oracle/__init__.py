@@ -62,6 +62,7 @@ def _lib():
                                      i32]
         L.orc_layer.argtypes = [vp, i64, i64, i64, i64, i64, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, dbl, vp, i64, i32,
                                 vp, i32, i32]
+        L.orc_layer_h.argtypes = L.orc_layer.argtypes + [vp, vp, vp]
         _LIB = L
     return _LIB
 
@@ -302,10 +303,13 @@ def down_from_h(hq, hs, w2, s2, act: str = "mxfp8") -> np.ndarray:
 
 
 def layer(x_bf16, ids, wts, experts: "synth.ExpertWeights", shared: "synth.ExpertWeights | None",
-          limit: float = 10.0, tokens=None, mode: int = 1, act: str = "mxfp8"):
+          limit: float = 10.0, tokens=None, mode: int = 1, act: str = "mxfp8", want_h: bool = False):
     """y fp64 [n_sel, d] for the listed tokens (None: all), given the routing (ids, wts).
     mode 1 goes through the permutation; mode 0 evaluates each (token, expert) pair directly.
-    act: the activation format x and h are quantised to ("mxfp8", or "mxfp4" for the FP4 variant)."""
+    act: the activation format x and h are quantised to ("mxfp8", or "mxfp4" for the FP4 variant).
+    want_h: also return the h each (token, slot) row computed -- codes [n_sel, k+1, f] (or f/2 packed
+    with mxfp4), scales [n_sel, k+1, f/32] and h before quantisation fp64 [n_sel, k+1, f], slot k being
+    the shared expert (zeros without one) -- as (y, hq, hs, hpre)."""
     x = _c(x_bf16, np.uint16)
     T, d = x.shape
     ids = _c(ids, np.int32)
@@ -318,9 +322,16 @@ def layer(x_bf16, ids, wts, experts: "synth.ExpertWeights", shared: "synth.Exper
     y = np.empty((n_sel, d), dtype=np.float64)
     sh = [None] * 4 if shared is None else [_c(a, np.uint8) for a in (shared.w13, shared.s13, shared.w2, shared.s2)]
     ex = [_c(a, np.uint8) for a in (experts.w13, experts.s13, experts.w2, experts.s2)]
-    _lib().orc_layer(_p(x), T, d, f, E, k, _p(ids), _p(wts), *(_p(a) for a in ex), *(_p(a) for a in sh), limit,
-                     _p(tok), n_sel, mode, _p(y), 0, _act(act))
-    return y
+    if not want_h:
+        _lib().orc_layer(_p(x), T, d, f, E, k, _p(ids), _p(wts), *(_p(a) for a in ex), *(_p(a) for a in sh), limit,
+                         _p(tok), n_sel, mode, _p(y), 0, _act(act))
+        return y
+    hq = np.zeros((n_sel, k + 1, act_row_bytes(act, f)), dtype=np.uint8)
+    hs = np.zeros((n_sel, k + 1, f // 32), dtype=np.uint8)
+    hpre = np.zeros((n_sel, k + 1, f), dtype=np.float64)
+    _lib().orc_layer_h(_p(x), T, d, f, E, k, _p(ids), _p(wts), *(_p(a) for a in ex), *(_p(a) for a in sh), limit,
+                       _p(tok), n_sel, mode, _p(y), 0, _act(act), _p(hq), _p(hs), _p(hpre))
+    return y, hq, hs, hpre
 
 
 def route_inputs(inp: "synth.LayerInputs"):

@@ -23,7 +23,7 @@
 // saturation, E8M0 = floor(log2 amax) - emax) follow the OCP Microscaling Formats (MX)
 // v1.0 specification, as the layer's contract requires.
 //
-// Readings where the pages are silent (each listed in the design notes):
+// Readings taken where the pages are silent:
 //  * selection uses score + bias, the weights use the unbiased score, normalised over
 //    the k selected experts and multiplied by route_scale; ids are reported ascending;
 //  * gate clamped from above at L, up clamped to [-L, L], h = silu(gate) * up;
@@ -452,10 +452,19 @@ void orc_expert_ffn(int64_t n_rows, int64_t n_groups, const int32_t* offsets, co
 // given (ids/wts from orc_route or orc_hash_route).  mode 0: dense per token (each (t, j) pair
 // evaluated directly); mode 1: through the permutation (rows in expert-major order, then a combine).
 // y_out is [n_sel, d] in the order of `tokens`.  Shared expert pointers may be null.
-void orc_layer(const uint16_t* x, int64_t T, int64_t d, int64_t f, int64_t E, int64_t k, const int32_t* ids,
-               const double* wts, const uint8_t* w13, const uint8_t* s13, const uint8_t* w2, const uint8_t* s2,
-               const uint8_t* sh_w13, const uint8_t* sh_s13, const uint8_t* sh_w2, const uint8_t* sh_s2,
-               double limit, const int32_t* tokens, int64_t n_sel, int mode, double* y_out, int threads, int act) {
+// The layer, optionally also returning what each (selected token, slot) row computed on the way: the h
+// codes, scales and h before quantisation, [n_sel][k + 1][...] with slot k the shared expert (left
+// untouched without one).  hq / hs / hpre may be null.
+void orc_layer_h(const uint16_t* x, int64_t T, int64_t d, int64_t f, int64_t E, int64_t k, const int32_t* ids,
+                 const double* wts, const uint8_t* w13, const uint8_t* s13, const uint8_t* w2, const uint8_t* s2,
+                 const uint8_t* sh_w13, const uint8_t* sh_s13, const uint8_t* sh_w2, const uint8_t* sh_s2,
+                 double limit, const int32_t* tokens, int64_t n_sel, int mode, double* y_out, int threads, int act,
+                 uint8_t* hq_out, uint8_t* hs_out, double* hpre_out) {
+  const int64_t hb = act_row_bytes(act, f);
+  // slot (i, j) of the optional h outputs
+  auto hq_at = [&](int64_t i, int64_t j) { return hq_out ? hq_out + (i * (k + 1) + j) * hb : nullptr; };
+  auto hs_at = [&](int64_t i, int64_t j) { return hs_out ? hs_out + (i * (k + 1) + j) * (f / 32) : nullptr; };
+  auto hp_at = [&](int64_t i, int64_t j) { return hpre_out ? hpre_out + (i * (k + 1) + j) * f : nullptr; };
   if (!tokens) n_sel = T;
   auto tok_of = [&](int64_t i) -> int64_t { return tokens ? tokens[i] : i; };
   // activations of the selected tokens (MXFP8, or MXFP4 for the FP4 variant)
@@ -477,7 +486,8 @@ void orc_layer(const uint16_t* x, int64_t T, int64_t d, int64_t f, int64_t E, in
     Expert sh{sh_w13, sh_s13, sh_w2, sh_s2};
     parallel_for(n_sel, threads, [&](int64_t lo, int64_t hi) {
       for (int64_t i = lo; i < hi; ++i)
-        expert_row(&q[i * ab], &s[i * (d / 32)], d, f, sh, limit, &ysh[i * d], nullptr, nullptr, nullptr, act);
+        expert_row(&q[i * ab], &s[i * (d / 32)], d, f, sh, limit, &ysh[i * d], hq_at(i, k), hs_at(i, k), hp_at(i, k),
+                   act);
     });
   }
   if (mode == 0) {
@@ -489,7 +499,8 @@ void orc_layer(const uint16_t* x, int64_t T, int64_t d, int64_t f, int64_t E, in
         for (int64_t o = 0; o < d; ++o) y[o] = 0.0;
         for (int64_t j = 0; j < k; ++j) {
           Expert ex = expert_at(w13, s13, w2, s2, ids[t * k + j], d, f);
-          expert_row(&q[i * ab], &s[i * (d / 32)], d, f, ex, limit, ye.data(), nullptr, nullptr, nullptr, act);
+          expert_row(&q[i * ab], &s[i * (d / 32)], d, f, ex, limit, ye.data(), hq_at(i, j), hs_at(i, j), hp_at(i, j),
+                     act);
           for (int64_t o = 0; o < d; ++o) y[o] += wts[t * k + j] * ye[o];
         }
         for (int64_t o = 0; o < d; ++o) y[o] += ysh[i * d + o];
@@ -505,13 +516,18 @@ void orc_layer(const uint16_t* x, int64_t T, int64_t d, int64_t f, int64_t E, in
   orc_permute(sel_ids.data(), n_sel, k, E, counts.data(), offsets.data(), perm.data(), inv.data());
   int64_t R = n_sel * k;
   std::vector<double> yr((size_t)R * d);
+  std::vector<int32_t> slot_of((size_t)R);  // routing slot j of row r (inv[i * k + j] = r)
+  for (int64_t i = 0; i < n_sel; ++i)
+    for (int64_t j = 0; j < k; ++j) slot_of[inv[i * k + j]] = (int32_t)j;
   parallel_for(R, threads, [&](int64_t lo, int64_t hi) {
     for (int64_t r = lo; r < hi; ++r) {
       int64_t e = 0;
       while (!(offsets[e] <= r && r < offsets[e + 1])) ++e;
       Expert ex = expert_at(w13, s13, w2, s2, e, d, f);
       int64_t i = perm[r];
-      expert_row(&q[i * ab], &s[i * (d / 32)], d, f, ex, limit, &yr[r * d], nullptr, nullptr, nullptr, act);
+      const int64_t j = slot_of[r];
+      expert_row(&q[i * ab], &s[i * (d / 32)], d, f, ex, limit, &yr[r * d], hq_at(i, j), hs_at(i, j), hp_at(i, j),
+                 act);
     }
   });
   for (int64_t i = 0; i < n_sel; ++i) {
@@ -524,6 +540,14 @@ void orc_layer(const uint16_t* x, int64_t T, int64_t d, int64_t f, int64_t E, in
     }
     for (int64_t o = 0; o < d; ++o) y[o] += ysh[i * d + o];
   }
+}
+
+void orc_layer(const uint16_t* x, int64_t T, int64_t d, int64_t f, int64_t E, int64_t k, const int32_t* ids,
+               const double* wts, const uint8_t* w13, const uint8_t* s13, const uint8_t* w2, const uint8_t* s2,
+               const uint8_t* sh_w13, const uint8_t* sh_s13, const uint8_t* sh_w2, const uint8_t* sh_s2,
+               double limit, const int32_t* tokens, int64_t n_sel, int mode, double* y_out, int threads, int act) {
+  orc_layer_h(x, T, d, f, E, k, ids, wts, w13, s13, w2, s2, sh_w13, sh_s13, sh_w2, sh_s2, limit, tokens, n_sel, mode,
+              y_out, threads, act, nullptr, nullptr, nullptr);
 }
 
 }  // extern "C"

@@ -193,11 +193,15 @@ class LayerInputs:
 
 
 def gen_layer(wl: Workload, seed: int = 0, attempts: np.ndarray | None = None, with_shared: bool = True,
-              threads: int | None = None) -> LayerInputs:
+              threads: int | None = None, experts: ExpertWeights | None = None) -> LayerInputs:
     """All inputs of one layer forward.  The router (or hash table) is drawn even when a test later
-    replaces x rows through ``attempts``; weights never depend on x."""
+    replaces x rows through ``attempts``; weights never depend on x.  ``experts``: routed weights already
+    drawn for the same (seed, E, d, f), which are then reused instead of drawn again."""
     x = gen_x(seed, wl.T, wl.d, attempts, threads=threads)
-    experts = gen_experts(seed, wl.E, wl.d, wl.f, shared=False, threads=threads)
+    if experts is None:
+        experts = gen_experts(seed, wl.E, wl.d, wl.f, shared=False, threads=threads)
+    elif experts.w13.shape != (wl.E, 2 * wl.f, wl.d // 2):
+        raise ValueError("reused expert weights do not match the workload's shape")
     shared = gen_experts(seed, 1, wl.d, wl.f, shared=True, threads=threads) if with_shared else None
     if wl.hashed:
         tok = gen_token_ids(seed, wl.T, wl.hash_vocab)

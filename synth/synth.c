@@ -13,9 +13,11 @@
  *
  * Expert weights are produced directly in MXFP4 form (E2M1 codes + E8M0 scale bytes):
  * no quantiser lives here.  The code distribution is a fixed categorical law chosen
- * to look like N(0, 1/d) values after per-32 MX quantisation (derivation in the
- * design notes); the scale byte per block is 127 + e0 or 127 + e0 - 1 with
- * e0 = floor(log2(2.2 / sqrt(d))) - 2.
+ * to look like N(0, 1/d) values after per-32 MX quantisation: the maximum of 32 such
+ * normals is about 2.2 / sqrt(d), which fixes the usual block exponent e0, and a block
+ * gets the next lower exponent with probability 0.22 (the share of blocks whose maximum
+ * falls below the power of two); the scale byte per block is 127 + e0 or 127 + e0 - 1
+ * with e0 = floor(log2(2.2 / sqrt(d))) - 2.
  *
  * Build: gcc -O2 -ffp-contract=off -fPIC -shared -pthread synth.c -o libsynth.so -lm
  */

@@ -1,10 +1,14 @@
 """Parity of the CUDA path (through the C ABI) with the fp64 oracle.
 
 Integer and byte results are compared bit for bit: expert ids, counts, offsets, the permutation and
-its inverse, the MXFP8 activation codes and scale bytes.  Floating-point results use the layer's
-tolerance (max |dy| <= 2e-2 rms, mean relative error <= 5e-3) and, for the routing weights, a bound
-derived from fp32 dot products.  Small workloads are compared element by element; the full-size
-workloads (in the configuration the benchmark times) on sampled tokens plus all integer outputs.
+its inverse, the MXFP8 activation codes and scale bytes.  The layer output is checked in two steps:
+the fp32 sums the combine rounds (read back with moe_testing_read_y32) against the layer's contract
+exactly as written (max |dy| <= 2e-2 rms, mean relative error <= 5e-3), and the bf16 output against
+those sums rounded to nearest even, bit for bit.  The MXFP8 h codes the down projection consumed are
+compared with the oracle's, code by code, except at rounding midpoints the two precisions may
+straddle.  Every token row is compared for the small workloads and for verify8, verify512 and
+hash512; at prefill8192 at least 512 tokens, chosen so that every 128-row tile of every expert group
+(the shared expert's included) holds a compared row, plus the bit-exact rounding check on all rows.
 """
 import numpy as np
 import pytest
@@ -13,7 +17,8 @@ import torch
 import oracle
 import synth
 
-from gpu_support import (TOL_WEIGHT_REL, WORKLOADS, assert_close, bf16_to_f64, case, device, x_to_device)
+from gpu_support import (BF16_HALF_ULP_REL, TOL_MAX_RMS, TOL_WEIGHT_REL, WORKLOADS, assert_close, assert_strict, bf16_to_f64, case, check_h8, device,
+                         forward_strict, gpu_h_by_slot, x_to_device)
 
 pytestmark = pytest.mark.gpu
 
@@ -69,37 +74,71 @@ def test_permute_parity(name):
     assert np.array_equal(out["a_s"].cpu().numpy(), s[perm])
 
 
+def _strict_layer_parity(wl, inp, ids_ref, wts_ref, layer, tokens=None, what=""):
+    """Forward the whole batch; for the listed tokens (None: all) check the fp32 sums strictly against the
+    oracle and the h codes of each token's k + 1 rows; the bf16 output is checked on every row."""
+    x = x_to_device(inp.x)
+    y, y32 = forward_strict(layer, x)
+    assert np.array_equal(layer.last_topk_ids().cpu().numpy(), ids_ref)
+    toks = np.arange(wl.T, dtype=np.int32) if tokens is None else np.asarray(tokens, dtype=np.int32)
+    y_ref, hq_ref, hs_ref, hpre = oracle.layer(inp.x, ids_ref, wts_ref, inp.experts, inp.shared, wl.swiglu_limit,
+                                               tokens=None if tokens is None else toks, want_h=True)
+    assert_strict(y32.cpu().numpy().astype(np.float64)[toks], y_ref, f"{what} fp32 sums")
+    hq, hs = (t.cpu().numpy() for t in layer.last_h())
+    _, _, _, inv = oracle.permute(ids_ref, wl.E)
+    hq_d, hs_d = gpu_h_by_slot(hq, hs, inv, toks, wl.T * wl.k)
+    f = wl.f
+    check_h8(hq_d.reshape(-1, f), hs_d.reshape(-1, f // 32), hq_ref.reshape(-1, f), hs_ref.reshape(-1, f // 32),
+             hpre.reshape(-1, f), f"{what} h")
+    return y
+
+
 @pytest.mark.parametrize("name", SMALL)
 def test_forward_elementwise(name):
     wl, inp, ids_ref, wts_ref, layer = case(name)
-    x = x_to_device(inp.x)
-    y = layer.forward(x)
-    torch.cuda.synchronize()
-    layer.check()
-    assert np.array_equal(layer.last_topk_ids().cpu().numpy(), ids_ref)
-    y_ref = oracle.layer(inp.x, ids_ref, wts_ref, inp.experts, inp.shared, wl.swiglu_limit)
-    assert_close(bf16_to_f64(y), y_ref, f"{name} forward")
+    _strict_layer_parity(wl, inp, ids_ref, wts_ref, layer, what=name)
 
 
-def _sample_tokens(T, n=24, seed=1):
+def tile_covering_tokens(ids, E, T, tile_rows=128, n_min=512, seed=1):
+    """Tokens such that every row tile of every expert group holds one of them: for each routed group,
+    one random row of each run of tile_rows rows in its permuted order (so every hot expert's tiles and
+    every cold expert), one token of each tile_rows-token run of the shared group, then random tokens up
+    to n_min; plus the first and the last token."""
     rng = np.random.default_rng(seed)
-    extra = rng.choice(T, size=min(n, T), replace=False)
-    return np.unique(np.concatenate([[0, T - 1], extra])).astype(np.int32)
+    counts, offsets, perm, _ = oracle.permute(ids, E)
+    picks = [0, T - 1]
+    for g in range(E):
+        for r0 in range(offsets[g], offsets[g + 1], tile_rows):
+            r1 = min(r0 + tile_rows, offsets[g + 1])
+            picks.append(int(perm[rng.integers(r0, r1)]))
+    for t0 in range(0, T, tile_rows):
+        picks.append(int(rng.integers(t0, min(t0 + tile_rows, T))))
+    toks = np.unique(picks)
+    if toks.size < n_min:
+        rest = np.setdiff1d(np.arange(T), toks)
+        toks = np.unique(np.concatenate([toks, rng.choice(rest, n_min - toks.size, replace=False)]))
+    return toks.astype(np.int32)
 
 
-@pytest.mark.parametrize("name", FULL)
-def test_forward_full_size_sampled(name):
+@pytest.mark.parametrize("name", ["verify8", "verify512", "hash512"])
+def test_forward_full_size_every_row(name):
+    """The decode-shape workloads in the configuration the benchmark times, every token row."""
     wl, inp, ids_ref, wts_ref, layer = case(name)
-    x = x_to_device(inp.x)
-    y = layer.forward(x)
+    y = _strict_layer_parity(wl, inp, ids_ref, wts_ref, layer, what=name)
+    y2 = layer.forward(x_to_device(inp.x))
     torch.cuda.synchronize()
-    layer.check()
-    assert np.array_equal(layer.last_topk_ids().cpu().numpy(), ids_ref)
-    toks = _sample_tokens(wl.T)
-    y_ref = oracle.layer(inp.x, ids_ref, wts_ref, inp.experts, inp.shared, wl.swiglu_limit, tokens=toks)
-    assert_close(bf16_to_f64(y)[toks], y_ref, f"{name} forward (tokens {toks.tolist()})")
-    # every output row is finite and the whole output repeats bit for bit on a second call
-    y2 = layer.forward(x)
+    assert torch.equal(y, y2)  # repeatable bit for bit
+
+
+def test_forward_prefill_tile_covering_rows():
+    """prefill8192 (26 hot experts with thousands of rows, cold experts with one or a few, 8192 shared
+    rows): at least 512 tokens covering every 128-row tile of every group, compared strictly; the bf16
+    rounding is checked on all 8192 rows."""
+    wl, inp, ids_ref, wts_ref, layer = case("prefill8192")
+    toks = tile_covering_tokens(ids_ref, wl.E, wl.T)
+    assert toks.size >= 512
+    y = _strict_layer_parity(wl, inp, ids_ref, wts_ref, layer, tokens=toks, what="prefill8192")
+    y2 = layer.forward(x_to_device(inp.x))
     torch.cuda.synchronize()
     assert torch.isfinite(y.float()).all()
     assert torch.equal(y, y2)
@@ -120,12 +159,67 @@ def test_expert_ffn_stage(name):
                          torch.from_numpy(offsets).to(dev), torch.from_numpy(row_w.astype(np.float32)).to(dev))
     torch.cuda.synchronize()
     layer.check()
-    y_ref, _, _ = oracle.expert_ffn(a_q, a_s, inp.experts, offsets=offsets, row_w=row_w)
+    y_ref, hq_ref, hs_ref, hpre = oracle.expert_ffn(a_q, a_s, inp.experts, offsets=offsets, row_w=row_w,
+                                                    want_hpre=True)
     assert_close(bf16_to_f64(y), y_ref, f"{name} routed FFN")
+    hq, hs = (t.cpu().numpy() for t in layer.last_h())
+    check_h8(hq, hs, hq_ref, hs_ref, hpre, f"{name} routed FFN h")
     ys = layer.expert_ffn(torch.from_numpy(q).to(dev), torch.from_numpy(s).to(dev), shared=True)
     torch.cuda.synchronize()
     ys_ref, _, _ = oracle.expert_ffn(q, s, inp.shared)
     assert_close(bf16_to_f64(ys), ys_ref, f"{name} shared FFN")
+
+
+def test_expert_ffn_wide_weight_scales():
+    """Weight E8M0 bytes far from the generator's two values, through moe_expert_ffn: expert 0 with
+    every scale 40 binades above the usual (gate and up then pass the clamp), expert 1 with every scale
+    20 below (kept where no product leaves fp32's normal range), expert 2 with a quarter of its gate
+    and up rows at byte 0x00 (2^-127) and the rest usual, experts 3..7 with every block's byte drawn
+    from usual +-24.  Rows are compared one by one (each row within 2e-2 of its own rms plus its
+    bf16 rounding), and the h codes against the oracle's."""
+    wl = synth.Workload("wide_scales", 96, 512, 256, 8, 2)
+    inp, ids_ref, wts_ref, _ = oracle.margin_filtered_layer(wl, seed=9)
+    rng = np.random.default_rng(9)
+    for name in ("s13", "s2"):
+        sc = getattr(inp.experts, name).astype(np.int64)
+        sc[0] += 40
+        sc[1] -= 20
+        sc[3:] += rng.integers(-24, 25, size=sc[3:].shape)
+        if name == "s13":
+            quarter = rng.permutation(2 * wl.f)[: wl.f // 2]
+            sc[2, quarter] = 0
+        assert sc.min() >= 0 and sc.max() <= 254
+        setattr(inp.experts, name, sc.astype(np.uint8))
+    layer = _layer_from(inp)
+    try:
+        counts, offsets, perm, inv = oracle.permute(ids_ref, wl.E)
+        assert np.all(counts[:3] > 0)
+        q, s = oracle.quantize_x(inp.x)
+        a_q, a_s = q[perm], s[perm]
+        row_w = np.empty(perm.shape[0])
+        row_w[inv.reshape(-1)] = wts_ref.reshape(-1)
+        dev = device()
+        y = layer.expert_ffn(torch.from_numpy(a_q).to(dev), torch.from_numpy(a_s).to(dev),
+                             torch.from_numpy(offsets).to(dev), torch.from_numpy(row_w.astype(np.float32)).to(dev))
+        torch.cuda.synchronize()
+        layer.check()
+        y_ref, hq_ref, hs_ref, hpre = oracle.expert_ffn(a_q, a_s, inp.experts, offsets=offsets, row_w=row_w,
+                                                        want_hpre=True)
+        yd = bf16_to_f64(y)
+        assert np.all(np.isfinite(yd))
+        rms_r = np.sqrt(np.mean(y_ref ** 2, axis=1, keepdims=True))
+        err = np.abs(yd - y_ref)
+        excess = err - (TOL_MAX_RMS * rms_r + BF16_HALF_ULP_REL * np.abs(y_ref))
+        worst = int(np.argmax(excess.max(axis=1)))
+        print(f"wide scales: worst row {worst} (expert {np.searchsorted(offsets, worst, 'right') - 1}): "
+              f"max |dy| / row rms = {err[worst].max() / rms_r[worst, 0]:.3e}")
+        assert np.all(excess <= 0), f"row {worst} exceeds its own tolerance by {excess.max():.3e}"
+        # the construction reached the extremes: expert 0's rows are about 2^80 times expert 1's
+        assert rms_r[: offsets[1]].min() > 1e9 * rms_r[offsets[1]:offsets[2]].max()
+        hq, hs = (t.cpu().numpy() for t in layer.last_h())
+        check_h8(hq, hs, hq_ref, hs_ref, hpre, "wide scales h")
+    finally:
+        layer.close()
 
 
 @pytest.mark.parametrize("name", ["tiny", "wide", "verify8", "verify512"])
@@ -172,13 +266,7 @@ def test_resident_router_argument_checks():
 def test_tiny_ragged_sizes(T):
     """Chunk / tile edges: one token, partial 32-token chunks, expert groups longer than a 32-row tile."""
     wl, inp, ids_ref, wts_ref, layer = case("tiny", T=T)
-    x = x_to_device(inp.x)
-    y = layer.forward(x)
-    torch.cuda.synchronize()
-    layer.check()
-    assert np.array_equal(layer.last_topk_ids().cpu().numpy(), ids_ref)
-    y_ref = oracle.layer(inp.x, ids_ref, wts_ref, inp.experts, inp.shared, wl.swiglu_limit)
-    assert_close(bf16_to_f64(y), y_ref, f"tiny T={T}")
+    _strict_layer_parity(wl, inp, ids_ref, wts_ref, layer, what=f"tiny T={T}")
 
 
 @pytest.mark.parametrize("E,k,T", [(9, 2, 8), (9, 2, 40), (1, 1, 5), (1, 1, 37)])
@@ -189,13 +277,7 @@ def test_odd_and_single_expert_counts(E, k, T):
     inp, ids_ref, wts_ref, _ = oracle.margin_filtered_layer(wl, seed=6)
     layer = _layer_from(inp)
     try:
-        x = x_to_device(inp.x)
-        y = layer.forward(x)
-        torch.cuda.synchronize()
-        layer.check()
-        assert np.array_equal(layer.last_topk_ids().cpu().numpy(), ids_ref)
-        y_ref = oracle.layer(inp.x, ids_ref, wts_ref, inp.experts, inp.shared, wl.swiglu_limit)
-        assert_close(bf16_to_f64(y), y_ref, f"E={E} k={k} T={T}")
+        _strict_layer_parity(wl, inp, ids_ref, wts_ref, layer, what=f"E={E} k={k} T={T}")
     finally:
         layer.close()
 
@@ -224,11 +306,9 @@ def test_no_shared_expert_and_empty_experts():
     inp, ids_ref, wts_ref, _ = oracle.margin_filtered_layer(wl, seed=3, adjust=starve)
     assert ids_ref.min() >= 4
     layer = _layer_from(inp, with_shared=False)
-    y = layer.forward(x_to_device(inp.x))
-    torch.cuda.synchronize()
-    layer.check()
+    y, y32 = forward_strict(layer, x_to_device(inp.x))
     y_ref = oracle.layer(inp.x, ids_ref, wts_ref, inp.experts, None, wl.swiglu_limit)
-    assert_close(bf16_to_f64(y), y_ref, "no shared, empty experts")
+    assert_strict(y32.cpu().numpy().astype(np.float64), y_ref, "no shared, empty experts")
     layer.close()
 
 
@@ -237,11 +317,7 @@ def test_swiglu_clamp_engaged():
     wl = WORKLOADS["tiny"].with_T(64)
     inp, ids_ref, wts_ref, _ = oracle.margin_filtered_layer(wl, seed=5, x_scale=30.0)
     layer = _layer_from(inp)
-    y = layer.forward(x_to_device(inp.x))
-    torch.cuda.synchronize()
-    layer.check()
-    y_ref = oracle.layer(inp.x, ids_ref, wts_ref, inp.experts, inp.shared, wl.swiglu_limit)
-    assert_close(bf16_to_f64(y), y_ref, "clamped")
+    _strict_layer_parity(wl, inp, ids_ref, wts_ref, layer, what="clamped")
     layer.close()
 
 
@@ -278,13 +354,11 @@ def test_hash_out_of_range_token_is_reported():
     inp = synth.gen_layer(wl, seed=0)
     layer = MoELayer.from_host(inp, device=device(), max_T=16)
     tok = torch.from_numpy(inp.token_ids.copy()).to(device())
-    y = layer.forward(x_to_device(inp.x), token_ids=tok)
-    torch.cuda.synchronize()
-    layer.check()  # in range: no error
+    y, y32 = forward_strict(layer, x_to_device(inp.x), token_ids=tok)  # in range: no error
     ids_ref, wts_ref = oracle.hash_route(inp.token_ids, inp.hash_table, wl.k, wl.route_scale)
     assert np.array_equal(layer.last_topk_ids().cpu().numpy(), ids_ref)
     y_ref = oracle.layer(inp.x, ids_ref, wts_ref, inp.experts, inp.shared, wl.swiglu_limit)
-    assert_close(bf16_to_f64(y), y_ref, "hash tiny")
+    assert_strict(y32.cpu().numpy().astype(np.float64), y_ref, "hash tiny")
     tok[3] = 150
     layer.forward(x_to_device(inp.x), token_ids=tok)
     with pytest.raises(MoEError) as err:
@@ -308,11 +382,9 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     assert err.value.status == 6
     m.moe_testing_stall_loads(layer.h, False)
     m.moe_set_wait_budget(layer.h, 2_000_000_000)
-    y = layer.forward(x)
-    torch.cuda.synchronize()
-    layer.check()
+    y, y32 = forward_strict(layer, x)
     y_ref = oracle.layer(inp.x, ids_ref, wts_ref, inp.experts, inp.shared, wl.swiglu_limit)
-    assert_close(bf16_to_f64(y), y_ref, "after timeout")
+    assert_strict(y32.cpu().numpy().astype(np.float64), y_ref, "after timeout")
     layer.close()
 
 

@@ -148,3 +148,38 @@ def test_stack_with_resident_routers(stack_layers):
         for ly in learned:
             ly.resident_router = False
             moe_experts_set_router(ly.h, None, None)
+
+
+def test_graph_recaptures_after_a_handle_setter(stack_layers):
+    """A cached graph bakes in each layer's workspace.  After moe_set_workspace moves every layer to a new
+    buffer and the old one is freed (filled with garbage first, so stale reads would show), the next call
+    must capture again and still reproduce the direct launches bit for bit."""
+    from block_scaled_fp4_sqrt_gb300 import moe_set_workspace, moe_workspace_size
+    inputs, layers = stack_layers
+    tok = torch.from_numpy(inputs[0].token_ids).to(device())
+    x = x_to_device(synth.gen_x(11, T, 256))
+    direct, graph = _stack(layers), _stack(layers, use_graph=True)
+    try:
+        ref = direct.forward(x, token_ids=tok).clone()
+        out = torch.empty_like(x)
+        graph.forward(x, token_ids=tok, out=out)  # capture
+        graph.forward(x, token_ids=tok, out=out)  # replay
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref)
+        old = graph.workspaces[0]
+        new = torch.empty(moe_workspace_size(layers[0].cfg, T), dtype=torch.uint8, device=device())
+        for ly in layers:
+            moe_set_workspace(ly.h, new, T)
+        graph.workspaces = [new]
+        old.fill_(0xA5)  # whatever the graph would read from the old buffer is now garbage
+        torch.cuda.synchronize()
+        del old
+        out.zero_()
+        graph.forward(x, token_ids=tok, out=out)  # the handles changed: a new capture
+        graph.forward(x, token_ids=tok, out=out)  # and its replay
+        torch.cuda.synchronize()
+        graph.check()
+        assert torch.equal(out, ref)
+    finally:
+        direct.close()
+        graph.close()

@@ -185,6 +185,26 @@ def test_dense_equals_permuted_bitwise():
     assert np.array_equal(y2, y0[sel])
 
 
+def test_layer_h_outputs_are_the_rows_of_each_token_slot():
+    """layer(want_h=True) returns, for every (token, slot), the h of that token through that slot's expert
+    (slot k: the shared expert), the same in both evaluation orders, and y unchanged."""
+    wl, inp, ids, wts = _tiny_layer()
+    y = oracle.layer(inp.x, ids, wts, inp.experts, inp.shared)
+    sel = np.array([5, 0, 11])
+    q, s = oracle.quantize_x(inp.x)
+    for mode in (0, 1):
+        y1, hq, hs, hp = oracle.layer(inp.x, ids, wts, inp.experts, inp.shared, tokens=sel, mode=mode, want_h=True)
+        assert np.array_equal(y1, y[sel])
+        assert hq.shape == (3, wl.k + 1, wl.f) and hs.shape == (3, wl.k + 1, wl.f // 32)
+        for i, t in enumerate(sel):
+            for j in range(wl.k + 1):
+                src = inp.shared if j == wl.k else inp.experts
+                e = 0 if j == wl.k else ids[t, j]
+                _, hq_o, hs_o, hp_o = oracle.expert_row(q[t], s[t], src.w13[e], src.s13[e], src.w2[e], src.s2[e])
+                assert np.array_equal(hq[i, j], hq_o) and np.array_equal(hs[i, j], hs_o)
+                assert np.array_equal(hp[i, j], hp_o)
+
+
 def test_reductions():
     wl, inp, ids, wts = _tiny_layer()
     # no shared expert: y = routed part only; routed weights zero: y = shared only

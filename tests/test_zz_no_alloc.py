@@ -1,10 +1,10 @@
-"""moe_route_noalloc: the learned router for callers that can't call cudaMalloc (inside a CUDA-graph
-capture, under a host framework that owns all device memory, on paths that must not enter an
-allocator).  It keeps its scratch in a fixed array of library device memory instead of a workspace.
+"""moe_route_noalloc: the learned router for callers that can't call cudaMalloc (under a host framework
+that owns all device memory, on paths that must not enter an allocator).  It keeps its scratch in a
+fixed array of library device memory instead of a workspace.
 
-Checked here through the C ABI against moe_route (the handle + workspace entry point) on two calls in
-a row with different batch sizes, so the second call runs over the scratch the first one left; and
-the size limit of the fixed scratch.  This file runs last so that a failure here, under `-x`, stops
+Checked here through the C ABI against moe_route (the handle + workspace entry point) and against the
+oracle's routing on two calls in a row with different batch sizes, so the second call runs over the
+scratch the first one left; and the size limit of the fixed scratch.  This file runs last so that a failure here, under `-x`, stops
 only after every other test has run.
 """
 import numpy as np
@@ -27,13 +27,15 @@ def _router_inputs(seed, T, d, E, k):
     x = synth.gen_x(seed, T, d)
     attempts = np.zeros(T, np.int32)
     for _ in range(64):
-        _, _, margin = oracle.route(x, rw, rb, k)
+        ids, wts, margin = oracle.route(x, rw, rb, k)
         low = np.nonzero(margin < oracle.MARGIN_MIN)[0]
         if low.size == 0:
             break
         attempts[low] += 1
         x[low] = synth.gen_x(seed, T, d, attempts)[low]
-    return x, rw, rb
+    else:
+        raise RuntimeError("margin rejection did not converge")
+    return x, rw, rb, ids, wts
 
 
 @pytest.fixture(scope="module")
@@ -58,7 +60,7 @@ def test_noalloc_router_matches_moe_route_on_two_calls_in_a_row(moe):
         ws = torch.empty(moe.moe_workspace_size(cfg, max_T), dtype=torch.uint8, device=dev)
         moe.moe_set_workspace(h, ws, max_T)
         for seed, T in ((11, 512), (12, 300)):
-            xb, rw, rb = _router_inputs(seed, T, d, E, k)
+            xb, rw, rb, ids_orc, wts_orc = _router_inputs(seed, T, d, E, k)
             router_w = torch.from_numpy(rw).to(dev)
             router_b = torch.from_numpy(rb).to(dev)
             x = torch.from_numpy(xb.view(np.int16)).to(dev).view(torch.bfloat16)
@@ -72,6 +74,11 @@ def test_noalloc_router_matches_moe_route_on_two_calls_in_a_row(moe):
             assert torch.equal(ids, ids_ref), f"T={T}: expert ids differ"
             rel = ((w - w_ref).abs() / w_ref.abs()).max().item()
             assert rel <= TOL_WEIGHT_REL, f"T={T}: routing weights differ by {rel:.3e}"
+            # and against the fp64 oracle directly: ids bit for bit, weights within the same bound
+            assert np.array_equal(ids.cpu().numpy(), ids_orc), f"T={T}: expert ids differ from the oracle's"
+            w_np = w.cpu().numpy().astype(np.float64)
+            rel_o = np.max(np.abs(w_np - wts_orc) / np.abs(wts_orc))
+            assert rel_o <= TOL_WEIGHT_REL, f"T={T}: routing weights differ from the oracle's by {rel_o:.3e}"
         moe.moe_check(h)
     finally:
         moe.moe_experts_destroy(h)
