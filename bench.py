@@ -48,6 +48,8 @@ def parse_args():
     p.add_argument("--workloads", default="all",
                    help="after the headline, also measure these workloads into the line's 'workloads' object: "
                         "'all' (the five layer configurations), 'none', or a comma-separated list (one GPU only)")
+    p.add_argument("--one-sm-gemm", action="store_true",
+                   help="run 128-row tiles on the one-SM grouped GEMMs instead of CTA pairs (for A/B comparisons)")
     p.add_argument("--cpu-seconds-other", type=float, default=4.0,
                    help="target CPU time of the oracle baseline sample of each extra workload")
     return p.parse_args()
@@ -307,6 +309,9 @@ def measure_layer(args, wl, inp, dev, world, rank, mx_peak, mma_name, cpu_target
     fp4 = args.act == "mxfp4"
     # the router weights are made resident once, like the expert weights (moe_experts_set_router)
     layer = moe.MoELayer.from_host(inp, device=dev, max_T=wl.T, act=args.act, resident_router=True)
+    if args.one_sm_gemm:
+        for h in (layer.h, layer.h_shared):
+            moe.moe_testing_set_pair_gemm(h, False)
     x = torch.from_numpy(inp.x.view(np.int16)).to(dev).view(torch.bfloat16)
     out = torch.empty((wl.T, wl.d), dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -480,7 +485,8 @@ def measure_layer(args, wl, inp, dev, world, rank, mx_peak, mma_name, cpu_target
                       "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": lb / (ms * 1e-3) / 1e9 / pk["hbm_gbs"]}
     rec = {
         "ms_per_step": ms, "value": job_tokens_per_s(world, wl.T, ms), "unit": "tokens/s",
-        "config": dict(workload_config(wl, args.act), touched_experts=touched, parallelism=f"replicas x{world}"),
+        "config": dict(workload_config(wl, args.act), touched_experts=touched, parallelism=f"replicas x{world}",
+                       gemm="one-SM" if args.one_sm_gemm or wl.T * wl.k <= 16 * wl.E or fp4 else "CTA pairs"),
         "roofline": roof,
         "layer_roofline": layer_roof,
         "gemm_tensor": {"achieved": layer_fl / ((stage_ms["gemm_gate_up"] + stage_ms["gemm_down"]) * 1e-3) / 1e12,

@@ -28,7 +28,7 @@ EXPORTED = ("moe_experts_create", "moe_experts_set_hash_table", "moe_workspace_s
             "moe_testing_stall_loads", "moe_set_stage_events", "moe_route_noalloc", "moe_measure_mxf8f6f4_peak",
             "moe_stack_create", "moe_stack_forward", "moe_stack_destroy", "moe_mx_blocks_unpack",
             "moe_experts_set_activation_format", "moe_measure_mxf4_peak", "moe_testing_read_h",
-            "moe_experts_set_router", "moe_testing_read_y32")
+            "moe_experts_set_router", "moe_testing_read_y32", "moe_testing_set_pair_gemm")
 
 MOE_MX_NIBBLES_PAIRED, MOE_MX_NIBBLES_SPLIT = 0, 1
 MOE_ACT_MXFP8, MOE_ACT_MXFP4 = 0, 1
@@ -88,6 +88,7 @@ def lib() -> ctypes.CDLL:
         L.moe_testing_read_h.argtypes = [vp, vp, vp, ctypes.POINTER(i32), vp]
         L.moe_experts_set_router.argtypes = [vp, vp, vp, vp]
         L.moe_testing_read_y32.argtypes = [vp, vp, ctypes.POINTER(i32), vp]
+        L.moe_testing_set_pair_gemm.argtypes = [vp, i32]
         L.moe_stack_create.argtypes = [ctypes.POINTER(moe_stack_layer_t), i32, i32, ctypes.POINTER(vp)]
         L.moe_stack_forward.argtypes = [vp, inp, vp, vp, vp]
         L.moe_stack_destroy.argtypes = [vp]
@@ -222,6 +223,11 @@ def moe_testing_read_h(h, f: int, act: str, stream=None):
     if n.value:
         _ok("moe_testing_read_h", lib().moe_testing_read_h(h, _p(hq), _p(hs), ctypes.byref(n), _stream(stream)))
     return hq, hs
+
+
+def moe_testing_set_pair_gemm(h, enable: bool) -> None:
+    """Run 128-row tiles on CTA-pair GEMMs (the default) or on the one-SM kernels."""
+    _ok("moe_testing_set_pair_gemm", lib().moe_testing_set_pair_gemm(h, 1 if enable else 0))
 
 
 def moe_testing_read_y32(h, d: int, stream=None) -> torch.Tensor:

@@ -27,6 +27,10 @@ struct moe_experts_s {
   CUtensorMap tm2;
   CUtensorMap tm13p;  // ... and for kind::mxf4 (packed 64-byte rows, 64-byte swizzle)
   CUtensorMap tm2p;
+  CUtensorMap tm13h;  // kind::mxf8f6f4 codes in 128-row boxes: one CTA's half of a slab (CTA-pair GEMMs)
+  CUtensorMap tm2h;
+  CUtensorMap tm_sf13;  // the scale atoms as rows of 256 B, 4-row boxes (both atoms of a slab)
+  CUtensorMap tm_sf2;
   int act_fp4 = 0;    // activation format: 0 = MXFP8, 1 = MXFP4 (moe_experts_set_activation_format)
   __nv_bfloat16* router_split = nullptr;  // owned: resident router weight planes (moe_experts_set_router)
   float* router_w32 = nullptr;            // owned: the resident router weights in fp32 (small batches)
@@ -47,6 +51,7 @@ struct moe_experts_s {
   int32_t last_fwd_T = -1;     // T of the last moe_forward (its fp32 expert rows stay in the workspace), or -1
   int32_t last_fwd_shared = 0;  // whether that forward had a shared expert
   int stall_loads = 0;
+  int pair_gemm = 1;  // 128-row tiles on CTA pairs (moe_testing_set_pair_gemm)
   void* const* stage_events = nullptr;  // MOE_N_STAGES + 1 caller-owned cudaEvent_t, or null
   // Changes whenever something a recorded launch sequence depends on changes (workspace, router, hash
   // table, activation format, wait budget, test hooks, stage events): a stack's cached graph compares it.
@@ -129,6 +134,22 @@ moe_status_t make_map_packed(CUtensorMap* m, const void* base, uint64_t row_byte
   return MOE_OK;
 }
 
+// Scale atoms (512 B each) viewed as rows of 256 bytes: box {256 B, box_rows}, no swizzle, so a box of 2 rows
+// is one atom and a box of 4 rows two consecutive atoms, each landing contiguously in shared memory.
+moe_status_t make_map_atoms(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  cuuint64_t gdim[2] = {256u, rows};
+  cuuint64_t gstride[1] = {256u};
+  cuuint32_t box[2] = {256u, box_rows};
+  cuuint32_t estr[2] = {1u, 1u};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), gdim, gstride, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled (scale atoms) failed (%d)", (int)r);
+  return MOE_OK;
+}
+
 // bf16 K-major map: inner dimension K, outer `rows`, box {64 elements (128 B), box_rows}, 128-byte swizzle.
 moe_status_t make_map_bf16(CUtensorMap* m, const void* base, uint64_t K, uint64_t rows, uint32_t box_rows) {
   auto fn = encode_fn();
@@ -184,7 +205,9 @@ Dims dims_for(int max_T, int E, int k) {
   dm.rows = max_T * (k + 1);
   dm.G = E + 1;
   dm.n_chunks = (max_T + 31) / 32;
-  dm.max_tiles = (dm.rows + kSmallTileRows - 1) / kSmallTileRows + dm.G;  // the short tile shape needs most
+  // the short tile shape needs the most tiles; + G more covers the padding of the CTA-pair shape, which
+  // gives every group an even number of 128-row tiles
+  dm.max_tiles = (dm.rows + kSmallTileRows - 1) / kSmallTileRows + 2 * dm.G;
   return dm;
 }
 
@@ -302,6 +325,10 @@ moe_status_t moe_experts_create(const moe_config_t* cfg, int32_t n, const uint8_
   if (st == MOE_OK) st = make_map(&h->tm2, h->w2, true, 128, (uint64_t)n * d * (f / 128), 256);
   if (st == MOE_OK) st = make_map_packed(&h->tm13p, h->w13, 64, (uint64_t)n * 2 * f * (d / 128), 256);
   if (st == MOE_OK) st = make_map_packed(&h->tm2p, h->w2, 64, (uint64_t)n * d * (f / 128), 256);
+  if (st == MOE_OK) st = make_map(&h->tm13h, h->w13, true, 128, (uint64_t)n * 2 * f * (d / 128), 128);
+  if (st == MOE_OK) st = make_map(&h->tm2h, h->w2, true, 128, (uint64_t)n * d * (f / 128), 128);
+  if (st == MOE_OK) st = make_map_atoms(&h->tm_sf13, h->sf13, sf13_bytes / 256, 4);
+  if (st == MOE_OK) st = make_map_atoms(&h->tm_sf2, h->sf2, sf2_bytes / 256, 4);
   if (st != MOE_OK) {
     moe_experts_destroy(h);
     return st;
@@ -531,9 +558,16 @@ static int tile_rows_for(int rows, int groups) {
   return rows <= 16 * groups ? kSmallTileRows : kTileRows;
 }
 
+// 128-row tiles of MXFP8 activations run on CTA pairs (moe_set_pair_gemm can switch that off).
+static bool use_pairs(const moe_experts_s* h, int tile_rows) {
+  return tile_rows == kTileRows && !h->act_fp4 && h->pair_gemm;
+}
+
+// pair: the work list pads every group to an even number of 128-row tiles; run both GEMMs on CTA pairs.
 static moe_status_t run_ffn(moe_experts_s* h, moe_experts_s* sh, int rows, int E_groups_shared_index,
                             const uint8_t* a_q, const uint8_t* a_sf_atoms, const float* row_w, float* y_f32,
-                            __nv_bfloat16* y_bf16, int max_tiles, int tile_rows, bool timed, cudaStream_t s) {
+                            __nv_bfloat16* y_bf16, int max_tiles, int tile_rows, bool timed, cudaStream_t s,
+                            bool pair = false) {
   const int d = h->cfg.d_model, f = h->cfg.d_ff;
   const int fp4 = h->act_fp4;
   CUtensorMap tm_a, tm_a32, tm_h, tm_h32;
@@ -551,15 +585,31 @@ static moe_status_t run_ffn(moe_experts_s* h, moe_experts_s* sh, int rows, int E
   }
   if (st != MOE_OK) return st;
   const moe_experts_s* shx = sh ? sh : h;
+  pair = pair && !fp4 && tile_rows == kTileRows;
+  PairMaps pm13, pm2;
+  if (pair) {
+    pm13.w = h->tm13h;
+    pm13.w_shared = shx->tm13h;
+    pm13.sfw = h->tm_sf13;
+    pm13.sfw_shared = shx->tm_sf13;
+    pm2.w = h->tm2h;
+    pm2.w_shared = shx->tm2h;
+    pm2.sfw = h->tm_sf2;
+    pm2.sfw_shared = shx->tm_sf2;
+    st = make_map_atoms(&pm13.sfa, a_sf_atoms, (uint64_t)max_tiles * (d / 128) * 2, 2);
+    if (st == MOE_OK) st = make_map_atoms(&pm2.sfa, h->ws.h_sf, (uint64_t)max_tiles * (f / 128) * 2, 2);
+    if (st != MOE_OK) return st;
+  }
   MOE_CUDA(launch_gemm_gate_up(fp4 ? h->tm13p : h->tm13, fp4 ? shx->tm13p : shx->tm13, h->sf13, shx->sf13, tm_a, tm_a32,
                                a_sf_atoms, h->ws.tiles, h->ws.n_tiles, max_tiles, E_groups_shared_index, d, f,
                                h->cfg.swiglu_limit, h->ws.h_q, h->ws.h_sf, h->status, h->budget_ns, h->stall_loads,
-                               tile_rows, fp4, h->num_sms, s),
+                               tile_rows, fp4, h->num_sms, s, pair ? &pm13 : nullptr),
            "gate-up GEMM");
   if (timed) mark_stage(h, 3, s);
   MOE_CUDA(launch_gemm_down(fp4 ? h->tm2p : h->tm2, fp4 ? shx->tm2p : shx->tm2, h->sf2, shx->sf2, tm_h, tm_h32,
                             h->ws.h_sf, h->ws.tiles, h->ws.n_tiles, max_tiles, E_groups_shared_index, d, f, row_w, y_f32,
-                            y_bf16, h->status, h->budget_ns, h->stall_loads, tile_rows, fp4, h->num_sms, s),
+                            y_bf16, h->status, h->budget_ns, h->stall_loads, tile_rows, fp4, h->num_sms, s,
+                            pair ? &pm2 : nullptr),
            "down GEMM");
   return MOE_OK;
 }
@@ -579,14 +629,15 @@ moe_status_t moe_expert_ffn(moe_experts_t h, int32_t n_rows, const int32_t* offs
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const int groups = offsets ? h->n : 1;
   const int bn = tile_rows_for(n_rows, groups);
+  const bool pair = use_pairs(h, bn);
   MOE_CUDA(launch_tiles_from_offsets(offsets, groups, n_rows, bn, dm.max_tiles, h->ws.tile_off,
-                                     h->ws.n_tiles, h->ws.tiles, h->status, s),
+                                     h->ws.n_tiles, h->ws.tiles, h->status, s, pair ? 1 : 0),
            "tile list");
   MOE_CUDA(launch_rows_sf_to_atoms(a_s, h->ws.tiles, h->ws.n_tiles, h->cfg.d_model, dm.max_tiles, h->ws.a_sf, s),
            "scale atoms");
   h->last_rows = n_rows;
   return run_ffn(h, nullptr, n_rows, h->n, a_q, h->ws.a_sf, row_w, nullptr, static_cast<__nv_bfloat16*>(y_bf16),
-                 dm.max_tiles, bn, false, s);
+                 dm.max_tiles, bn, false, s, pair);
 }
 
 moe_status_t moe_set_stage_events(moe_experts_t h, void* const* events, int32_t n) {
@@ -635,6 +686,8 @@ moe_status_t forward_impl(const moe_input_t* x, const float* router_w, const flo
   const int bn = tile_rows_for(R, E);
   // learned routing of a small batch: the router's last CTA also writes the dispatch state
   const bool router_dispatch = !h->hash_table && T >= 1 && T <= kRouterSmallMaxT && bn >= kRouterSmallMaxT;
+  // the small-batch router's dispatch writes one tile per group: no pair padding, so one-SM GEMMs there
+  const bool pair = !router_dispatch && use_pairs(h, bn);
   SmallDispatch sd{G, has_shared, bn, dm.max_tiles, h->ws.chunk_hist, h->ws.counts, h->ws.offsets, h->ws.tile_off,
                    h->ws.n_tiles, h->ws.tiles};
   mark_stage(h, 0, s);
@@ -650,7 +703,7 @@ moe_status_t forward_impl(const moe_input_t* x, const float* router_w, const flo
   if (!router_dispatch) {
     MOE_CUDA(launch_histogram(h->ws.topk_ids, T, k, E, G, h->ws.chunk_hist, h->status, s), "histogram");
     MOE_CUDA(launch_scan(h->ws.chunk_hist, n_chunks, T, E, G, has_shared, bn, dm.max_tiles, h->ws.counts,
-                         h->ws.offsets, h->ws.tile_off, h->ws.n_tiles, h->ws.tiles, h->status, s),
+                         h->ws.offsets, h->ws.tile_off, h->ws.n_tiles, h->ws.tiles, h->status, s, pair ? 1 : 0),
              "scan");
   }
   MOE_CUDA(launch_gather(static_cast<const __nv_bfloat16*>(x->x_bf16), h->ws.topk_ids, h->ws.topk_w, h->ws.chunk_hist,
@@ -658,7 +711,8 @@ moe_status_t forward_impl(const moe_input_t* x, const float* router_w, const flo
                          nullptr, h->ws.perm_tok, h->ws.inv_pos, h->ws.row_w, h->act_fp4, s),
            "gather");
   mark_stage(h, 2, s);
-  st = run_ffn(h, sh, rows, E, h->ws.a_q, h->ws.a_sf, h->ws.row_w, h->ws.y_rows, nullptr, dm.max_tiles, bn, true, s);
+  st = run_ffn(h, sh, rows, E, h->ws.a_q, h->ws.a_sf, h->ws.row_w, h->ws.y_rows, nullptr, dm.max_tiles, bn, true, s,
+               pair);
   if (st != MOE_OK) return st;
   h->last_rows = rows;
   mark_stage(h, 4, s);
@@ -719,6 +773,13 @@ moe_status_t moe_testing_read_y32(moe_experts_t h, float* y32, int32_t* T, moe_s
   MOE_CUDA(launch_combine(h->ws.y_rows, h->ws.inv_pos, Tl, h->cfg.d_model, k, Tl * k, h->last_fwd_shared, nullptr,
                           nullptr, s, y32),
            "fp32 combine");
+  return MOE_OK;
+}
+
+moe_status_t moe_testing_set_pair_gemm(moe_experts_t h, int32_t enable) {
+  if (!h) return fail(MOE_ERR_INVALID_ARG, "handle is NULL");
+  h->pair_gemm = enable ? 1 : 0;
+  bump(h);
   return MOE_OK;
 }
 

@@ -101,6 +101,48 @@ __device__ __forceinline__ bool mbar_spin(uint64_t* bar, uint32_t parity, uint64
   }
 }
 
+// ------------------------------------------------------------------------- thread-block clusters
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// All threads of every CTA of the cluster: release this CTA's prior writes, then acquire the others'.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Address, in the cluster's shared window, of the same shared-memory location in CTA `rank`.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+
+// Arrive on an mbarrier of another CTA of the cluster (cluster_addr from mapa_shared), releasing this
+// thread's prior memory operations at cluster scope.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+// mbar_wait for a barrier that other CTAs arrive on: acquire at cluster scope, so that what those CTAs
+// released before arriving is visible afterwards.  Bounded like mbar_wait.
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, uint64_t budget_ns) {
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity), "r"(200000u)
+        : "memory");
+    if (ok) return true;
+    if (globaltimer_ns() - t0 > budget_ns) return false;
+  }
+}
+
 // ------------------------------------------------------------------------- routing
 __device__ __forceinline__ float softplus_f(float l) { return fmaxf(l, 0.f) + log1pf(expf(-fabsf(l))); }
 
@@ -167,6 +209,18 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
       " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_addr(dst)),
       "l"(map), "r"(x), "r"(y), "r"(smem_addr(bar)), "l"(policy)
+      : "memory");
+}
+
+// The CTA-pair form: this CTA's shared memory receives the tile, and the completion is counted on the
+// mbarrier named by leader_bar (a shared::cluster address; the even CTA's barrier, from mapa_shared),
+// which can thus track the loads of both CTAs of the pair.
+__device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* map, int x, int y, uint32_t leader_bar,
+                                                 uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cta.global.tile.mbarrier::complete_tx::bytes.cta_group::2.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_addr(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(leader_bar), "l"(policy)
       : "memory");
 }
 
@@ -314,6 +368,64 @@ __device__ __forceinline__ bool tc_stage2_mxf4_commit_poll(uint32_t d_tmem, uint
       : "=r"(ok)
       : "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(accumulate), "r"(idesc0), "r"(sfa_tmem), "r"(sfb_tmem),
         "r"(smem_addr(poll_bar)), "r"(poll_parity), "r"(smem_addr(commit_bar))
+      : "memory");
+  return ok != 0;
+}
+
+// ---- CTA-pair (cta_group::2) forms.  The even CTA of a two-CTA cluster issues them for the pair: an
+// MMA with M = 256 reads A rows 0..127 from its own shared memory and rows 128..255 from the peer's, and
+// the N rows of B half from each (at the same shared-memory offsets), and writes each CTA's 128 rows of
+// D into that CTA's tensor memory; a scale copy reads each CTA's own shared memory into its own tensor
+// memory.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t* slot, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(slot)), "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void tc_copy_sf_pair(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+// Arrive on the barrier at the same offset in both CTAs of the pair once the pair's prior MMAs retire.
+__device__ __forceinline__ void tc_commit_pair(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_addr(bar)),
+      "h"((uint16_t)3)
+      : "memory");
+}
+
+// The pair's form of tc_stage4_mx_commit_poll: four M = 256 block-scaled MMAs (K = 4 x 32), the stage's
+// commit multicast to both CTAs' barrier, and a non-blocking test (cluster-scope acquire: the peer CTA
+// arrives on these barriers) of another stage's barrier, read after the commit.
+__device__ __forceinline__ bool tc_stage4_mx_pair_commit_poll(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                                              uint32_t idesc0, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                                              uint32_t accumulate, uint64_t* commit_bar,
+                                                              uint64_t* poll_bar, uint32_t poll_parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p, q, t;\n .reg .b64 a1, a2, a3, b1, b2, b3;\n .reg .b32 i1, i2, i3;\n"
+      " mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 q, [%8], %9;\n"
+      " setp.ne.b32 p, %4, 0;\n"
+      " setp.eq.b32 t, 0, 0;\n"
+      " add.s64 a1, %2, 2;\n add.s64 b1, %3, 2;\n"
+      " add.s64 a2, %2, 4;\n add.s64 b2, %3, 4;\n"
+      " add.s64 a3, %2, 6;\n add.s64 b3, %3, 6;\n"
+      " or.b32 i1, %5, 0x20000010;\n or.b32 i2, %5, 0x40000020;\n or.b32 i3, %5, 0x60000030;\n"
+      " tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%1], %2, %3, %5, [%6], [%7], p;\n"
+      " tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%1], a1, b1, i1, [%6], [%7], t;\n"
+      " tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%1], a2, b2, i2, [%6], [%7], t;\n"
+      " tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%1], a3, b3, i3, [%6], [%7], t;\n"
+      " tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%10], %11;\n"
+      " selp.u32 %0, 1, 0, q;\n}\n"
+      : "=r"(ok)
+      : "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(accumulate), "r"(idesc0), "r"(sfa_tmem), "r"(sfb_tmem),
+        "r"(smem_addr(poll_bar)), "r"(poll_parity), "r"(smem_addr(commit_bar)), "h"((uint16_t)3)
       : "memory");
   return ok != 0;
 }

@@ -111,13 +111,14 @@ __global__ void __launch_bounds__(256) colscan_kernel(int32_t* __restrict__ chun
 }
 
 // Single block: per-group row counts (from counts, from caller offsets, or one group of n_rows) ->
-// offsets [G+1] (if requested), tile offsets [G+1], and the list of row tiles of at most bn rows.
+// offsets [G+1] (if requested), tile offsets [G+1], and the list of row tiles of at most bn rows.  With
+// pad_pairs every non-empty group gets an even number of tiles (the last one, if added, holds no rows).
 __global__ void __launch_bounds__(1024) groupscan_kernel(const int32_t* __restrict__ counts,
                                                          const int32_t* __restrict__ offsets_in, int G, int n_rows,
                                                          int bn, int max_tiles, int32_t* __restrict__ offsets,
                                                          int32_t* __restrict__ tile_off,
                                                          int32_t* __restrict__ n_tiles, RowTile* __restrict__ tiles,
-                                                         int* status) {
+                                                         int* status, int pad_pairs) {
   __shared__ int s_cnt[kMaxGroups], s_off[kMaxGroups], s_toff[kMaxGroups];
   __shared__ int bad;
   pdl_trigger();
@@ -140,8 +141,10 @@ __global__ void __launch_bounds__(1024) groupscan_kernel(const int32_t* __restri
       }
     }
     int tot_r, tot_t;
+    int nt = (c + bn - 1) / bn;
+    if (pad_pairs) nt += nt & 1;
     const int ex_r = block_exclusive_scan(c, &tot_r);
-    const int ex_t = block_exclusive_scan((c + bn - 1) / bn, &tot_t);
+    const int ex_t = block_exclusive_scan(nt, &tot_t);
     if (g < G) {
       s_cnt[g] = c;
       s_off[g] = offsets_in ? offsets_in[g] : carry_r + ex_r;
@@ -168,13 +171,15 @@ __global__ void __launch_bounds__(1024) groupscan_kernel(const int32_t* __restri
   if (bad) return;
   for (int g = threadIdx.x; g < G; g += blockDim.x) {
     const int cnt = s_cnt[g];
-    for (int i = 0; i * bn < cnt; ++i) {
+    int nt = (cnt + bn - 1) / bn;
+    if (pad_pairs) nt += nt & 1;
+    for (int i = 0; i < nt; ++i) {
       const int idx = s_toff[g] + i;
       if (idx < max_tiles) {
         RowTile rt;
         rt.group = g;
         rt.row0 = s_off[g] + i * bn;
-        rt.nrows = min(bn, cnt - i * bn);
+        rt.nrows = max(0, min(bn, cnt - i * bn));
         rt.pad = 0;
         tiles[idx] = rt;
       }
@@ -449,22 +454,22 @@ cudaError_t launch_histogram(const int32_t* ids, int T, int k, int E, int G, int
 
 cudaError_t launch_scan(int32_t* chunk_hist, int n_chunks, int T, int E, int G, int has_shared, int bn, int max_tiles,
                         int32_t* counts, int32_t* offsets, int32_t* tile_off, int32_t* n_tiles, RowTile* tiles,
-                        int* status, cudaStream_t s) {
+                        int* status, cudaStream_t s, int pad_pairs) {
   if (G > kMaxGroups) return cudaErrorInvalidValue;
   const int threads = n_chunks >= 256 ? 256 : ((n_chunks + 31) / 32) * 32;
   cudaError_t e = launch_pdl(colscan_kernel, dim3(G), dim3(threads), 0, s, chunk_hist, n_chunks, T, E, has_shared,
                              counts);
   if (e != cudaSuccess) return e;
   return launch_pdl(groupscan_kernel, dim3(1), dim3(1024), 0, s, (const int32_t*)counts, (const int32_t*)nullptr, G, 0,
-                    bn, max_tiles, offsets, tile_off, n_tiles, tiles, status);
+                    bn, max_tiles, offsets, tile_off, n_tiles, tiles, status, pad_pairs);
 }
 
 cudaError_t launch_tiles_from_offsets(const int32_t* offsets, int G, int n_rows, int bn, int max_tiles,
                                       int32_t* tile_off, int32_t* n_tiles, RowTile* tiles, int* status,
-                                      cudaStream_t s) {
+                                      cudaStream_t s, int pad_pairs) {
   if (G > kMaxGroups) return cudaErrorInvalidValue;
   return launch_pdl(groupscan_kernel, dim3(1), dim3(1024), 0, s, (const int32_t*)nullptr, offsets, G, n_rows, bn,
-                    max_tiles, (int32_t*)nullptr, tile_off, n_tiles, tiles, status);
+                    max_tiles, (int32_t*)nullptr, tile_off, n_tiles, tiles, status, pad_pairs);
 }
 
 cudaError_t launch_gather(const __nv_bfloat16* x, const int32_t* ids, const float* wts, const int32_t* chunk_hist,

@@ -33,6 +33,8 @@
 // stage's K = 128 is one 64-byte row per operand row (64-byte swizzle), two MMAs per stage, so the
 // weight ring takes half the shared memory and the tensor pipe does twice the work per instruction.
 // The weights, their scale atoms and the activation scale atoms are the same as in the MXFP8 path.
+#include <atomic>
+
 #include "moe_device.cuh"
 
 namespace moe {
@@ -109,7 +111,104 @@ struct GemmArgs {
   int stall_loads;  // test hook: issue no loads, so the consumers' bounded waits run out
 };
 
-__device__ __forceinline__ float silu_f(float z) { return z / (1.0f + expf(-z)); }
+// silu(z) = z / (1 + e^-z) with the hardware exponential and reciprocal (__expf, __fdividef): a few
+// instructions instead of the IEEE-exact sequences.  Their relative error (about 1e-6) is far below the
+// MXFP8 step of h (2^-3), so it moves an h code only where h sits within that distance of a rounding
+// midpoint.  The epilogue warps share the SM's issue slots with the MMA-issuing thread, whose issue rate
+// bounds the grouped GEMMs, so fewer epilogue instructions mean faster MMA issue.  For z below about -88,
+// e^-z overflows to infinity and the quotient is -0, the limit of silu.
+__device__ __forceinline__ float silu_f(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
+
+// The epilogue of one work item for one warp: the warp's 32 token rows (TMEM lane quadrant q) and its
+// column quarter c of the accumulator, already in registers (v0, v1), for row tile `ti` (rows rt) and
+// output tile mt.  Gate-up: SwiGLU with clamp, then the MX requantisation of h; down: the routing-weighted
+// rows, fp32 through the warp's staging buffer stg (EPI) or direct, or bf16.
+template <int EPI, bool FP4>
+__device__ __forceinline__ void epilogue_rows(const GemmArgs& a, const RowTile& rt, int ti, int mt, int q, int c,
+                                              int lane, float* stg, bool active, float (&v0)[32], float (&v1)[32]) {
+  const int lr = q * 32 + lane;  // token row inside the tile
+  if (EPI && !a.gate_up) {
+    // fp32 rows through the warp's staging buffer: lane l writes its row's 32 values, then each
+    // quarter warp stores one row's 128 contiguous bytes
+    if (active) {
+      const bool row_ok = lr < rt.nrows;
+      const float wr = !row_ok ? 0.f : (a.row_w ? __ldg(&a.row_w[rt.row0 + lr]) : 1.0f);
+      float* ybase = a.y_f32 + (size_t)rt.row0 * a.d + (size_t)mt * kN + 64 * c;
+      auto stage_half = [&](const float(&v)[32], int half) {
+        float4* srow = reinterpret_cast<float4*>(stg + lane * kStageStride);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          srow[i] = make_float4(v[4 * i] * wr, v[4 * i + 1] * wr, v[4 * i + 2] * wr, v[4 * i + 3] * wr);
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int rr = q * 32 + 4 * i + (lane >> 3);  // row inside the tile
+          const float4 val = reinterpret_cast<const float4*>(stg + (4 * i + (lane >> 3)) * kStageStride)[lane & 7];
+          if (rr < rt.nrows) reinterpret_cast<float4*>(ybase + (size_t)rr * a.d + 32 * half)[lane & 7] = val;
+        }
+        __syncwarp();
+      };
+      stage_half(v0, 0);
+      stage_half(v1, 1);
+    }
+    return;
+  }
+  if (!active || lr >= rt.nrows) return;
+  const int r = rt.row0 + lr;
+  if (a.gate_up) {
+    const float L = a.limit;
+    float* h = v0;  // h overwrites the gate values in place
+    float amax = 0.f;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const float gc = fminf(v0[j], L);
+      const float uc = fminf(fmaxf(v1[j], -L), L);
+      h[j] = silu_f(gc) * uc;
+      amax = fmaxf(amax, fabsf(h[j]));
+    }
+    const int se = FP4 ? mxfp4_block_exp(amax) : mxfp8_block_exp(amax);
+    const float mul = exp2_neg_int(se);
+    if (FP4) {  // 32 E2M1 codes: 16 bytes at h column mt * 128 + 32 c of a row of f / 2 bytes
+      *reinterpret_cast<uint4*>(a.h_q + (size_t)r * (a.f / 2) + mt * (kKGroup / 2) + 16 * c) = e2m1_block(v0, mul);
+    } else {
+      uint32_t packed[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint32_t lo = e4m3x2(h[4 * i] * mul, h[4 * i + 1] * mul);
+        const uint32_t hi = e4m3x2(h[4 * i + 2] * mul, h[4 * i + 3] * mul);
+        packed[i] = lo | (hi << 16);
+      }
+      uint4* dst = reinterpret_cast<uint4*>(a.h_q + (size_t)r * a.f + mt * kKGroup + 32 * c);
+      dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+      dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+    }
+    a.h_sf[((size_t)ti * (a.f / kKGroup) + mt) * kSfAtomBytes + (lr & 31) * 16 + (lr >> 5) * 4 + c] =
+        (uint8_t)(se + 127);
+  } else {
+    const float wr = a.row_w ? __ldg(&a.row_w[r]) : 1.0f;
+    const size_t col0 = (size_t)mt * kN + 64 * c;
+    if (a.y_f32) {
+      float4* dst = reinterpret_cast<float4*>(a.y_f32 + (size_t)r * a.d + col0);
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        dst[i] = make_float4(v0[4 * i] * wr, v0[4 * i + 1] * wr, v0[4 * i + 2] * wr, v0[4 * i + 3] * wr);
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        dst[8 + i] = make_float4(v1[4 * i] * wr, v1[4 * i + 1] * wr, v1[4 * i + 2] * wr, v1[4 * i + 3] * wr);
+    } else {
+      uint4* dst = reinterpret_cast<uint4*>(a.y_bf16 + (size_t)r * a.d + col0);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float* src = i < 4 ? &v0[8 * i] : &v1[8 * (i - 4)];
+        uint4 o;
+        __nv_bfloat162* ov = reinterpret_cast<__nv_bfloat162*>(&o);
+#pragma unroll
+        for (int p = 0; p < 4; ++p) ov[p] = __floats2bfloat162_rn(src[2 * p] * wr, src[2 * p + 1] * wr);
+        dst[i] = o;
+      }
+    }
+  }
+}
 
 template <int STAGES, int AROWS, int EPI, bool FP4>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -246,31 +345,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t cph = 0;    // its phase
       int lg = 0, ls = 0;  // first stage whose scales are not in TMEM yet, and its slot / phase
       uint32_t lph = 0;
-      int g = 0;
-      for (int item = 0; item < n_items && ok; ++item) {
-        for (int kg = 0; kg < a.KG; ++kg, ++g) {
-          if (lg == g) {  // this stage has not been seen yet: wait for it
-            if (abort_flag || !mbar_wait(&full[ls], lph, a.budget_ns)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            copy_sf(ls);
-            ++lg;
-            if (++ls == STAGES) {
-              ls = 0;
-              lph ^= 1u;
-            }
+      int g = 0, kg = 0, item = 0;
+      // The inner loop issues stages back to back and holds no branch with a wait loop inside: such a
+      // branch, even never taken, slowed the MMA issue by a fifth (measured).  A work item's start (the
+      // accumulator handoff) and a stage whose scales are not in TMEM yet leave it for the outer loop.
+      while (g < n_st) {
+        if (kg == 0) {  // a new work item: the epilogue must have drained the accumulator
+          const uint32_t par = ((uint32_t)item & 1u) ^ 1u;
+          if (abort_flag || !(kPollHandoff ? mbar_spin(acc_empty, par, a.budget_ns)
+                                           : mbar_wait(acc_empty, par, a.budget_ns))) {
+            ok = false;
+            break;
           }
-          if (kg == 0) {  // a new work item: the epilogue must have drained the accumulator
-            const uint32_t par = ((uint32_t)item & 1u) ^ 1u;
-            if (abort_flag || !(kPollHandoff ? mbar_spin(acc_empty, par, a.budget_ns)
-                                             : mbar_wait(acc_empty, par, a.budget_ns))) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
+          tc_fence_after();
+        }
+        if (lg == g) {  // this stage has not been seen yet: wait for it
+          if (abort_flag || !mbar_wait(&full[ls], lph, a.budget_ns)) {
+            ok = false;
+            break;
           }
+          tc_fence_after();
+          copy_sf(ls);
+          ++lg;
+          if (++ls == STAGES) {
+            ls = 0;
+            lph ^= 1u;
+          }
+        }
+        for (;;) {
           const bool look = lg < n_st && lg <= g + kAhead;
           // with nothing to look ahead for, the test re-reads this stage's own (completed) barrier
           const uint64_t ad = a_desc0 + (uint64_t)((cs * C::kASlot) >> 4);
@@ -282,7 +384,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                   : tc_stage4_mx_commit_poll(tbase, ad, bd, kIdesc0, sfa, sfa + 4, kg != 0 ? 1u : 0u, &empty[cs],
                                              look ? &full[ls] : &full[cs], look ? lph : cph);
           any = true;
-          if (kg == a.KG - 1) tc_commit(acc_full);
           if (look && landed) {
             tc_fence_after();
             copy_sf(ls);
@@ -296,6 +397,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             cs = 0;
             cph ^= 1u;
           }
+          ++g;
+          if (++kg == a.KG) {
+            tc_commit(acc_full);
+            kg = 0;
+            ++item;
+            break;
+          }
+          if (lg == g) break;
         }
       }
       if (!ok) {
@@ -340,88 +449,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(acc_empty);
-      if (EPI && !a.gate_up) {
-        // fp32 rows through the warp's staging buffer: lane l writes its row's 32 values, then each
-        // quarter warp stores one row's 128 contiguous bytes
-        if (active) {
-          const bool row_ok = lr < rt.nrows;
-          const float wr = !row_ok ? 0.f : (a.row_w ? __ldg(&a.row_w[rt.row0 + lr]) : 1.0f);
-          float* stg = reinterpret_cast<float*>(smem + C::kEpiOff) + (warp - 2) * kStageFloats;
-          float* ybase = a.y_f32 + (size_t)rt.row0 * a.d + (size_t)mt * kN + 64 * c;
-          auto stage_half = [&](const float(&v)[32], int half) {
-            float4* srow = reinterpret_cast<float4*>(stg + lane * kStageStride);
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-              srow[i] = make_float4(v[4 * i] * wr, v[4 * i + 1] * wr, v[4 * i + 2] * wr, v[4 * i + 3] * wr);
-            __syncwarp();
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const int rr = q * 32 + 4 * i + (lane >> 3);  // row inside the tile
-              const float4 val = reinterpret_cast<const float4*>(stg + (4 * i + (lane >> 3)) * kStageStride)[lane & 7];
-              if (rr < rt.nrows) reinterpret_cast<float4*>(ybase + (size_t)rr * a.d + 32 * half)[lane & 7] = val;
-            }
-            __syncwarp();
-          };
-          stage_half(v0, 0);
-          stage_half(v1, 1);
-        }
-        continue;
-      }
-      if (!active || lr >= rt.nrows) continue;
-      const int r = rt.row0 + lr;
-      if (a.gate_up) {
-        const float L = a.limit;
-        float* h = v0;  // h overwrites the gate values in place
-        float amax = 0.f;
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const float gc = fminf(v0[j], L);
-          const float uc = fminf(fmaxf(v1[j], -L), L);
-          h[j] = silu_f(gc) * uc;
-          amax = fmaxf(amax, fabsf(h[j]));
-        }
-        const int se = FP4 ? mxfp4_block_exp(amax) : mxfp8_block_exp(amax);
-        const float mul = exp2_neg_int(se);
-        if (FP4) {  // 32 E2M1 codes: 16 bytes at h column mt * 128 + 32 c of a row of f / 2 bytes
-          *reinterpret_cast<uint4*>(a.h_q + (size_t)r * (a.f / 2) + mt * (kKGroup / 2) + 16 * c) = e2m1_block(v0, mul);
-        } else {
-          uint32_t packed[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const uint32_t lo = e4m3x2(h[4 * i] * mul, h[4 * i + 1] * mul);
-            const uint32_t hi = e4m3x2(h[4 * i + 2] * mul, h[4 * i + 3] * mul);
-            packed[i] = lo | (hi << 16);
-          }
-          uint4* dst = reinterpret_cast<uint4*>(a.h_q + (size_t)r * a.f + mt * kKGroup + 32 * c);
-          dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-          dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
-        }
-        a.h_sf[((size_t)ti * (a.f / kKGroup) + mt) * kSfAtomBytes + (lr & 31) * 16 + (lr >> 5) * 4 + c] =
-            (uint8_t)(se + 127);
-      } else {
-        const float wr = a.row_w ? __ldg(&a.row_w[r]) : 1.0f;
-        const size_t col0 = (size_t)mt * kN + 64 * c;
-        if (a.y_f32) {
-          float4* dst = reinterpret_cast<float4*>(a.y_f32 + (size_t)r * a.d + col0);
-#pragma unroll
-          for (int i = 0; i < 8; ++i)
-            dst[i] = make_float4(v0[4 * i] * wr, v0[4 * i + 1] * wr, v0[4 * i + 2] * wr, v0[4 * i + 3] * wr);
-#pragma unroll
-          for (int i = 0; i < 8; ++i)
-            dst[8 + i] = make_float4(v1[4 * i] * wr, v1[4 * i + 1] * wr, v1[4 * i + 2] * wr, v1[4 * i + 3] * wr);
-        } else {
-          uint4* dst = reinterpret_cast<uint4*>(a.y_bf16 + (size_t)r * a.d + col0);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const float* src = i < 4 ? &v0[8 * i] : &v1[8 * (i - 4)];
-            uint4 o;
-            __nv_bfloat162* ov = reinterpret_cast<__nv_bfloat162*>(&o);
-#pragma unroll
-            for (int p = 0; p < 4; ++p) ov[p] = __floats2bfloat162_rn(src[2 * p] * wr, src[2 * p + 1] * wr);
-            dst[i] = o;
-          }
-        }
-      }
+      epilogue_rows<EPI, FP4>(a, rt, ti, mt, q, c, lane,
+                              reinterpret_cast<float*>(smem + C::kEpiOff) + (warp - 2) * kStageFloats, active, v0, v1);
     }
   }
 
@@ -429,6 +458,287 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tbase, C::kTmemCols);
+}
+
+// ---------------------------------------------------------------------------------------------------
+// CTA-pair shape for large expert groups (the prefill chunk): a cluster of two CTAs on two SMs runs every
+// work item as one M = 256 tcgen05.mma.cta_group::2 per K step.  The even CTA (the leader) issues the
+// MMAs; each CTA holds 128 of the 256 token rows (two consecutive 128-row tiles of one expert group) and
+// 128 of the 256 weight rows (gate 128 | up 128 of one FFN slice, or 256 down rows), and receives its own
+// 128 rows of the [256 x 256] fp32 accumulator in its tensor memory.  Against the one-SM kernel each SM
+// stores and reads half the weight tile per stage (16 KB instead of 32 KB of byte-expanded FP4), which
+// leaves room for 6 stages instead of 4, and pulls half the weight bytes from L2.
+//
+// Both CTAs' TMA loads of a stage (weights, activations, and the scale atoms through 2-D maps of
+// 256-byte rows) count their bytes on the leader's `full` barrier (the .cta_group::2 form of the copy);
+// the leader's commits arrive on both CTAs' `empty` and `acc_full` barriers (multicast); the peer's
+// epilogue warps arrive on the leader's `acc_empty` barrier across the cluster.  Every tcgen05 operation
+// of the kernel uses cta_group::2.  Each CTA's tensor memory holds the scale atoms of the whole N = 256
+// (both weight atoms) and of its own 128 activation rows.  The work list pads every expert group to an
+// even number of row tiles, so the two tiles of a pair always belong to the same group.
+template <int STAGES, int EPI>
+struct PairCfg {
+  static constexpr int kRowBytes = 128;                   // one operand row of a stage (K = 128) in smem
+  static constexpr uint32_t kSbo = 8 * kRowBytes;
+  static constexpr int kASlot = kBM * kRowBytes;          // this CTA's 128 token rows
+  static constexpr int kBSlot = (kN / 2) * kRowBytes;     // this CTA's 128 weight rows (FP4 expanded to bytes)
+  static constexpr int kSfSlot = 3 * kSfAtomBytes;        // activation atom, then the two weight atoms
+  static constexpr int kAOff = 0;
+  static constexpr int kBOff = STAGES * kASlot;
+  static constexpr int kSfOff = kBOff + STAGES * kBSlot;
+  static constexpr int kEpiOff = kSfOff + STAGES * kSfSlot;
+  static constexpr int kEpiBytes = EPI ? kEpiWarps * kStageFloats * 4 : 0;
+  static constexpr int kBarOff = kEpiOff + kEpiBytes;
+  static constexpr int kBarBytes = (2 * STAGES + 3) * 8;
+  static constexpr int kSmem = kBarOff + 1024 + kBarBytes;
+  // bytes one CTA's loads of a stage move (global side): packed FP4 weights, activations, three atoms
+  static constexpr uint32_t kTxCta = (kN / 2) * 64 + kBM * kRowBytes + 3 * kSfAtomBytes;
+  static constexpr int kAccCols = kN;
+  static constexpr int kSfCols = 12;
+  static constexpr int kTmemCols = 512;
+  static_assert(kBOff % 1024 == 0 && kSfOff % 1024 == 0, "swizzled tiles need 1024-byte alignment");
+  static_assert(kAccCols + STAGES * kSfCols <= kTmemCols, "TMEM budget");
+  static_assert(kEpiOff % 16 == 0, "staging rows are float4-aligned");
+  static_assert(kSmem <= 232448 - 64, "shared memory budget");
+};
+
+template <int STAGES, int EPI>
+__global__ void __launch_bounds__(kThreads, 1)
+    grouped_mx_gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_w_shared,
+                                const __grid_constant__ CUtensorMap tm_act, const __grid_constant__ CUtensorMap tm_sfw,
+                                const __grid_constant__ CUtensorMap tm_sfw_shared,
+                                const __grid_constant__ CUtensorMap tm_sfa, const GemmArgs a) {
+  using C = PairCfg<STAGES, EPI>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
+  uint64_t* empty = full + STAGES;
+  uint64_t* acc_full = empty + STAGES;
+  uint64_t* acc_empty = acc_full + 1;
+  uint64_t* drain = acc_empty + 1;
+  __shared__ uint32_t tmem_slot;
+  __shared__ volatile int abort_flag;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int pair = (int)(blockIdx.x >> 1), n_pairs = (int)(gridDim.x >> 1);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);  // the leader's producer (expect_tx of both CTAs' bytes); unused in the peer
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(acc_full, 1);
+    mbar_init(acc_empty, 2 * kEpiWarps);  // drain warps of both CTAs; only the leader's is used
+    mbar_init(drain, 1);
+    abort_flag = 0;
+    mbar_fence_init();
+  }
+  if (warp == 0) {
+    prefetch_tensormap(&tm_w);
+    prefetch_tensormap(&tm_w_shared);
+    prefetch_tensormap(&tm_act);
+    prefetch_tensormap(&tm_sfw);
+    prefetch_tensormap(&tm_sfw_shared);
+    prefetch_tensormap(&tm_sfa);
+  }
+  if (warp == 1) tmem_alloc_pair(&tmem_slot, C::kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();  // both CTAs' barriers exist before any remote arrival
+  tc_fence_after();
+  const uint32_t tbase = tmem_slot;
+  pdl_wait();
+  int n_tiles = *reinterpret_cast<const volatile int32_t*>(a.n_tiles);
+  if (n_tiles > a.max_tiles) n_tiles = a.max_tiles;
+  const int total = (n_tiles >> 1) * a.m_tiles;  // work items: (tile pair, output tile)
+  const int n_items = total > pair ? (total - pair + n_pairs - 1) / n_pairs : 0;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------------------------------------------------------- TMA producer (both CTAs)
+      const uint64_t pol_w = l2_policy_evict_first();
+      const uint64_t pol_a = l2_policy_evict_last();
+      const uint32_t full0 = mapa_shared(smem_addr(&full[0]), 0);  // the leader's barriers
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued = 0, last_par = 0;
+      bool ok = true;
+      for (int w = pair; w < total && ok && !a.stall_loads; w += n_pairs) {
+        const int pi = w / a.m_tiles, mt = w - pi * a.m_tiles;
+        const int ti = 2 * pi + (int)rank;  // this CTA's row tile
+        const RowTile rt = a.tiles[ti];
+        const int g = a.tiles[2 * pi].group;
+        const bool sh = g == a.E;
+        const CUtensorMap* tw = sh ? &tm_w_shared : &tm_w;
+        const CUtensorMap* tsw = sh ? &tm_sfw_shared : &tm_sfw;
+        const int e = sh ? 0 : g;
+        const int slab = e * a.KG * a.m_tiles + mt;  // packed weights [expert][K group][output tile]
+        for (int kg = 0; kg < a.KG; ++kg) {
+          if (abort_flag || !mbar_wait(&empty[stage], phase ^ 1u, a.budget_ns)) {
+            ok = false;
+            break;
+          }
+          if (leader) mbar_arrive_expect_tx(&full[stage], 2 * C::kTxCta);
+          const uint32_t fb = full0 + (uint32_t)(stage * 8);
+          const int sl = slab + kg * a.m_tiles;
+          tma_load_2d_pair(smem + C::kBOff + stage * C::kBSlot, tw, 0, sl * kN + (int)rank * (kN / 2), fb, pol_w);
+          tma_load_2d_pair(smem + C::kAOff + stage * C::kASlot, &tm_act, kg * C::kRowBytes, rt.row0, fb, pol_a);
+          uint8_t* sf = smem + C::kSfOff + stage * C::kSfSlot;
+          tma_load_2d_pair(sf, &tm_sfa, 0, 2 * (ti * a.KG + kg), fb, pol_a);  // one atom: 2 rows of 256 B
+          tma_load_2d_pair(sf + kSfAtomBytes, tsw, 0, 4 * sl, fb, pol_w);     // two atoms: 4 rows
+          issued |= 1u << stage;
+          last_par = (last_par & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        set_status(a.status, DEV_TIMEOUT);
+        abort_flag = 1;
+        // the leader's barriers count both CTAs' copies: let those in flight land before shared memory goes
+        if (leader)
+          for (int s = 0; s < STAGES; ++s)
+            if ((issued >> s) & 1u) (void)mbar_wait(&full[s], (last_par >> s) & 1u, 20000000ull);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && leader) {
+      // ---------------------------------------------------------------- MMA issuer (leader only)
+      // The one-SM issuer's structure (fused stage blocks, scale copies up to kAhead stages early) with the
+      // pair's forms: M = 256, commits multicast to both CTAs.
+      constexpr uint32_t kIdesc0 = mma_idesc(0, 5, 2 * kBM, kN, 0, 0);
+      constexpr int kAhead = 2;
+      static_assert(STAGES > kAhead, "scale copies run up to kAhead stages ahead of the MMAs");
+      const uint64_t a_desc0 = smem_desc(smem_addr(smem + C::kAOff), 16, C::kSbo, 2);
+      const uint64_t b_desc0 = smem_desc(smem_addr(smem + C::kBOff), 16, C::kSbo, 2);
+      const uint64_t sf_desc0 = smem_desc(smem_addr(smem + C::kSfOff), 128, 128, 0);
+      const uint32_t sf_tmem0 = tbase + (uint32_t)C::kAccCols;
+      auto copy_sf = [&](int slot) {
+        const uint64_t dsc = sf_desc0 + (uint64_t)((slot * C::kSfSlot) >> 4);
+        const uint32_t t = sf_tmem0 + (uint32_t)(slot * C::kSfCols);
+        tc_copy_sf_pair(t, dsc);
+        tc_copy_sf_pair(t + 4, dsc + (kSfAtomBytes >> 4));
+        tc_copy_sf_pair(t + 8, dsc + 2 * (kSfAtomBytes >> 4));
+      };
+      const int n_st = n_items * a.KG;
+      bool ok = true, any = false;
+      int cs = 0;
+      uint32_t cph = 0;
+      int lg = 0, ls = 0;
+      uint32_t lph = 0;
+      int g = 0, kg = 0, item = 0;
+      while (g < n_st) {  // the one-SM issuer's loop structure: waits only in the outer loop
+        if (kg == 0) {  // both CTAs' epilogues must have drained the accumulator
+          if (abort_flag || !mbar_wait_cluster(acc_empty, ((uint32_t)item & 1u) ^ 1u, a.budget_ns)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+        }
+        if (lg == g) {
+          if (abort_flag || !mbar_wait(&full[ls], lph, a.budget_ns)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          copy_sf(ls);
+          ++lg;
+          if (++ls == STAGES) {
+            ls = 0;
+            lph ^= 1u;
+          }
+        }
+        for (;;) {
+          const bool look = lg < n_st && lg <= g + kAhead;
+          const uint64_t ad = a_desc0 + (uint64_t)((cs * C::kASlot) >> 4);
+          const uint64_t bd = b_desc0 + (uint64_t)((cs * C::kBSlot) >> 4);
+          const uint32_t sfa = sf_tmem0 + (uint32_t)(cs * C::kSfCols);
+          const bool landed = tc_stage4_mx_pair_commit_poll(tbase, ad, bd, kIdesc0, sfa, sfa + 4, kg != 0 ? 1u : 0u,
+                                                            &empty[cs], look ? &full[ls] : &full[cs],
+                                                            look ? lph : cph);
+          any = true;
+          if (look && landed) {
+            tc_fence_after();
+            copy_sf(ls);
+            ++lg;
+            if (++ls == STAGES) {
+              ls = 0;
+              lph ^= 1u;
+            }
+          }
+          if (++cs == STAGES) {
+            cs = 0;
+            cph ^= 1u;
+          }
+          ++g;
+          if (++kg == a.KG) {
+            tc_commit_pair(acc_full);
+            kg = 0;
+            ++item;
+            break;
+          }
+          if (lg == g) break;
+        }
+      }
+      if (!ok) {
+        set_status(a.status, DEV_TIMEOUT);
+        abort_flag = 1;
+      }
+      if (any) {  // all issued MMAs must retire before either CTA releases its tensor memory
+        tc_commit_pair(drain);
+        if (!mbar_wait(drain, 0, a.budget_ns)) set_status(a.status, DEV_TIMEOUT);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------------ epilogue (warps 2..17, both CTAs)
+    const int q = warp & 3;
+    const int c = (warp - 2) >> 2;
+    const uint32_t acc_empty_leader = mapa_shared(smem_addr(acc_empty), 0);
+    int it = 0;
+    for (int w = pair; w < total; w += n_pairs, ++it) {
+      bool got = !abort_flag && mbar_wait(acc_full, (uint32_t)it & 1u, a.budget_ns);
+      got = __all_sync(0xFFFFFFFFu, got);
+      if (!got) {
+        if (lane == 0) {
+          set_status(a.status, DEV_TIMEOUT);
+          abort_flag = 1;
+        }
+        break;
+      }
+      tc_fence_after();
+      const int pi = w / a.m_tiles, mt = w - pi * a.m_tiles;
+      const int ti = 2 * pi + (int)rank;
+      const RowTile rt = a.tiles[ti];
+      const bool active = q * 32 < rt.nrows;  // warp-uniform
+      const uint32_t tl = tbase + ((uint32_t)(q * 32) << 16);
+      float v0[32], v1[32];
+      if (active) {
+        tmem_ld32(tl + (uint32_t)(a.gate_up ? 32 * c : 64 * c), v0);
+        tmem_ld32(tl + (uint32_t)(a.gate_up ? 128 + 32 * c : 64 * c + 32), v1);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if (leader)
+          mbar_arrive(acc_empty);
+        else
+          mbar_arrive_remote(acc_empty_leader);
+      }
+      epilogue_rows<EPI, false>(a, rt, ti, mt, q, c, lane,
+                                reinterpret_cast<float*>(smem + C::kEpiOff) + (warp - 2) * kStageFloats, active, v0,
+                                v1);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();  // neither CTA releases its tensor or shared memory while the pair still uses them
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc_pair(tbase, C::kTmemCols);
 }
 
 template <int STAGES, int AROWS, int EPI, bool FP4>
@@ -445,14 +755,62 @@ cudaError_t launch_shape(const CUtensorMap& w, const CUtensorMap& w_sh, const CU
                     w_sh, act, act_small, a);
 }
 
+// CTA-pair launch: clusters of two CTAs with programmatic dependent launch.  The grid is as many pairs as
+// the device co-schedules at one CTA per SM (the occupancy query, once per device), at most num_sms / 2.
+template <int STAGES, int EPI>
+cudaError_t launch_pair(const PairMaps& pm, const CUtensorMap& act, const GemmArgs& a, int num_sms, cudaStream_t s) {
+  using C = PairCfg<STAGES, EPI>;
+  auto kernel = grouped_mx_gemm_pair_kernel<STAGES, EPI>;
+  static PerDeviceOnce smem_optin;
+  cudaError_t e = smem_optin.run(
+      [&] { return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem); });
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = C::kSmem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  static std::atomic<int> pairs_cached[64];  // per device; 0 = not queried yet
+  int dev = 0;
+  e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  int pairs = dev >= 0 && dev < 64 ? pairs_cached[dev].load(std::memory_order_relaxed) : 0;
+  if (pairs == 0) {
+    cfg.gridDim = dim3(2 * (num_sms / 2));
+    cfg.numAttrs = 1;
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, kernel, &cfg);
+    if (e != cudaSuccess) return e;
+    pairs = n < 1 ? 1 : (n > num_sms / 2 ? num_sms / 2 : n);
+    if (dev >= 0 && dev < 64) pairs_cached[dev].store(pairs, std::memory_order_relaxed);
+  }
+  cfg.gridDim = dim3(2 * pairs);
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kernel, pm.w, pm.w_shared, act, pm.sfw, pm.sfw_shared, pm.sfa, a);
+}
+
 // tile_rows 32: 6 stages of 32-row activation slots.  tile_rows 128: 4 stages of 128-row slots, or for
 // the down projection's fp32 rows 3 stages plus the epilogue's staging buffers (the 16-byte scattered
 // stores of the direct epilogue bound that GEMM at the 8192-token shape: 835 us with them, 373 us
 // without any stores).
 // FP4: the packed weight ring is half as large, so every shape holds more stages.
+// pair (128-row tiles, MXFP8 activations): the CTA-pair kernel, 6 stages for gate-up; 4 stages plus the
+// staging buffers for the fp32 down rows; 5 stages for bf16 down rows (the grouped FFN call).
 cudaError_t launch_grouped(const CUtensorMap& w, const CUtensorMap& w_sh, const CUtensorMap& act,
                            const CUtensorMap& act_small, const GemmArgs& a, int tile_rows, int act_fp4, int num_sms,
-                           cudaStream_t s) {
+                           cudaStream_t s, const PairMaps* pair) {
+  if (pair && tile_rows == kBM && !act_fp4) {
+    if (a.gate_up) return launch_pair<6, 0>(*pair, act, a, num_sms, s);
+    if (a.y_f32) return launch_pair<4, 1>(*pair, act, a, num_sms, s);
+    return launch_pair<5, 0>(*pair, act, a, num_sms, s);
+  }
   if (act_fp4) {
     if (tile_rows == kSmallRows) return launch_shape<8, kSmallRows, 0, true>(w, w_sh, act, act_small, a, num_sms, s);
     if (!a.gate_up && a.y_f32) return launch_shape<6, kBM, 1, true>(w, w_sh, act, act_small, a, num_sms, s);
@@ -470,7 +828,7 @@ cudaError_t launch_gemm_gate_up(const CUtensorMap& w_routed, const CUtensorMap& 
                                 const uint8_t* act_sf, const RowTile* tiles, const int32_t* n_tiles, int max_tiles,
                                 int E, int d, int f, float limit, uint8_t* h_q, uint8_t* h_sf, int* status,
                                 uint64_t wait_budget_ns, int stall_loads, int tile_rows, int act_fp4, int num_sms,
-                                cudaStream_t s) {
+                                cudaStream_t s, const PairMaps* pair) {
   GemmArgs a{};
   a.sf_routed = sf_routed;
   a.sf_shared = sf_shared ? sf_shared : sf_routed;
@@ -490,7 +848,7 @@ cudaError_t launch_gemm_gate_up(const CUtensorMap& w_routed, const CUtensorMap& 
   a.status = status;
   a.budget_ns = wait_budget_ns;
   a.stall_loads = stall_loads;
-  return launch_grouped(w_routed, w_shared, act, act_small, a, tile_rows, act_fp4, num_sms, s);
+  return launch_grouped(w_routed, w_shared, act, act_small, a, tile_rows, act_fp4, num_sms, s, pair);
 }
 
 cudaError_t launch_gemm_down(const CUtensorMap& w_routed, const CUtensorMap& w_shared, const uint8_t* sf_routed,
@@ -498,7 +856,7 @@ cudaError_t launch_gemm_down(const CUtensorMap& w_routed, const CUtensorMap& w_s
                              const uint8_t* act_sf, const RowTile* tiles, const int32_t* n_tiles, int max_tiles, int E,
                              int d, int f, const float* row_w, float* y_f32, __nv_bfloat16* y_bf16, int* status,
                              uint64_t wait_budget_ns, int stall_loads, int tile_rows, int act_fp4, int num_sms,
-                             cudaStream_t s) {
+                             cudaStream_t s, const PairMaps* pair) {
   GemmArgs a{};
   a.sf_routed = sf_routed;
   a.sf_shared = sf_shared ? sf_shared : sf_routed;
@@ -518,7 +876,7 @@ cudaError_t launch_gemm_down(const CUtensorMap& w_routed, const CUtensorMap& w_s
   a.status = status;
   a.budget_ns = wait_budget_ns;
   a.stall_loads = stall_loads;
-  return launch_grouped(w_routed, w_shared, act, act_small, a, tile_rows, act_fp4, num_sms, s);
+  return launch_grouped(w_routed, w_shared, act, act_small, a, tile_rows, act_fp4, num_sms, s, pair);
 }
 
 }  // namespace moe

@@ -165,7 +165,7 @@ cudaError_t launch_histogram(const int32_t* ids, int T, int k, int E, int G, int
                              cudaStream_t s);
 cudaError_t launch_scan(int32_t* chunk_hist, int n_chunks, int T, int E, int G, int has_shared, int bn, int max_tiles,
                         int32_t* counts, int32_t* offsets, int32_t* tile_off, int32_t* n_tiles, RowTile* tiles,
-                        int* status, cudaStream_t s);
+                        int* status, cudaStream_t s, int pad_pairs = 0);
 // Quantise x to MXFP8 (act_fp4: MXFP4, rows of d/2 bytes) and scatter each token row to its k routed
 // rows (+ its shared row).  a_sf_atoms / a_s_rows may each be null (kernel-layout scale atoms /
 // canonical [rows, d/32]).
@@ -179,9 +179,11 @@ cudaError_t launch_rows_sf_to_atoms(const uint8_t* a_s_rows, const RowTile* tile
 // Per-tile atoms -> canonical [rows, K/32] (reads back the h scales for tests).
 cudaError_t launch_atoms_to_rows_sf(const uint8_t* atoms, const RowTile* tiles, const int32_t* n_tiles, int K,
                                     int max_tiles, uint8_t* rows_sf, cudaStream_t s);
+// pad_pairs: every group's tile count is rounded up to an even number (the padding tile has no rows), so
+// that tiles 2p and 2p + 1 belong to one group (the CTA-pair GEMM shape).
 cudaError_t launch_tiles_from_offsets(const int32_t* offsets, int G, int n_rows, int bn, int max_tiles,
                                       int32_t* tile_off, int32_t* n_tiles, RowTile* tiles, int* status,
-                                      cudaStream_t s);
+                                      cudaStream_t s, int pad_pairs = 0);
 
 // Weight repacking at handle creation.  mode 0: gate-up rows [n, 2f, K] (gate rows 0..f-1, up rows
 // f..2f-1); mode 1: down rows [n, d, K].  Packed codes [n, K/128, rows/256, 256, 64 B]: each 256-row
@@ -191,6 +193,13 @@ cudaError_t launch_pack_weights(const uint8_t* codes, int n, int rows, int K, in
                                 cudaStream_t s);
 cudaError_t launch_pack_weight_sf(const uint8_t* sc, int n, int rows, int K, int mode, uint8_t* atoms,
                                   cudaStream_t s);
+
+// Tensor maps of the CTA-pair shape of the grouped GEMMs (large expert groups, MXFP8 activations).
+struct PairMaps {
+  CUtensorMap w, w_shared;      // weight codes with 128-row boxes (one CTA's half of a 256-row slab)
+  CUtensorMap sfw, sfw_shared;  // weight scale atoms as rows of 256 B, 4-row boxes (both atoms of a slab)
+  CUtensorMap sfa;              // activation (gate-up) or h (down) scale atoms, 2-row boxes (one atom)
+};
 
 // Grouped GEMMs.  act_fp4 = 0: MXFP8 activations (E4M3 rows of K bytes) x MXFP4 weights on
 // kind::mxf8f6f4, weight maps of 16U4_ALIGN16B type (K = 128 elements expanded to 128-byte rows);
@@ -202,14 +211,16 @@ cudaError_t launch_gemm_gate_up(const CUtensorMap& w_routed, const CUtensorMap& 
                                 const RowTile* tiles, const int32_t* n_tiles, int max_tiles, int E, int d, int f,
                                 float limit,
                                 uint8_t* h_q, uint8_t* h_sf, int* status, uint64_t wait_budget_ns, int stall_loads,
-                                int tile_rows, int act_fp4, int num_sms, cudaStream_t s);
+                                int tile_rows, int act_fp4, int num_sms, cudaStream_t s,
+                                const PairMaps* pair = nullptr);
 cudaError_t launch_gemm_down(const CUtensorMap& w_routed, const CUtensorMap& w_shared, const uint8_t* sf_routed,
                              const uint8_t* sf_shared, const CUtensorMap& act, const CUtensorMap& act_small,
                              const uint8_t* act_sf,
                              const RowTile* tiles, const int32_t* n_tiles, int max_tiles, int E, int d, int f,
                              const float* row_w, float* y_f32, __nv_bfloat16* y_bf16, int* status,
                              uint64_t wait_budget_ns, int stall_loads, int tile_rows, int act_fp4, int num_sms,
-                             cudaStream_t s);
+                             cudaStream_t s,
+                                const PairMaps* pair = nullptr);
 
 // out_f32 non-NULL: the fp32 sums go there instead, without the rounding to bf16 (out is then unused).
 cudaError_t launch_combine(const float* y_rows, const int32_t* inv_pos, int T, int d, int k, int R, int has_shared,

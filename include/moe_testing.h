@@ -24,6 +24,14 @@ extern "C" {
 MOE_API moe_status_t moe_testing_stall_loads(moe_experts_t experts, int32_t enable);
 
 /*
+ * enable = 0: later calls on this handle run batches with 128-row tiles on the one-SM grouped GEMMs
+ * instead of the CTA-pair ones (two SMs per work item, M = 256; the default for MXFP8 activations);
+ * enable != 0 restores the default.  Both give results that agree with the oracle; tests compare them,
+ * and benchmarks use it to measure one against the other.  Errors: MOE_ERR_INVALID_ARG (NULL handle).
+ */
+MOE_API moe_status_t moe_testing_set_pair_gemm(moe_experts_t experts, int32_t enable);
+
+/*
  * Reads back the SwiGLU output h of the last moe_forward / moe_expert_ffn on this handle, as the
  * down projection consumed it: *n_rows receives its row count (the call's routed rows in permuted
  * order, then one shared row per token in token order; 0 if there was none), h_q [n_rows, d_ff]
