@@ -48,8 +48,8 @@ def parse_args():
     p.add_argument("--workloads", default="all",
                    help="after the headline, also measure these workloads into the line's 'workloads' object: "
                         "'all' (the five layer configurations), 'none', or a comma-separated list (one GPU only)")
-    p.add_argument("--one-sm-gemm", action="store_true",
-                   help="run 128-row tiles on the one-SM grouped GEMMs instead of CTA pairs (for A/B comparisons)")
+    p.add_argument("--pair-gemm", action="store_true",
+                   help="run 128-row tiles on the CTA-pair grouped GEMMs instead of the one-SM kernels (A/B comparisons)")
     p.add_argument("--cpu-seconds-other", type=float, default=4.0,
                    help="target CPU time of the oracle baseline sample of each extra workload")
     return p.parse_args()
@@ -309,9 +309,9 @@ def measure_layer(args, wl, inp, dev, world, rank, mx_peak, mma_name, cpu_target
     fp4 = args.act == "mxfp4"
     # the router weights are made resident once, like the expert weights (moe_experts_set_router)
     layer = moe.MoELayer.from_host(inp, device=dev, max_T=wl.T, act=args.act, resident_router=True)
-    if args.one_sm_gemm:
+    if args.pair_gemm:
         for h in (layer.h, layer.h_shared):
-            moe.moe_testing_set_pair_gemm(h, False)
+            moe.moe_testing_set_pair_gemm(h, True)
     x = torch.from_numpy(inp.x.view(np.int16)).to(dev).view(torch.bfloat16)
     out = torch.empty((wl.T, wl.d), dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -362,9 +362,11 @@ def measure_layer(args, wl, inp, dev, world, rank, mx_peak, mma_name, cpu_target
     torch.cuda.synchronize()
     moe.moe_set_stage_events(layer.h, None)
     layer.check()
-    stage_ms = {name: statistics.mean(ev[i].elapsed_time(ev[i + 1]) for ev in events)
+    # medians over the steps: one step held up on the host (the events time the GPU between launches)
+    # must not decide which kernel is the dominant one
+    stage_ms = {name: statistics.median(ev[i].elapsed_time(ev[i + 1]) for ev in events)
                 for i, name in enumerate(moe.STAGE_NAMES)}
-    ms_staged = max_over_ranks(statistics.mean(ev[0].elapsed_time(ev[-1]) for ev in events), dev)
+    ms_staged = max_over_ranks(statistics.median(ev[0].elapsed_time(ev[-1]) for ev in events), dev)
 
     # ---- end to end: pinned host x in, bf16 out back to the host, every step.  The headline runs the steps
     # as a serving loop would: two device buffers, the H2D copy of step i+1 and the D2H copy of step i-1 on
@@ -486,7 +488,7 @@ def measure_layer(args, wl, inp, dev, world, rank, mx_peak, mma_name, cpu_target
     rec = {
         "ms_per_step": ms, "value": job_tokens_per_s(world, wl.T, ms), "unit": "tokens/s",
         "config": dict(workload_config(wl, args.act), touched_experts=touched, parallelism=f"replicas x{world}",
-                       gemm="one-SM" if args.one_sm_gemm or wl.T * wl.k <= 16 * wl.E or fp4 else "CTA pairs"),
+                       gemm="CTA pairs" if args.pair_gemm and wl.T * wl.k > 16 * wl.E and not fp4 else "one-SM"),
         "roofline": roof,
         "layer_roofline": layer_roof,
         "gemm_tensor": {"achieved": layer_fl / ((stage_ms["gemm_gate_up"] + stage_ms["gemm_down"]) * 1e-3) / 1e12,
@@ -494,7 +496,7 @@ def measure_layer(args, wl, inp, dev, world, rank, mx_peak, mma_name, cpu_target
                         "frac": layer_fl / ((stage_ms["gemm_gate_up"] + stage_ms["gemm_down"]) * 1e-3) / 1e12 / mx_peak},
         "stage_ms": stage_ms,
         "stage_timing": {"ms_per_step": ms_staged, "how": "second pass of the same steps with CUDA events "
-                         "between the stages (events serialise the launches there)"},
+                         "between the stages (events serialise the launches there); medians over the steps"},
         "e2e": {"value": job_tokens_per_s(world, wl.T, ms_e2e), "unit": "tokens/s",
                 "h2d_bytes_per_step": wl.T * wl.d * 2 + (wl.T * 4 if wl.hashed else 0),
                 "d2h_bytes_per_step": wl.T * wl.d * 2, "ms_per_step": ms_e2e,

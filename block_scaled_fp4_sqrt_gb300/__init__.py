@@ -226,7 +226,7 @@ def moe_testing_read_h(h, f: int, act: str, stream=None):
 
 
 def moe_testing_set_pair_gemm(h, enable: bool) -> None:
-    """Run 128-row tiles on CTA-pair GEMMs (the default) or on the one-SM kernels."""
+    """Run 128-row tiles on the CTA-pair GEMMs, or on the one-SM kernels (the default)."""
     _ok("moe_testing_set_pair_gemm", lib().moe_testing_set_pair_gemm(h, 1 if enable else 0))
 
 

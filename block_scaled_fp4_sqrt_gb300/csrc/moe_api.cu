@@ -51,7 +51,7 @@ struct moe_experts_s {
   int32_t last_fwd_T = -1;     // T of the last moe_forward (its fp32 expert rows stay in the workspace), or -1
   int32_t last_fwd_shared = 0;  // whether that forward had a shared expert
   int stall_loads = 0;
-  int pair_gemm = 1;  // 128-row tiles on CTA pairs (moe_testing_set_pair_gemm)
+  int pair_gemm = 0;  // 128-row tiles on CTA pairs (moe_testing_set_pair_gemm); one-SM kernels by default
   void* const* stage_events = nullptr;  // MOE_N_STAGES + 1 caller-owned cudaEvent_t, or null
   // Changes whenever something a recorded launch sequence depends on changes (workspace, router, hash
   // table, activation format, wait budget, test hooks, stage events): a stack's cached graph compares it.
@@ -558,7 +558,7 @@ static int tile_rows_for(int rows, int groups) {
   return rows <= 16 * groups ? kSmallTileRows : kTileRows;
 }
 
-// 128-row tiles of MXFP8 activations run on CTA pairs (moe_set_pair_gemm can switch that off).
+// 128-row tiles of MXFP8 activations run on CTA pairs when the handle asks for it (moe_testing_set_pair_gemm).
 static bool use_pairs(const moe_experts_s* h, int tile_rows) {
   return tile_rows == kTileRows && !h->act_fp4 && h->pair_gemm;
 }

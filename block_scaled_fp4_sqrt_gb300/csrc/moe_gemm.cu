@@ -47,11 +47,13 @@ constexpr int kSmallRows = 32;  // groups this small load a 32-row activation bo
 constexpr int kEpiWarps = 16;
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 
-// Staging buffer of one epilogue warp for coalesced fp32 row stores: 32 rows x 32 columns, rows 144 B
-// apart (36 floats) so that the row-per-lane writes and the line-per-quarter-warp reads are both free
-// of bank conflicts.
+// Staging buffer of one epilogue warp for coalesced fp32 row stores: 8 rows x 32 columns (the warp's 32
+// rows pass through it 8 at a time), rows 144 B apart (36 floats) so that the row-per-lane writes and the
+// line-per-quarter-warp reads are both free of bank conflicts.  8 rows rather than 32 leave the shared
+// memory to one more pipeline stage of the down GEMM.
 constexpr int kStageStride = 36;
-constexpr int kStageFloats = 32 * kStageStride;
+constexpr int kStageRows = 8;
+constexpr int kStageFloats = kStageRows * kStageStride;
 
 // EPI = 1: the down projection's fp32 rows leave through a per-warp shared-memory transpose (full
 // 128-byte lines per quarter warp) instead of 16-byte stores to 32 different rows per instruction.
@@ -128,25 +130,32 @@ __device__ __forceinline__ void epilogue_rows(const GemmArgs& a, const RowTile& 
                                               int lane, float* stg, bool active, float (&v0)[32], float (&v1)[32]) {
   const int lr = q * 32 + lane;  // token row inside the tile
   if (EPI && !a.gate_up) {
-    // fp32 rows through the warp's staging buffer: lane l writes its row's 32 values, then each
-    // quarter warp stores one row's 128 contiguous bytes
+    // fp32 rows through the warp's staging buffer
     if (active) {
       const bool row_ok = lr < rt.nrows;
       const float wr = !row_ok ? 0.f : (a.row_w ? __ldg(&a.row_w[rt.row0 + lr]) : 1.0f);
       float* ybase = a.y_f32 + (size_t)rt.row0 * a.d + (size_t)mt * kN + 64 * c;
+      // lanes 8p .. 8p+7 write their rows' 32 values into the buffer; then each quarter warp stores one
+      // buffered row's 128 contiguous bytes (two rows per quarter warp and pass)
       auto stage_half = [&](const float(&v)[32], int half) {
-        float4* srow = reinterpret_cast<float4*>(stg + lane * kStageStride);
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-          srow[i] = make_float4(v[4 * i] * wr, v[4 * i + 1] * wr, v[4 * i + 2] * wr, v[4 * i + 3] * wr);
-        __syncwarp();
+        for (int p = 0; p < 32 / kStageRows; ++p) {
+          if ((lane >> 3) == p) {
+            float4* srow = reinterpret_cast<float4*>(stg + (lane & 7) * kStageStride);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int rr = q * 32 + 4 * i + (lane >> 3);  // row inside the tile
-          const float4 val = reinterpret_cast<const float4*>(stg + (4 * i + (lane >> 3)) * kStageStride)[lane & 7];
-          if (rr < rt.nrows) reinterpret_cast<float4*>(ybase + (size_t)rr * a.d + 32 * half)[lane & 7] = val;
+            for (int i = 0; i < 8; ++i)
+              srow[i] = make_float4(v[4 * i] * wr, v[4 * i + 1] * wr, v[4 * i + 2] * wr, v[4 * i + 3] * wr);
+          }
+          __syncwarp();
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            const int br = 4 * i + (lane >> 3);  // buffered row
+            const int rr = q * 32 + 8 * p + br;  // row inside the tile
+            const float4 val = reinterpret_cast<const float4*>(stg + br * kStageStride)[lane & 7];
+            if (rr < rt.nrows) reinterpret_cast<float4*>(ybase + (size_t)rr * a.d + 32 * half)[lane & 7] = val;
+          }
+          __syncwarp();
         }
-        __syncwarp();
       };
       stage_half(v0, 0);
       stage_half(v1, 1);
@@ -216,9 +225,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                            const __grid_constant__ CUtensorMap tm_act, const __grid_constant__ CUtensorMap tm_act_small,
                            const GemmArgs a) {
   using C = Cfg<STAGES, AROWS, EPI, FP4>;
-  // The accumulator handoff (acc_full / acc_empty) is polled in the 32-row shape: there only the issuer and
-  // four epilogue warps run, and polling took 4 % off the T = 8 step (measured).  With 128-row tiles the 16
-  // polling epilogue warps took issue slots from the producer and issuer (the T = 8192 step 2 % slower).
+  // The accumulator handoff: the issuer polls acc_empty in both shapes (one thread, nothing else to do).
+  // The epilogue warps poll acc_full in the 32-row shape: there only the issuer and four epilogue warps
+  // run, and polling took 4 % off the T = 8 step (measured).  With 128-row tiles the 16 polling epilogue
+  // warps took issue slots from the producer and issuer (the T = 8192 step 2 % slower), so they suspend.
   constexpr bool kPollHandoff = AROWS == kSmallRows;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -265,7 +275,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     if (lane == 0) {
       // ---------------------------------------------------------------- TMA producer
-      const uint64_t pol_w = l2_policy_evict_first();  // weights: streamed once per row tile
+      // weights: streamed once by the 32-row (verify) shape; with 128-row tiles an expert's slab is read by
+      // each of its row tiles, which the CTAs walk at about the same time, so let those reads hit in L2
+      const uint64_t pol_w = AROWS == kSmallRows ? l2_policy_evict_first() : l2_policy_evict_normal();
       const uint64_t pol_a = l2_policy_evict_last();   // activations: re-read by every output tile
       int stage = 0;
       uint32_t phase = 0;
@@ -352,8 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       while (g < n_st) {
         if (kg == 0) {  // a new work item: the epilogue must have drained the accumulator
           const uint32_t par = ((uint32_t)item & 1u) ^ 1u;
-          if (abort_flag || !(kPollHandoff ? mbar_spin(acc_empty, par, a.budget_ns)
-                                           : mbar_wait(acc_empty, par, a.budget_ns))) {
+          if (abort_flag || !mbar_spin(acc_empty, par, a.budget_ns)) {
             ok = false;
             break;
           }
@@ -558,7 +569,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     if (lane == 0) {
       // ---------------------------------------------------------------- TMA producer (both CTAs)
-      const uint64_t pol_w = l2_policy_evict_first();
+      const uint64_t pol_w = l2_policy_evict_normal();  // an expert's slab is read by each of its tile pairs
       const uint64_t pol_a = l2_policy_evict_last();
       const uint32_t full0 = mapa_shared(smem_addr(&full[0]), 0);  // the leader's barriers
       int stage = 0;
@@ -796,28 +807,28 @@ cudaError_t launch_pair(const PairMaps& pm, const CUtensorMap& act, const GemmAr
   return cudaLaunchKernelEx(&cfg, kernel, pm.w, pm.w_shared, act, pm.sfw, pm.sfw_shared, pm.sfa, a);
 }
 
-// tile_rows 32: 6 stages of 32-row activation slots.  tile_rows 128: 4 stages of 128-row slots, or for
-// the down projection's fp32 rows 3 stages plus the epilogue's staging buffers (the 16-byte scattered
+// tile_rows 32: 6 stages of 32-row activation slots.  tile_rows 128: 4 stages of 128-row slots, also for
+// the down projection's fp32 rows next to the epilogue's staging buffers (the 16-byte scattered
 // stores of the direct epilogue bound that GEMM at the 8192-token shape: 835 us with them, 373 us
 // without any stores).
 // FP4: the packed weight ring is half as large, so every shape holds more stages.
-// pair (128-row tiles, MXFP8 activations): the CTA-pair kernel, 6 stages for gate-up; 4 stages plus the
-// staging buffers for the fp32 down rows; 5 stages for bf16 down rows (the grouped FFN call).
+// pair (128-row tiles, MXFP8 activations): the CTA-pair kernel, 6 stages for gate-up and for the fp32 down
+// rows (next to their staging buffers); 5 stages for bf16 down rows (the grouped FFN call).
 cudaError_t launch_grouped(const CUtensorMap& w, const CUtensorMap& w_sh, const CUtensorMap& act,
                            const CUtensorMap& act_small, const GemmArgs& a, int tile_rows, int act_fp4, int num_sms,
                            cudaStream_t s, const PairMaps* pair) {
   if (pair && tile_rows == kBM && !act_fp4) {
     if (a.gate_up) return launch_pair<6, 0>(*pair, act, a, num_sms, s);
-    if (a.y_f32) return launch_pair<4, 1>(*pair, act, a, num_sms, s);
+    if (a.y_f32) return launch_pair<6, 1>(*pair, act, a, num_sms, s);
     return launch_pair<5, 0>(*pair, act, a, num_sms, s);
   }
   if (act_fp4) {
     if (tile_rows == kSmallRows) return launch_shape<8, kSmallRows, 0, true>(w, w_sh, act, act_small, a, num_sms, s);
-    if (!a.gate_up && a.y_f32) return launch_shape<6, kBM, 1, true>(w, w_sh, act, act_small, a, num_sms, s);
+    if (!a.gate_up && a.y_f32) return launch_shape<8, kBM, 1, true>(w, w_sh, act, act_small, a, num_sms, s);
     return launch_shape<8, kBM, 0, true>(w, w_sh, act, act_small, a, num_sms, s);
   }
   if (tile_rows == kSmallRows) return launch_shape<6, kSmallRows, 0, false>(w, w_sh, act, act_small, a, num_sms, s);
-  if (!a.gate_up && a.y_f32) return launch_shape<3, kBM, 1, false>(w, w_sh, act, act_small, a, num_sms, s);
+  if (!a.gate_up && a.y_f32) return launch_shape<4, kBM, 1, false>(w, w_sh, act, act_small, a, num_sms, s);
   return launch_shape<4, kBM, 0, false>(w, w_sh, act, act_small, a, num_sms, s);
 }
 

@@ -24,10 +24,13 @@ extern "C" {
 MOE_API moe_status_t moe_testing_stall_loads(moe_experts_t experts, int32_t enable);
 
 /*
- * enable = 0: later calls on this handle run batches with 128-row tiles on the one-SM grouped GEMMs
- * instead of the CTA-pair ones (two SMs per work item, M = 256; the default for MXFP8 activations);
- * enable != 0 restores the default.  Both give results that agree with the oracle; tests compare them,
- * and benchmarks use it to measure one against the other.  Errors: MOE_ERR_INVALID_ARG (NULL handle).
+ * enable != 0: later calls on this handle run batches with 128-row tiles (MXFP8 activations) on the
+ * CTA-pair grouped GEMMs -- two SMs per work item, one M = 256 tcgen05.mma.cta_group::2 per K step, each
+ * SM holding half the weight tile -- instead of the one-SM kernels (the default); enable = 0 restores
+ * the default.  Both give the same results (bit for bit in the tests); the pair kernel pads every expert
+ * group to an even number of row tiles, which costs more than it gains on skewed routing with many
+ * single-tile experts.  Tests compare the two; benchmarks measure one against the other.
+ * Errors: MOE_ERR_INVALID_ARG (NULL handle).
  */
 MOE_API moe_status_t moe_testing_set_pair_gemm(moe_experts_t experts, int32_t enable);
 

@@ -390,25 +390,25 @@ def test_bounded_wait_reports_timeout_and_context_survives():
 
 @pytest.mark.parametrize("name,T", [("medium", None), ("tiny", 256), ("tiny", 100)])
 def test_cta_pair_and_one_sm_gemms_both_match_the_oracle(name, T):
-    """Batches with 128-row tiles run their grouped GEMMs on CTA pairs (M = 256 over two SMs) by default;
-    the one-SM kernels remain selectable.  Both meet the strict bound and give the same routing; the
-    print shows how far apart their fp32 sums are (accumulation order)."""
+    """Batches with 128-row tiles run their grouped GEMMs on the one-SM kernels by default, or on CTA pairs
+    (M = 256 over two SMs) when the handle selects them.  Both meet the strict bound and give the same
+    routing; the print shows how far apart their fp32 sums are (accumulation order)."""
     from block_scaled_fp4_sqrt_gb300 import moe_testing_set_pair_gemm
     wl, inp, ids_ref, wts_ref, layer = case(name, T=T)
-    y_pair = _strict_layer_parity(wl, inp, ids_ref, wts_ref, layer, what=f"{name} T={wl.T} CTA pair")
-    y32_pair = layer.last_y32()
+    _strict_layer_parity(wl, inp, ids_ref, wts_ref, layer, what=f"{name} T={wl.T} one SM")
+    y32_one = layer.last_y32()
     for h in (layer.h, layer.h_shared):
-        moe_testing_set_pair_gemm(h, False)
+        moe_testing_set_pair_gemm(h, True)
     try:
-        _strict_layer_parity(wl, inp, ids_ref, wts_ref, layer, what=f"{name} T={wl.T} one SM")
-        y32_one = layer.last_y32()
+        _strict_layer_parity(wl, inp, ids_ref, wts_ref, layer, what=f"{name} T={wl.T} CTA pair")
+        y32_pair = layer.last_y32()
         torch.cuda.synchronize()
         d = (y32_pair - y32_one).abs().max().item() / y32_one.pow(2).mean().sqrt().item()
         print(f"{name} T={wl.T}: max |pair - one SM| / rms = {d:.3e}")
         assert d <= 2e-2
     finally:
         for h in (layer.h, layer.h_shared):
-            moe_testing_set_pair_gemm(h, True)
+            moe_testing_set_pair_gemm(h, False)
 
 
 def test_cta_pair_bounded_wait_reports_timeout_and_context_survives():
@@ -418,6 +418,8 @@ def test_cta_pair_bounded_wait_reports_timeout_and_context_survives():
     wl = WORKLOADS["tiny"].with_T(256)
     inp, ids_ref, wts_ref, _ = oracle.margin_filtered_layer(wl, seed=8)
     layer = _layer_from(inp)
+    for h in (layer.h, layer.h_shared):
+        m.moe_testing_set_pair_gemm(h, True)
     x = x_to_device(inp.x)
     m.moe_set_wait_budget(layer.h, 20_000_000)  # 20 ms
     m.moe_testing_stall_loads(layer.h, True)
