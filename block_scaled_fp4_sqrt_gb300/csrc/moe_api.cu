@@ -11,6 +11,7 @@
 #include <string>
 
 #include "moe.h"
+#include "moe_dispatch_state.cuh"
 #include "moe_internal.h"
 #include "moe_testing.h"
 
@@ -453,16 +454,18 @@ static moe_status_t check_input(const moe_experts_s* h, const moe_input_t* x) {
   return MOE_OK;
 }
 
-// disp: for learned routing with T <= kRouterSmallMaxT only (the small-batch router writes the dispatch state).
+// disp: the small-batch router (learned routing, T <= kRouterSmallMaxT) writes the dispatch state;
+// dout: the cluster router (learned, up to 256 experts) or the hash router writes it (T <= kRouterDispatchMaxT).
 static moe_status_t route_into(moe_experts_s* h, const moe_input_t* x, const float* router_w, const float* router_bias,
-                               int32_t* ids, float* wts, cudaStream_t s, const SmallDispatch* disp = nullptr) {
+                               int32_t* ids, float* wts, cudaStream_t s, const SmallDispatch* disp = nullptr,
+                               const DispatchOut* dout = nullptr) {
   const int T = x->T, E = h->cfg.n_experts, k = h->cfg.top_k, d = h->cfg.d_model;
   if (h->hash_table) {
     if (router_w || router_bias) return fail(MOE_ERR_INVALID_ARG, "hash layer: router_w and router_bias must be NULL");
     if (!x->token_ids) return fail(MOE_ERR_INVALID_ARG, "hash layer: token_ids is NULL");
     if (T == 0) return MOE_OK;
     MOE_CUDA(launch_hash_route(x->token_ids, h->hash_table, h->hash_V, T, E, k, h->cfg.route_scale, ids, wts, h->status,
-                               s),
+                               s, h->ws.route_done, dout),
              "hash route");
     return MOE_OK;
   }
@@ -496,7 +499,7 @@ static moe_status_t route_into(moe_experts_s* h, const moe_input_t* x, const flo
   }
   if (E <= 256) {  // logits, split-K reduction and top-k in one cluster kernel
     MOE_CUDA(launch_router_fused(tm_x, tm_w, router_bias, T, E, d, k, h->cfg.route_scale, router_fused_split(T, d), ids,
-                                 wts, h->status, h->budget_ns, s),
+                                 wts, h->status, h->budget_ns, s, h->ws.route_done, dout),
              "router");
     return MOE_OK;
   }
@@ -684,14 +687,21 @@ moe_status_t forward_impl(const moe_input_t* x, const float* router_w, const flo
   const Dims dm = dims_for(h->ws_max_T, E, k);
   const int n_chunks = (T + 31) / 32;
   const int bn = tile_rows_for(R, E);
-  // learned routing of a small batch: the router's last CTA also writes the dispatch state
-  const bool router_dispatch = !h->hash_table && T >= 1 && T <= kRouterSmallMaxT && bn >= kRouterSmallMaxT;
+  // learned routing of a small batch: the small-batch router's last CTA also writes the dispatch state
+  const bool small_dispatch = !h->hash_table && T >= 1 && T <= kRouterSmallMaxT && bn >= kRouterSmallMaxT;
   // the small-batch router's dispatch writes one tile per group: no pair padding, so one-SM GEMMs there
-  const bool pair = !router_dispatch && use_pairs(h, bn);
+  const bool pair = !small_dispatch && use_pairs(h, bn);
+  // batches up to kRouterDispatchMaxT rows: the cluster router's (or the hash router's) last CTA writes it
+  const bool big_dispatch = !small_dispatch && T >= 1 && T <= kRouterDispatchMaxT &&
+                            (h->hash_table ? dispatch_state_smem_ints(G, T) * 4 <= 48 * 1024 : E <= 256);
+  const bool router_dispatch = small_dispatch || big_dispatch;
   SmallDispatch sd{G, has_shared, bn, dm.max_tiles, h->ws.chunk_hist, h->ws.counts, h->ws.offsets, h->ws.tile_off,
                    h->ws.n_tiles, h->ws.tiles};
+  DispatchOut dout{G, has_shared, bn, dm.max_tiles, pair ? 1 : 0, h->ws.chunk_hist, h->ws.counts, h->ws.offsets,
+                   h->ws.tile_off, h->ws.n_tiles, h->ws.tiles};
   mark_stage(h, 0, s);
-  st = route_into(h, x, router_w, router_bias, h->ws.topk_ids, h->ws.topk_w, s, router_dispatch ? &sd : nullptr);
+  st = route_into(h, x, router_w, router_bias, h->ws.topk_ids, h->ws.topk_w, s, small_dispatch ? &sd : nullptr,
+                  big_dispatch ? &dout : nullptr);
   if (st != MOE_OK) return st;
   h->last_T = T;
   h->last_fwd_T = -1;

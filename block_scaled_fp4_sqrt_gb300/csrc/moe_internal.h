@@ -27,6 +27,7 @@ constexpr int kKGroup = 128;       // K elements per pipeline stage (one 128-byt
 constexpr int kSfAtomBytes = 512;  // scale-factor atom: 128 rows x 4 K-blocks of 32
 constexpr int kTileRows = 128;     // token rows per row tile (tcgen05 M) in the grouped GEMMs
 constexpr int kSmallTileRows = 32; // row tiles of the verify-batch shape (short activation slots)
+constexpr int kRouterDispatchMaxT = 1024;  // batches up to this size get their dispatch state from the router
 
 // One row tile of the grouped GEMMs: rows [row0, row0 + nrows) of group `group`.
 struct RowTile {
@@ -131,9 +132,12 @@ cudaError_t launch_router_logits(const __nv_bfloat16* x, const float* w, int T, 
 int router_tc_split(int T, int E, int d);
 int router_tc_epad(int E);
 int router_fused_split(int T, int d);
+struct DispatchOut;  // moe_dispatch_state.cuh
+// The cluster router; with disp, its last CTA also writes the batch's dispatch state (done: a zeroed counter).
 cudaError_t launch_router_fused(const CUtensorMap& tm_x, const CUtensorMap& tm_w, const float* bias, int T, int E,
                                 int d, int k, float route_scale, int split, int32_t* ids, float* wts, int* status,
-                                uint64_t budget_ns, cudaStream_t s);
+                                uint64_t budget_ns, cudaStream_t s, int* done = nullptr,
+                                const DispatchOut* disp = nullptr);
 cudaError_t launch_split_router(const float* w, int E, int d, __nv_bfloat16* out, cudaStream_t s);
 cudaError_t launch_router_tc(const CUtensorMap& tm_x, const CUtensorMap& tm_w, int T, int E, int d, int split,
                              float* partial, int* status, uint64_t budget_ns, cudaStream_t s);
@@ -158,8 +162,10 @@ struct SmallDispatch {
 cudaError_t launch_router_small(const __nv_bfloat16* x, const float* w, const float* bias, int T, int d, int E, int k,
                                 float route_scale, float* logits, int* done, int32_t* ids, float* wts,
                                 int early_params, const SmallDispatch* disp, cudaStream_t s);
+// The hash router; with disp, its last block also writes the batch's dispatch state (done: a zeroed counter).
 cudaError_t launch_hash_route(const int32_t* tok, const int32_t* table, int V, int T, int E, int k, float route_scale,
-                              int32_t* ids, float* wts, int* status, cudaStream_t s);
+                              int32_t* ids, float* wts, int* status, cudaStream_t s, int* done = nullptr,
+                              const DispatchOut* disp = nullptr);
 
 cudaError_t launch_histogram(const int32_t* ids, int T, int k, int E, int G, int32_t* chunk_hist, int* status,
                              cudaStream_t s);

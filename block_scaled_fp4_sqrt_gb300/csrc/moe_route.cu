@@ -5,6 +5,9 @@
 #include <float.h>
 
 #include "moe_device.cuh"
+#include "moe_dispatch_state.cuh"
+
+static_assert(moe::kRouterDispatchMaxT <= moe::kDispatchStateMaxT, "router-written dispatch state: batch size");
 
 namespace moe {
 
@@ -353,37 +356,51 @@ __global__ void __launch_bounds__(256) router_small_kernel(const __nv_bfloat16* 
 // Hash routing: ids = the token's table row (ascending), weights route_scale / k.  Out-of-range token
 // ids or table entries raise a device status bit and are replaced by valid values so that no later
 // kernel indexes out of bounds.
+// With disp.counts set, the last block to finish also writes the batch's dispatch state (dynamic shared
+// memory: dispatch_state_smem_ints(G, T) ints).
 __global__ void hash_route_kernel(const int32_t* __restrict__ tok, const int32_t* __restrict__ table, int V, int T,
                                   int E, int k, float route_scale, int32_t* __restrict__ ids, float* __restrict__ wts,
-                                  int* status) {
+                                  int* status, int* done, DispatchOut disp) {
   pdl_trigger();
   pdl_wait();
   int t = blockIdx.x * blockDim.x + threadIdx.x;
-  if (t >= T) return;
-  int v = tok[t];
-  if (v < 0 || v >= V) {
-    set_status(status, DEV_BAD_TOKEN_ID);
-    v = 0;
-  }
-  int row[kMaxTopK];
-  for (int j = 0; j < k; ++j) {
-    int e = table[(size_t)v * k + j];
-    if (e < 0 || e >= E) {
-      set_status(status, DEV_BAD_EXPERT_ID);
-      e = 0;
+  if (t < T) {
+    int v = tok[t];
+    if (v < 0 || v >= V) {
+      set_status(status, DEV_BAD_TOKEN_ID);
+      v = 0;
     }
-    row[j] = e;
+    int row[kMaxTopK];
+    for (int j = 0; j < k; ++j) {
+      int e = table[(size_t)v * k + j];
+      if (e < 0 || e >= E) {
+        set_status(status, DEV_BAD_EXPERT_ID);
+        e = 0;
+      }
+      row[j] = e;
+    }
+    for (int a = 1; a < k; ++a) {
+      int c = row[a], b = a - 1;
+      while (b >= 0 && row[b] > c) { row[b + 1] = row[b]; --b; }
+      row[b + 1] = c;
+    }
+    float w = route_scale / (float)k;
+    for (int j = 0; j < k; ++j) {
+      ids[(size_t)t * k + j] = row[j];
+      wts[(size_t)t * k + j] = w;
+    }
   }
-  for (int a = 1; a < k; ++a) {
-    int c = row[a], b = a - 1;
-    while (b >= 0 && row[b] > c) { row[b + 1] = row[b]; --b; }
-    row[b + 1] = c;
-  }
-  float w = route_scale / (float)k;
-  for (int j = 0; j < k; ++j) {
-    ids[(size_t)t * k + j] = row[j];
-    wts[(size_t)t * k + j] = w;
-  }
+  if (!disp.counts) return;
+  extern __shared__ int dsm[];
+  __shared__ int s_last;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) s_last = atomicAdd(done, 1) == (int)gridDim.x - 1;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  if (threadIdx.x == 0) *done = 0;
+  write_dispatch_state(ids, T, k, E, disp, dsm);
 }
 
 }  // namespace
@@ -441,9 +458,20 @@ cudaError_t launch_router_small(const __nv_bfloat16* x, const float* w, const fl
 }
 
 cudaError_t launch_hash_route(const int32_t* tok, const int32_t* table, int V, int T, int E, int k, float route_scale,
-                              int32_t* ids, float* wts, int* status, cudaStream_t s) {
-  return launch_pdl(hash_route_kernel, dim3((T + 127) / 128), dim3(128), 0, s, tok, table, V, T, E, k, route_scale, ids,
-                    wts, status);
+                              int32_t* ids, float* wts, int* status, cudaStream_t s, int* done,
+                              const DispatchOut* disp) {
+  DispatchOut dd{};
+  size_t smem = 0;
+  if (disp) {
+    if (!done || T > kDispatchStateMaxT) return cudaErrorInvalidValue;
+    dd = *disp;
+    smem = (size_t)dispatch_state_smem_ints(dd.G, T) * 4;
+    if (smem > 48 * 1024) return cudaErrorInvalidValue;
+  }
+  // with the dispatch state to write, wider blocks give its one writer block more warps
+  const int threads = disp ? 512 : 128;
+  return launch_pdl(hash_route_kernel, dim3((T + threads - 1) / threads), dim3(threads), smem, s, tok, table, V, T, E,
+                    k, route_scale, ids, wts, status, done, dd);
 }
 
 }  // namespace moe

@@ -9,6 +9,7 @@
 #include <algorithm>
 
 #include "moe_device.cuh"
+#include "moe_dispatch_state.cuh"
 
 namespace moe {
 
@@ -234,6 +235,8 @@ struct FusedArgs {
   int k_per_split;  // multiple of kRK
   int* status;
   uint64_t budget_ns;
+  int* done;         // CTAs finished (zero between calls), when the last one writes the dispatch state
+  DispatchOut disp;  // disp.counts == NULL: no dispatch state
 };
 
 __device__ __forceinline__ void cluster_sync_all() {
@@ -417,6 +420,19 @@ __global__ void __launch_bounds__(kFThreads, 1) router_fused_kernel(const __grid
   cluster_sync_all();  // no CTA leaves while another still reads its partial
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tbase, 256);
+  if (a.disp.counts) {
+    // the last CTA of the grid to finish writes the batch's dispatch state from the ids every CTA wrote
+    __shared__ int s_last;
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) s_last = atomicAdd(a.done, 1) == (int)(gridDim.x * gridDim.y) - 1;
+    __syncthreads();
+    if (s_last) {
+      __threadfence();
+      if (threadIdx.x == 0) *a.done = 0;  // every CTA of this call has counted
+      write_dispatch_state(a.ids, a.T, a.k, a.E, a.disp, reinterpret_cast<int*>(smem));
+    }
+  }
 }
 
 }  // namespace
@@ -501,9 +517,12 @@ static cudaError_t launch_fused_S(const CUtensorMap& tm_x, const CUtensorMap& tm
 
 cudaError_t launch_router_fused(const CUtensorMap& tm_x, const CUtensorMap& tm_w, const float* bias, int T, int E,
                                 int d, int k, float route_scale, int split, int32_t* ids, float* wts, int* status,
-                                uint64_t budget_ns, cudaStream_t s) {
+                                uint64_t budget_ns, cudaStream_t s, int* done, const DispatchOut* disp) {
   if (E > kRN) return cudaErrorInvalidValue;
-  const FusedArgs a{bias, ids, wts, T, E, router_tc_epad(E), d, k, route_scale, d / split, status, budget_ns};
+  if (disp && (!done || T > kDispatchStateMaxT || dispatch_state_smem_ints(disp->G, T) * 4 > kRStages * kRStage))
+    return cudaErrorInvalidValue;
+  FusedArgs a{bias, ids, wts, T, E, router_tc_epad(E), d, k, route_scale, d / split, status, budget_ns, done, {}};
+  if (disp) a.disp = *disp;
   switch (split) {
     case 1: return launch_fused_S<1>(tm_x, tm_w, a, s);
     case 2: return launch_fused_S<2>(tm_x, tm_w, a, s);
