@@ -49,7 +49,7 @@ struct moe_experts_s {
   int device = 0;
   int32_t last_T = 0;
   int32_t last_rows = 0;  // rows of the last grouped FFN (its h stays in the workspace)
-  int32_t last_fwd_T = -1;     // T of the last moe_forward (its fp32 expert rows stay in the workspace), or -1
+  int32_t last_fwd_T = -1;     // T of the last moe_forward (its expert rows stay in the workspace), or -1
   int32_t last_fwd_shared = 0;  // whether that forward had a shared expert
   int stall_loads = 0;
   int pair_gemm = 0;  // 128-row tiles on CTA pairs (moe_testing_set_pair_gemm); one-SM kernels by default
@@ -245,7 +245,8 @@ size_t workspace_layout(int max_T, int d, int f, int E, int k, Workspace* ws, vo
   w.a_sf = (uint8_t*)take((size_t)dm.max_tiles * (d / 128) * kSfAtomBytes);
   w.h_q = (uint8_t*)take((size_t)dm.rows * f);
   w.h_sf = (uint8_t*)take((size_t)dm.max_tiles * (f / 128) * kSfAtomBytes);
-  w.y_rows = (float*)take((size_t)dm.rows * d * 4);
+  w.y_rows.val = (__half*)take((size_t)dm.rows * d * 2);
+  w.y_rows.exp = (uint8_t*)take((size_t)dm.rows * (d / 32));
   w.route_done = (int32_t*)take(4);
   if (ws) *ws = w;
   return align_up(off, 256);
@@ -568,7 +569,7 @@ static bool use_pairs(const moe_experts_s* h, int tile_rows) {
 
 // pair: the work list pads every group to an even number of 128-row tiles; run both GEMMs on CTA pairs.
 static moe_status_t run_ffn(moe_experts_s* h, moe_experts_s* sh, int rows, int E_groups_shared_index,
-                            const uint8_t* a_q, const uint8_t* a_sf_atoms, const float* row_w, float* y_f32,
+                            const uint8_t* a_q, const uint8_t* a_sf_atoms, const float* row_w, ExpertRows y16,
                             __nv_bfloat16* y_bf16, int max_tiles, int tile_rows, bool timed, cudaStream_t s,
                             bool pair = false) {
   const int d = h->cfg.d_model, f = h->cfg.d_ff;
@@ -610,7 +611,7 @@ static moe_status_t run_ffn(moe_experts_s* h, moe_experts_s* sh, int rows, int E
            "gate-up GEMM");
   if (timed) mark_stage(h, 3, s);
   MOE_CUDA(launch_gemm_down(fp4 ? h->tm2p : h->tm2, fp4 ? shx->tm2p : shx->tm2, h->sf2, shx->sf2, tm_h, tm_h32,
-                            h->ws.h_sf, h->ws.tiles, h->ws.n_tiles, max_tiles, E_groups_shared_index, d, f, row_w, y_f32,
+                            h->ws.h_sf, h->ws.tiles, h->ws.n_tiles, max_tiles, E_groups_shared_index, d, f, row_w, y16,
                             y_bf16, h->status, h->budget_ns, h->stall_loads, tile_rows, fp4, h->num_sms, s,
                             pair ? &pm2 : nullptr),
            "down GEMM");
@@ -639,8 +640,8 @@ moe_status_t moe_expert_ffn(moe_experts_t h, int32_t n_rows, const int32_t* offs
   MOE_CUDA(launch_rows_sf_to_atoms(a_s, h->ws.tiles, h->ws.n_tiles, h->cfg.d_model, dm.max_tiles, h->ws.a_sf, s),
            "scale atoms");
   h->last_rows = n_rows;
-  return run_ffn(h, nullptr, n_rows, h->n, a_q, h->ws.a_sf, row_w, nullptr, static_cast<__nv_bfloat16*>(y_bf16),
-                 dm.max_tiles, bn, false, s, pair);
+  return run_ffn(h, nullptr, n_rows, h->n, a_q, h->ws.a_sf, row_w, ExpertRows{nullptr, nullptr},
+                 static_cast<__nv_bfloat16*>(y_bf16), dm.max_tiles, bn, false, s, pair);
 }
 
 moe_status_t moe_set_stage_events(moe_experts_t h, void* const* events, int32_t n) {

@@ -5,6 +5,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -487,6 +488,46 @@ __device__ __forceinline__ float exp2_neg_int(int s) {
   if (e >= 1) return __uint_as_float((uint32_t)e << 23);
   return __uint_as_float(1u << (22 + e));  // e in [0, -?]: only s = 127 reaches here (e = 0 -> 2^-127)
 }
+
+// ------------------------------------------------------------------------- scaled fp16 expert rows
+// Block exponent s of 32 expert-row values with maximum magnitude amax: amax * 2^-s lies in [2^14, 2^15),
+// inside fp16's range with its full 11 significant bits.  s stays in [-126, 127], so that 2^s and 2^-s are
+// normal fp32 numbers; an all-zero block takes s = 0.
+__device__ __forceinline__ int row16_block_exp(float amax) {
+  if (!(amax > 0.0f)) return 0;
+  const int s = floor_log2_f32(amax) - 14;
+  return s < -126 ? -126 : (s > 127 ? 127 : s);
+}
+
+// v[j] *= w, then the 32 products as fp16 times 2^-s (round to nearest even), packed in place: v[i] for
+// i < 16 then holds the bits of the fp16 pair (2i, 2i + 1), element 2i in the low half, and v[16..31] is
+// free.  Packing in place keeps the epilogue's register footprint at the 32 values.  Returns the block's
+// scale byte s + 127.
+__device__ __forceinline__ uint8_t row16_encode32(float (&v)[32], float w) {
+  float amax = 0.f;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    v[j] *= w;
+    amax = fmaxf(amax, fabsf(v[j]));
+  }
+  const int s = row16_block_exp(amax);
+  const float m = exp2_neg_int(s);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const __half2 h2 = __floats2half2_rn(v[2 * i] * m, v[2 * i + 1] * m);
+    v[i] = __uint_as_float(*reinterpret_cast<const uint32_t*>(&h2));
+  }
+  return (uint8_t)(s + 127);
+}
+
+// Packed word i of a block encoded by row16_encode32, as 16 bytes: words 4i .. 4i + 3.
+__device__ __forceinline__ uint4 row16_words(const float (&v)[32], int i) {
+  return make_uint4(__float_as_uint(v[4 * i]), __float_as_uint(v[4 * i + 1]), __float_as_uint(v[4 * i + 2]),
+                    __float_as_uint(v[4 * i + 3]));
+}
+
+// 2^(byte - 127) for a scale byte written by row16_encode32 (byte in [1, 254]).
+__device__ __forceinline__ float row16_scale(uint32_t byte) { return __uint_as_float(byte << 23); }
 
 // Round-to-nearest-even, saturating E4M3 conversion of two values (hardware cvt); lo in bits 0..7.
 __device__ __forceinline__ uint16_t e4m3x2(float lo, float hi) {

@@ -362,81 +362,95 @@ __global__ void __launch_bounds__(128) gather_kernel(
   }
 }
 
-// out[t, c] = bf16( sum_j Yr[inv_pos[t, j], c] + Yr[R + t, c] ), fp32 rows, 8 columns per thread.
+// out[t, c] = bf16( sum_j Yr[inv_pos[t, j], c] + Yr[R + t, c] ) in fp32; the rows are scaled fp16 (ExpertRows:
+// value * 2^(byte - 127), one byte per 32 columns), exact in fp32.  A block takes one token at a time and
+// a thread 16 columns of it: two 16-byte loads and one scale byte per row, all rows' loads in flight at
+// once (the combine streams the rows from HBM, so bytes in flight per thread set its speed).
 // F32OUT writes the same fp32 sum without the final rounding (the test hook moe_testing_read_y32).
 template <bool F32OUT>
-__global__ void combine_kernel(const float* __restrict__ y_rows, const int32_t* __restrict__ inv_pos, int T, int d,
-                               int k, int R, int has_shared, const __nv_bfloat16* residual, void* out_) {
+__global__ void __launch_bounds__(256, 2) combine_kernel(ExpertRows y_rows, const int32_t* __restrict__ inv_pos, int T,
+                                                      int d, int k, int R, int has_shared,
+                                                      const __nv_bfloat16* residual, void* out_) {
   pdl_trigger();
   pdl_wait();
-  const int vec_per_row = d / 8;
-  const size_t total = (size_t)T * vec_per_row;
-  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
-    const int t = (int)(i / vec_per_row), c8 = (int)(i % vec_per_row);
-    float acc[8];
-    if (residual) {  // a residual stream enters first: out = bf16(x + sum of the rows); out may alias it
-      const uint4 rv = reinterpret_cast<const uint4*>(residual + (size_t)t * d)[c8];
-      const __nv_bfloat16* rh = reinterpret_cast<const __nv_bfloat16*>(&rv);
+  const int vec_per_row = d / 16, nb = d / 32;
+  const __half* __restrict__ yv = y_rows.val;
+  const uint8_t* __restrict__ ye = y_rows.exp;
+  const int n = k + (has_shared ? 1 : 0);
+  for (int t = blockIdx.x; t < T; t += gridDim.x) {
+    for (int c = threadIdx.x; c < vec_per_row; c += blockDim.x) {
+      float acc[16];
+      if (residual) {  // a residual stream enters first: out = bf16(x + sum of the rows); out may alias it
+        const uint4* rp = reinterpret_cast<const uint4*>(residual + (size_t)t * d) + 2 * c;
+        const uint4 r0 = rp[0], r1 = rp[1];
+        const __nv_bfloat16* h0 = reinterpret_cast<const __nv_bfloat16*>(&r0);
+        const __nv_bfloat16* h1 = reinterpret_cast<const __nv_bfloat16*>(&r1);
 #pragma unroll
-      for (int q = 0; q < 8; ++q) acc[q] = __bfloat162float(rh[q]);
-    } else {
-#pragma unroll
-      for (int q = 0; q < 8; ++q) acc[q] = 0.f;
-    }
-    auto add_row = [&](int r) {
-      const float4* src = reinterpret_cast<const float4*>(y_rows + (size_t)r * d) + 2 * c8;
-      const float4 a = __ldg(src), b = __ldg(src + 1);
-      acc[0] += a.x;
-      acc[1] += a.y;
-      acc[2] += a.z;
-      acc[3] += a.w;
-      acc[4] += b.x;
-      acc[5] += b.y;
-      acc[6] += b.z;
-      acc[7] += b.w;
-    };
-    const int n = k + (has_shared ? 1 : 0);
-    if (n <= 8) {
-      // all row indices, then all row loads, then the sum in slot order: the loads overlap instead of
-      // queueing behind one another's latency
-      int rows[8];
-      float4 va[8], vb[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j)
-        rows[j] = j < k ? __ldg(&inv_pos[(size_t)t * k + j]) : (j == k && has_shared ? R + t : -1);
-#pragma unroll
-      for (int j = 0; j < 8; ++j)
-        if (rows[j] >= 0) {
-          const float4* src = reinterpret_cast<const float4*>(y_rows + (size_t)rows[j] * d) + 2 * c8;
-          va[j] = __ldg(src);
-          vb[j] = __ldg(src + 1);
+        for (int q = 0; q < 8; ++q) {
+          acc[q] = __bfloat162float(h0[q]);
+          acc[8 + q] = __bfloat162float(h1[q]);
         }
+      } else {
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-        if (rows[j] >= 0) {
-          acc[0] += va[j].x;
-          acc[1] += va[j].y;
-          acc[2] += va[j].z;
-          acc[3] += va[j].w;
-          acc[4] += vb[j].x;
-          acc[5] += vb[j].y;
-          acc[6] += vb[j].z;
-          acc[7] += vb[j].w;
+        for (int q = 0; q < 16; ++q) acc[q] = 0.f;
+      }
+      auto add = [&](uint4 v, float sc, int o) {
+        const __half2* h2 = reinterpret_cast<const __half2*>(&v);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float2 f = __half22float2(h2[q]);
+          acc[o + 2 * q] += f.x * sc;
+          acc[o + 2 * q + 1] += f.y * sc;
         }
-    } else {
-      for (int j = 0; j < k; ++j) add_row(__ldg(&inv_pos[(size_t)t * k + j]));
-      if (has_shared) add_row(R + t);
-    }
-    if (F32OUT) {
-      float4* dst = reinterpret_cast<float4*>(static_cast<float*>(out_) + (size_t)t * d) + 2 * c8;
-      dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-      dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
-    } else {
-      uint4 o;
-      __nv_bfloat16* ov = reinterpret_cast<__nv_bfloat16*>(&o);
+      };
+      if (n <= 8) {
+        // all row indices, then all row loads, then the sum in slot order
+        int rows[8];
+        uint4 va[8], vb[8];
+        uint32_t e[8];
 #pragma unroll
-      for (int q = 0; q < 8; ++q) ov[q] = __float2bfloat16_rn(acc[q]);
-      reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out_) + (size_t)t * d)[c8] = o;
+        for (int j = 0; j < 8; ++j)
+          rows[j] = j < k ? __ldg(&inv_pos[(size_t)t * k + j]) : (j == k && has_shared ? R + t : -1);
+        const uint4* yv4 = reinterpret_cast<const uint4*>(yv) + 2 * c;
+        const uint8_t* yec = ye + (c >> 1);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if (rows[j] >= 0) {  // 32-bit offsets: rows * d / 8 stays below 2^32 for every workspace size
+            const uint32_t o = (uint32_t)rows[j] * (uint32_t)(d / 8);
+            va[j] = __ldg(yv4 + o);
+            vb[j] = __ldg(yv4 + o + 1);
+            e[j] = __ldg(yec + (uint32_t)rows[j] * (uint32_t)nb);
+          }
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if (rows[j] >= 0) {
+            const float sc = row16_scale(e[j]);
+            add(va[j], sc, 0);
+            add(vb[j], sc, 8);
+          }
+      } else {
+        auto add_row = [&](int r) {
+          const uint4* p = reinterpret_cast<const uint4*>(yv + (size_t)r * d) + 2 * c;
+          const float sc = row16_scale(__ldg(ye + (size_t)r * nb + (c >> 1)));
+          add(__ldg(p), sc, 0);
+          add(__ldg(p + 1), sc, 8);
+        };
+        for (int j = 0; j < k; ++j) add_row(__ldg(&inv_pos[(size_t)t * k + j]));
+        if (has_shared) add_row(R + t);
+      }
+      if (F32OUT) {
+        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(out_) + (size_t)t * d) + 4 * c;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) dst[q] = make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
+      } else {
+        uint4 o[2];
+        __nv_bfloat16* ov = reinterpret_cast<__nv_bfloat16*>(o);
+#pragma unroll
+        for (int q = 0; q < 16; ++q) ov[q] = __float2bfloat16_rn(acc[q]);
+        uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out_) + (size_t)t * d) + 2 * c;
+        dst[0] = o[0];
+        dst[1] = o[1];
+      }
     }
   }
 }
@@ -489,18 +503,19 @@ cudaError_t launch_gather(const __nv_bfloat16* x, const int32_t* ids, const floa
                     offsets, tile_off, T, d, k, E, has_shared, bn, a_q, a_sf_atoms, a_s_rows, perm_tok, inv_pos, row_w);
 }
 
-cudaError_t launch_combine(const float* y_rows, const int32_t* inv_pos, int T, int d, int k, int R,
+cudaError_t launch_combine(ExpertRows y_rows, const int32_t* inv_pos, int T, int d, int k, int R,
                            int has_shared, const __nv_bfloat16* residual, __nv_bfloat16* out, cudaStream_t s,
                            float* out_f32) {
-  const size_t total = (size_t)T * (d / 8);
-  int blocks = (int)((total + 255) / 256);
-  if (blocks > 152 * 16) blocks = 152 * 16;
+  if ((uint64_t)(R + (has_shared ? T : 0)) * (uint64_t)(d / 8) >= (1ull << 32)) return cudaErrorInvalidValue;
+  const int vec_per_row = d / 16;
+  const int threads = vec_per_row >= 256 ? 256 : ((vec_per_row + 31) / 32) * 32;
+  int blocks = T < 152 * 8 ? T : 152 * 8;
   if (blocks < 1) blocks = 1;
   if (out_f32)
-    return launch_pdl(combine_kernel<true>, dim3(blocks), dim3(256), 0, s, y_rows, inv_pos, T, d, k, R, has_shared,
-                      residual, static_cast<void*>(out_f32));
-  return launch_pdl(combine_kernel<false>, dim3(blocks), dim3(256), 0, s, y_rows, inv_pos, T, d, k, R, has_shared,
-                    residual, static_cast<void*>(out));
+    return launch_pdl(combine_kernel<true>, dim3(blocks), dim3(threads), 0, s, y_rows, inv_pos, T, d, k, R,
+                      has_shared, residual, static_cast<void*>(out_f32));
+  return launch_pdl(combine_kernel<false>, dim3(blocks), dim3(threads), 0, s, y_rows, inv_pos, T, d, k, R,
+                    has_shared, residual, static_cast<void*>(out));
 }
 
 }  // namespace moe

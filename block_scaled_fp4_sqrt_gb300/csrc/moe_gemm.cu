@@ -5,9 +5,9 @@
 //    clamp(U, -L, L) (Ops.SiLUMulClamp, swiglu_limit = 10), re-quantised to MXFP8 along the FFN
 //    dimension ("expert FFN (fused dequant + GEMM)", FaStar README "Features"; TensorSharp page
 //    "How TensorSharp runs it").
-//  * down:     Y = w_row * (H . W2^T) per permuted row, fp32 (summed by the combine kernel, the
-//    weighted-sum epilogue moe_scatter_add of the TensorSharp page, "DSpark and MoE CPU offload") or
-//    bf16 (the standalone grouped FFN call).
+//  * down:     Y = w_row * (H . W2^T) per permuted row, as fp16 with one power-of-two scale per 32
+//    columns (summed in fp32 by the combine kernel, the weighted-sum epilogue moe_scatter_add of the
+//    TensorSharp page, "DSpark and MoE CPU offload") or bf16 (the standalone grouped FFN call).
 //
 // Tile shape.  One MMA (M = 128, N <= 256, K = 32) takes the same time for any N, so the weights sit
 // on the N side: 256 weight rows per MMA (gate 128 + up 128 of one 128-wide FFN slice, or 256 rows of
@@ -47,15 +47,15 @@ constexpr int kSmallRows = 32;  // groups this small load a 32-row activation bo
 constexpr int kEpiWarps = 16;
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 
-// Staging buffer of one epilogue warp for coalesced fp32 row stores: 8 rows x 32 columns (the warp's 32
-// rows pass through it 8 at a time), rows 144 B apart (36 floats) so that the row-per-lane writes and the
+// Staging buffer of one epilogue warp for coalesced expert-row stores: 8 rows of 128 bytes (the warp's 32
+// rows pass through it 8 at a time), rows 144 B apart (36 words) so that the row-per-lane writes and the
 // line-per-quarter-warp reads are both free of bank conflicts.  8 rows rather than 32 leave the shared
 // memory to one more pipeline stage of the down GEMM.
 constexpr int kStageStride = 36;
 constexpr int kStageRows = 8;
 constexpr int kStageFloats = kStageRows * kStageStride;
 
-// EPI = 1: the down projection's fp32 rows leave through a per-warp shared-memory transpose (full
+// EPI = 1: the down projection's expert rows leave through a per-warp shared-memory transpose (full
 // 128-byte lines per quarter warp) instead of 16-byte stores to 32 different rows per instruction.
 // FP4: packed MXFP4 operands (64-byte rows, kind::mxf4) instead of E4M3 x byte-expanded E2M1.
 template <int STAGES, int AROWS, int EPI = 0, bool FP4 = false>
@@ -97,15 +97,15 @@ struct GemmArgs {
   int E;        // group E is the shared expert
   int KG;       // K / 128
   int m_tiles;  // 256-wide output tiles per row tile (f/128 gate-up slices, or d/256)
-  int gate_up;  // 1: SwiGLU + MXFP8 epilogue; 0: weighted fp32 / bf16 rows
+  int gate_up;  // 1: SwiGLU + MXFP8 epilogue; 0: weighted rows (scaled fp16, or bf16)
   // gate-up epilogue
   float limit;
   uint8_t* h_q;
   uint8_t* h_sf;
   int f;
-  // down epilogue: exactly one of y_f32 / y_bf16 is set
+  // down epilogue: exactly one of y16.val / y_bf16 is set
   const float* row_w;
-  float* y_f32;
+  ExpertRows y16;
   __nv_bfloat16* y_bf16;
   int d;
   int* status;
@@ -124,41 +124,43 @@ __device__ __forceinline__ float silu_f(float z) { return __fdividef(z, 1.0f + _
 // The epilogue of one work item for one warp: the warp's 32 token rows (TMEM lane quadrant q) and its
 // column quarter c of the accumulator, already in registers (v0, v1), for row tile `ti` (rows rt) and
 // output tile mt.  Gate-up: SwiGLU with clamp, then the MX requantisation of h; down: the routing-weighted
-// rows, fp32 through the warp's staging buffer stg (EPI) or direct, or bf16.
+// rows, as scaled fp16 (ExpertRows) through the warp's staging buffer stg (EPI) or direct, or as bf16.
 template <int EPI, bool FP4>
 __device__ __forceinline__ void epilogue_rows(const GemmArgs& a, const RowTile& rt, int ti, int mt, int q, int c,
                                               int lane, float* stg, bool active, float (&v0)[32], float (&v1)[32]) {
   const int lr = q * 32 + lane;  // token row inside the tile
   if (EPI && !a.gate_up) {
-    // fp32 rows through the warp's staging buffer
+    // scaled fp16 rows through the warp's staging buffer
     if (active) {
       const bool row_ok = lr < rt.nrows;
       const float wr = !row_ok ? 0.f : (a.row_w ? __ldg(&a.row_w[rt.row0 + lr]) : 1.0f);
-      float* ybase = a.y_f32 + (size_t)rt.row0 * a.d + (size_t)mt * kN + 64 * c;
-      // lanes 8p .. 8p+7 write their rows' 32 values into the buffer; then each quarter warp stores one
-      // buffered row's 128 contiguous bytes (two rows per quarter warp and pass)
-      auto stage_half = [&](const float(&v)[32], int half) {
+      // this lane's row: 64 columns, 128 bytes, packed into v0[0..15] and v1[0..15]
+      const uint32_t e0 = row16_encode32(v0, wr), e1 = row16_encode32(v1, wr);
+      __half* ybase = a.y16.val + (size_t)rt.row0 * a.d + (size_t)mt * kN + 64 * c;
+      // lanes 8p .. 8p+7 write their rows' 128 bytes into the buffer; then each quarter warp stores one
+      // buffered row (four rows per pass and instruction, two instructions per pass)
 #pragma unroll
-        for (int p = 0; p < 32 / kStageRows; ++p) {
-          if ((lane >> 3) == p) {
-            float4* srow = reinterpret_cast<float4*>(stg + (lane & 7) * kStageStride);
+      for (int p = 0; p < 32 / kStageRows; ++p) {
+        if ((lane >> 3) == p) {
+          uint4* srow = reinterpret_cast<uint4*>(stg + (lane & 7) * kStageStride);
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-              srow[i] = make_float4(v[4 * i] * wr, v[4 * i + 1] * wr, v[4 * i + 2] * wr, v[4 * i + 3] * wr);
-          }
-          __syncwarp();
+          for (int i = 0; i < 4; ++i) srow[i] = row16_words(v0, i);
 #pragma unroll
-          for (int i = 0; i < 2; ++i) {
-            const int br = 4 * i + (lane >> 3);  // buffered row
-            const int rr = q * 32 + 8 * p + br;  // row inside the tile
-            const float4 val = reinterpret_cast<const float4*>(stg + br * kStageStride)[lane & 7];
-            if (rr < rt.nrows) reinterpret_cast<float4*>(ybase + (size_t)rr * a.d + 32 * half)[lane & 7] = val;
-          }
-          __syncwarp();
+          for (int i = 0; i < 4; ++i) srow[4 + i] = row16_words(v1, i);
         }
-      };
-      stage_half(v0, 0);
-      stage_half(v1, 1);
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const int br = 4 * i + (lane >> 3);  // buffered row
+          const int rr = q * 32 + 8 * p + br;  // row inside the tile
+          const uint4 val = reinterpret_cast<const uint4*>(stg + br * kStageStride)[lane & 7];
+          if (rr < rt.nrows) reinterpret_cast<uint4*>(ybase + (size_t)rr * a.d)[lane & 7] = val;
+        }
+        __syncwarp();
+      }
+      if (row_ok)
+        *reinterpret_cast<uint16_t*>(a.y16.exp + (size_t)(rt.row0 + lr) * (a.d / 32) + mt * (kN / 32) + 2 * c) =
+            (uint16_t)(e0 | (e1 << 8));
     }
     return;
   }
@@ -196,14 +198,14 @@ __device__ __forceinline__ void epilogue_rows(const GemmArgs& a, const RowTile& 
   } else {
     const float wr = a.row_w ? __ldg(&a.row_w[r]) : 1.0f;
     const size_t col0 = (size_t)mt * kN + 64 * c;
-    if (a.y_f32) {
-      float4* dst = reinterpret_cast<float4*>(a.y_f32 + (size_t)r * a.d + col0);
+    if (a.y16.val) {
+      const uint32_t e0 = row16_encode32(v0, wr), e1 = row16_encode32(v1, wr);
+      uint4* dst = reinterpret_cast<uint4*>(a.y16.val + (size_t)r * a.d + col0);
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
-        dst[i] = make_float4(v0[4 * i] * wr, v0[4 * i + 1] * wr, v0[4 * i + 2] * wr, v0[4 * i + 3] * wr);
+      for (int i = 0; i < 4; ++i) dst[i] = row16_words(v0, i);
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
-        dst[8 + i] = make_float4(v1[4 * i] * wr, v1[4 * i + 1] * wr, v1[4 * i + 2] * wr, v1[4 * i + 3] * wr);
+      for (int i = 0; i < 4; ++i) dst[4 + i] = row16_words(v1, i);
+      *reinterpret_cast<uint16_t*>(a.y16.exp + (size_t)r * (a.d / 32) + col0 / 32) = (uint16_t)(e0 | (e1 << 8));
     } else {
       uint4* dst = reinterpret_cast<uint4*>(a.y_bf16 + (size_t)r * a.d + col0);
 #pragma unroll
@@ -808,27 +810,28 @@ cudaError_t launch_pair(const PairMaps& pm, const CUtensorMap& act, const GemmAr
 }
 
 // tile_rows 32: 6 stages of 32-row activation slots.  tile_rows 128: 4 stages of 128-row slots, also for
-// the down projection's fp32 rows next to the epilogue's staging buffers (the 16-byte scattered
-// stores of the direct epilogue bound that GEMM at the 8192-token shape: 835 us with them, 373 us
+// the down projection's expert rows next to the epilogue's staging buffers (the 16-byte scattered
+// stores of a direct epilogue bounded that GEMM at the 8192-token shape: 835 us with them, 373 us
 // without any stores).
 // FP4: the packed weight ring is half as large, so every shape holds more stages.
-// pair (128-row tiles, MXFP8 activations): the CTA-pair kernel, 6 stages for gate-up and for the fp32 down
-// rows (next to their staging buffers); 5 stages for bf16 down rows (the grouped FFN call).
+// pair (128-row tiles, MXFP8 activations): the CTA-pair kernel, 6 stages for gate-up and for the down
+// projection's expert rows (next to their staging buffers); 5 stages for bf16 down rows (the grouped FFN
+// call).
 cudaError_t launch_grouped(const CUtensorMap& w, const CUtensorMap& w_sh, const CUtensorMap& act,
                            const CUtensorMap& act_small, const GemmArgs& a, int tile_rows, int act_fp4, int num_sms,
                            cudaStream_t s, const PairMaps* pair) {
   if (pair && tile_rows == kBM && !act_fp4) {
     if (a.gate_up) return launch_pair<6, 0>(*pair, act, a, num_sms, s);
-    if (a.y_f32) return launch_pair<6, 1>(*pair, act, a, num_sms, s);
+    if (a.y16.val) return launch_pair<6, 1>(*pair, act, a, num_sms, s);
     return launch_pair<5, 0>(*pair, act, a, num_sms, s);
   }
   if (act_fp4) {
     if (tile_rows == kSmallRows) return launch_shape<8, kSmallRows, 0, true>(w, w_sh, act, act_small, a, num_sms, s);
-    if (!a.gate_up && a.y_f32) return launch_shape<8, kBM, 1, true>(w, w_sh, act, act_small, a, num_sms, s);
+    if (!a.gate_up && a.y16.val) return launch_shape<8, kBM, 1, true>(w, w_sh, act, act_small, a, num_sms, s);
     return launch_shape<8, kBM, 0, true>(w, w_sh, act, act_small, a, num_sms, s);
   }
   if (tile_rows == kSmallRows) return launch_shape<6, kSmallRows, 0, false>(w, w_sh, act, act_small, a, num_sms, s);
-  if (!a.gate_up && a.y_f32) return launch_shape<4, kBM, 1, false>(w, w_sh, act, act_small, a, num_sms, s);
+  if (!a.gate_up && a.y16.val) return launch_shape<4, kBM, 1, false>(w, w_sh, act, act_small, a, num_sms, s);
   return launch_shape<4, kBM, 0, false>(w, w_sh, act, act_small, a, num_sms, s);
 }
 
@@ -865,7 +868,7 @@ cudaError_t launch_gemm_gate_up(const CUtensorMap& w_routed, const CUtensorMap& 
 cudaError_t launch_gemm_down(const CUtensorMap& w_routed, const CUtensorMap& w_shared, const uint8_t* sf_routed,
                              const uint8_t* sf_shared, const CUtensorMap& act, const CUtensorMap& act_small,
                              const uint8_t* act_sf, const RowTile* tiles, const int32_t* n_tiles, int max_tiles, int E,
-                             int d, int f, const float* row_w, float* y_f32, __nv_bfloat16* y_bf16, int* status,
+                             int d, int f, const float* row_w, ExpertRows y16, __nv_bfloat16* y_bf16, int* status,
                              uint64_t wait_budget_ns, int stall_loads, int tile_rows, int act_fp4, int num_sms,
                              cudaStream_t s, const PairMaps* pair) {
   GemmArgs a{};
@@ -880,7 +883,7 @@ cudaError_t launch_gemm_down(const CUtensorMap& w_routed, const CUtensorMap& w_s
   a.m_tiles = d / kN;
   a.gate_up = 0;
   a.row_w = row_w;
-  a.y_f32 = y_f32;
+  a.y16 = y16;
   a.y_bf16 = y_bf16;
   a.d = d;
   a.f = f;

@@ -3,6 +3,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -13,6 +14,15 @@
 #include "moe.h"
 
 namespace moe {
+
+// The weighted expert rows between the down GEMM and the combine: fp16 values [rows, d] and one scale byte
+// per 32 columns [rows, d / 32]; element = value * 2^(byte - 127).  The down epilogue picks each block's
+// scale so that the block maximum lands in [2^14, 2^15): every element keeps fp16's 11 significant bits
+// (rounding error at most 2^-11 relative) down to 2^-28 of its block maximum, whatever the weights' range.
+struct ExpertRows {
+  __half* val;
+  uint8_t* exp;
+};
 
 // Device status bits (sticky, OR-ed into the handle's status word).
 enum : int {
@@ -67,7 +77,7 @@ struct Workspace {
   uint8_t* a_sf;        // [max_tiles, d/128, 512]
   uint8_t* h_q;         // [rows, f]
   uint8_t* h_sf;        // [max_tiles, f/128, 512]
-  float* y_rows;         // [rows, d] weighted expert outputs (fp32)
+  ExpertRows y_rows;     // [rows, d] weighted expert outputs (scaled fp16) and [rows, d / 32] scales
   int32_t* route_done;   // [1] CTA count of the small-batch router (zero between calls)
 };
 
@@ -223,13 +233,13 @@ cudaError_t launch_gemm_down(const CUtensorMap& w_routed, const CUtensorMap& w_s
                              const uint8_t* sf_shared, const CUtensorMap& act, const CUtensorMap& act_small,
                              const uint8_t* act_sf,
                              const RowTile* tiles, const int32_t* n_tiles, int max_tiles, int E, int d, int f,
-                             const float* row_w, float* y_f32, __nv_bfloat16* y_bf16, int* status,
+                             const float* row_w, ExpertRows y16, __nv_bfloat16* y_bf16, int* status,
                              uint64_t wait_budget_ns, int stall_loads, int tile_rows, int act_fp4, int num_sms,
                              cudaStream_t s,
                                 const PairMaps* pair = nullptr);
 
 // out_f32 non-NULL: the fp32 sums go there instead, without the rounding to bf16 (out is then unused).
-cudaError_t launch_combine(const float* y_rows, const int32_t* inv_pos, int T, int d, int k, int R, int has_shared,
+cudaError_t launch_combine(ExpertRows y_rows, const int32_t* inv_pos, int T, int d, int k, int R, int has_shared,
                            const __nv_bfloat16* residual, __nv_bfloat16* out, cudaStream_t s,
                            float* out_f32 = nullptr);
 

@@ -205,7 +205,8 @@ MOE_API moe_status_t moe_expert_ffn(moe_experts_t experts, int32_t n_rows, const
 
 /*
  * The whole layer: out[t] = sum_j w_tj * FFN_{e_tj}(x_t) + FFN_shared(x_t), bf16 [T, d_model]
- * (fp32 sums, one rounding to bf16).  `shared` may be NULL (no shared expert).  Routing as in
+ * (each weighted row kept as fp16 with a power-of-two scale per 32 columns, the rows summed in fp32 in
+ * slot order, one rounding to bf16).  `shared` may be NULL (no shared expert).  Routing as in
  * moe_route (hash layers: router_w = router_bias = NULL).  The routing of the last call stays in
  * the workspace (moe_get_routing).  Everything stays on the device: the call never waits for the
  * GPU and copies nothing to or from the host.
