@@ -109,7 +109,8 @@ def expert_bytes(wl):
 
 def stage_bytes(wl, touched, rows, act: str = "mxfp8"):
     """Algorithmic HBM bytes per launch of each stage (touched = experts read, including the shared one).
-    Activation rows (A, H) take one byte per element in MXFP8 and half a byte in MXFP4."""
+    Activation rows (A, H) take one byte per element in MXFP8 and half a byte in MXFP4; the weighted expert
+    rows between the down GEMM and the combine take two bytes per element plus a scale byte per 32."""
     d, f, T, k, E = wl.d, wl.f, wl.T, wl.k, wl.E
     per = 2 if act == "mxfp4" else 1
     gate_up_w = 2 * f * d // 2 + 2 * f * d // 32
@@ -119,8 +120,8 @@ def stage_bytes(wl, touched, rows, act: str = "mxfp8"):
         "route": router,
         "dispatch": T * d * 2 + rows * (d // per + d // 32),
         "gemm_gate_up": touched * gate_up_w + rows * (d // per + d // 32) + rows * (f // per + f // 32),
-        "gemm_down": touched * down_w + rows * (f // per + f // 32) + rows * d * 4,
-        "combine": rows * d * 4 + T * d * 2,
+        "gemm_down": touched * down_w + rows * (f // per + f // 32) + rows * (2 * d + d // 32),
+        "combine": rows * (2 * d + d // 32) + T * d * 2,
     }
 
 
