@@ -385,25 +385,60 @@ __global__ void __launch_bounds__(kFThreads, 1) router_fused_kernel(const __grid
   for (int src = 0; src < S; ++src) remote[src] = cluster_map(part_addr, (uint32_t)src);
   // the warp's logit row, re-read in the one-expert-per-lane layout of the selection
   float* lrow = reinterpret_cast<float*>(smem + kRM * kFStride * 4) + warp * kRN;
-  for (int rr = warp; rr < rows_per; rr += kFThreads / 32) {
+  // lane l sums experts 4l..4l+3 and 128+4l..+3 of a row over the S partials, in rank order.  With few
+  // partials (S <= 4: long token loops per warp) both halves of the warp's next row are loaded while the
+  // current row is selected; with more, per half, S 16-byte loads are in flight at once.
+  constexpr bool kAhead = S <= 4;
+  constexpr int kNext = kAhead ? 2 * S : 1;
+  constexpr int kWarps = kFThreads / 32;
+  float4 nxt[kNext];
+  auto fetch = [&](int rr) {
+    const int r = z * rows_per + rr;
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+      for (int src = 0; src < S; ++src)
+        nxt[(h * S + src) % kNext] = ld_cluster_f4(remote[src] + (uint32_t)((r * kFStride + 128 * h + 4 * lane) * 4));
+  };
+  if (kAhead && warp < rows_per && t0 + z * rows_per + warp < a.T) fetch(warp);
+  for (int rr = warp; rr < rows_per; rr += kWarps) {
     const int r = z * rows_per + rr, t = t0 + r;
     if (t >= a.T) continue;  // warp-uniform
-    // lane l sums experts 4l..4l+3 and 128+4l..: per half, S 16-byte loads in flight at once
+    if (kAhead) {
+      float4 cur[kNext];
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const uint32_t off = (uint32_t)((r * kFStride + 128 * h + 4 * lane) * 4);
-      float4 v[S];
+      for (int i = 0; i < kNext; ++i) cur[i] = nxt[i];
+      if (rr + kWarps < rows_per && t + kWarps < a.T) fetch(rr + kWarps);
 #pragma unroll
-      for (int src = 0; src < S; ++src) v[src] = ld_cluster_f4(remote[src] + off);
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int h = 0; h < 2; ++h) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-      for (int src = 0; src < S; ++src) {
-        acc.x += v[src].x;
-        acc.y += v[src].y;
-        acc.z += v[src].z;
-        acc.w += v[src].w;
+        for (int src = 0; src < S; ++src) {
+          const float4 v = cur[(h * S + src) % kNext];
+          acc.x += v.x;
+          acc.y += v.y;
+          acc.z += v.z;
+          acc.w += v.w;
+        }
+        reinterpret_cast<float4*>(lrow + 128 * h)[lane] = acc;
       }
-      reinterpret_cast<float4*>(lrow + 128 * h)[lane] = acc;
+    } else {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const uint32_t off = (uint32_t)((r * kFStride + 128 * h + 4 * lane) * 4);
+        float4 v[S];
+#pragma unroll
+        for (int src = 0; src < S; ++src) v[src] = ld_cluster_f4(remote[src] + off);
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int src = 0; src < S; ++src) {
+          acc.x += v[src].x;
+          acc.y += v[src].y;
+          acc.z += v[src].z;
+          acc.w += v[src].w;
+        }
+        reinterpret_cast<float4*>(lrow + 128 * h)[lane] = acc;
+      }
     }
     __syncwarp();
     float sc[8], sel[8];
