@@ -499,19 +499,18 @@ __device__ __forceinline__ int row16_block_exp(float amax) {
   return s < -126 ? -126 : (s > 127 ? 127 : s);
 }
 
-// v[j] *= w, then the 32 products as fp16 times 2^-s (round to nearest even), packed in place: v[i] for
-// i < 16 then holds the bits of the fp16 pair (2i, 2i + 1), element 2i in the low half, and v[16..31] is
-// free.  Packing in place keeps the epilogue's register footprint at the 32 values.  Returns the block's
-// scale byte s + 127.
+// The 32 products v[j] * w as fp16 times 2^-s (round to nearest even), packed in place: v[i] for i < 16 then
+// holds the bits of the fp16 pair (2i, 2i + 1), element 2i in the low half, and v[16..31] is free.  The
+// scale is taken from max |v| * |w| (rounding is monotonic, so this is the largest rounded product) and the
+// weight folded into one multiplier w * 2^-s: scaling by a power of two commutes with rounding, so each code
+// is that of the rounded product whenever nothing is subnormal.  Packing in place keeps the epilogue's
+// register footprint at the 32 values.  Returns the block's scale byte s + 127.
 __device__ __forceinline__ uint8_t row16_encode32(float (&v)[32], float w) {
   float amax = 0.f;
 #pragma unroll
-  for (int j = 0; j < 32; ++j) {
-    v[j] *= w;
-    amax = fmaxf(amax, fabsf(v[j]));
-  }
-  const int s = row16_block_exp(amax);
-  const float m = exp2_neg_int(s);
+  for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(v[j]));
+  const int s = row16_block_exp(amax * fabsf(w));
+  const float m = w * exp2_neg_int(s);
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
     const __half2 h2 = __floats2half2_rn(v[2 * i] * m, v[2 * i + 1] * m);
