@@ -45,7 +45,28 @@ constexpr int kN = 256;         // weight rows per MMA (tcgen05 N)
 constexpr int kBM = kTileRows;  // token rows per MMA (tcgen05 M) = 128
 constexpr int kSmallRows = 32;  // groups this small load a 32-row activation box
 constexpr int kEpiWarps = 16;
-constexpr int kThreads = 64 + 32 * kEpiWarps;
+constexpr int kThreads = 64 + 32 * kEpiWarps;  // the CTA-pair kernel: producer, issuer, 16 epilogue warps
+
+// The one-SM kernel's warps.  A warp reaches the TMEM lanes of quadrant (warp % 4) only, and warps with the
+// same index mod 4 share one of the SM's four sub-partitions (issue slots).  Warp 1 issues the MMAs.
+// In the 32-row shape only quadrant 0's four epilogue warps work, so the producer sits on another
+// sub-partition: warp 2 produces, warp 16 idles, and the epilogue warps are four per quadrant
+//   q0: 0 4 8 12   q1: 5 9 13 17   q2: 6 10 14 18   q3: 3 7 11 15   (column quarter = position in the list);
+// that took the verify512 step from 0.628 to 0.618 ms (A/B on one box).  With 128-row tiles every quadrant
+// works and both that placement and a 19th (idle) warp measured 0.5-1 % slower at T = 8192, so there the
+// CTA keeps 18 warps: warp 0 produces and warps 2..17 drain (column quarter (warp - 2) / 4).
+template <int AROWS>
+struct Roles1 {
+  static constexpr bool kSmall = AROWS == 32;
+  static constexpr int kThreads = kSmall ? 19 * 32 : 18 * 32;
+  static constexpr int kProducer = kSmall ? 2 : 0;
+  static constexpr int kIdle = kSmall ? 16 : -1;
+  __device__ static int quarter(int warp) {
+    if (!kSmall) return (warp - 2) >> 2;
+    const int q = warp & 3;
+    return (warp - (q == 0 ? 0 : q == 1 ? 5 : q == 2 ? 6 : 3)) >> 2;
+  }
+};
 
 // Staging buffer of one epilogue warp for coalesced expert-row stores: 8 rows of 128 bytes (the warp's 32
 // rows pass through it 8 at a time), rows 144 B apart (36 words) so that the row-per-lane writes and the
@@ -231,7 +252,7 @@ __device__ __forceinline__ void epilogue_rows(const GemmArgs& a, const RowTile& 
 }
 
 template <int STAGES, int AROWS, int EPI, bool FP4>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Roles1<AROWS>::kThreads, 1)
     grouped_mx_gemm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_w_shared,
                            const __grid_constant__ CUtensorMap tm_act, const __grid_constant__ CUtensorMap tm_act_small,
                            const GemmArgs a) {
@@ -283,7 +304,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (n_tiles > a.max_tiles) n_tiles = a.max_tiles;
   const int total = n_tiles * a.m_tiles;
 
-  if (warp == 0) {
+  using R = Roles1<AROWS>;
+  if (warp == R::kProducer) {
     if (lane == 0) {
       // ---------------------------------------------------------------- TMA producer
       // weights: streamed once by the 32-row (verify) shape; with 128-row tiles an expert's slab is read by
@@ -438,11 +460,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(drain, 0, a.budget_ns)) set_status(a.status, DEV_TIMEOUT);
       }
     }
-  } else {
-    // ------------------------------------------------------------------ epilogue (warps 2..17)
+  } else if (warp != R::kIdle) {
+    // ------------------------------------------------------------------ epilogue (16 warps)
     const int q = warp & 3;         // TMEM lane quadrant: token rows 32q .. 32q+31
-    const int c = (warp - 2) >> 2;  // column quarter
-    const int lr = q * 32 + lane;   // token row inside the tile
+    const int c = R::quarter(warp); // column quarter
+    const int lr = q * 32 + lane;       // token row inside the tile
     int it = 0;
     // 32-row tiles keep their rows in TMEM lanes 0..31: the other quadrants' warps have nothing to do
     const int my_total = (AROWS == kSmallRows && q != 0) ? 0 : total;
@@ -472,7 +494,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(acc_empty);
       epilogue_rows<EPI, FP4, AROWS == kBM ? kEpiNapNs : 0>(a, rt, ti, mt, q, c, lane,
-                              reinterpret_cast<float*>(smem + C::kEpiOff) + (warp - 2) * kStageFloats, active, v0, v1);
+                              reinterpret_cast<float*>(smem + C::kEpiOff) + (4 * q + c) * kStageFloats, active, v0,
+                              v1);
     }
   }
 
@@ -773,8 +796,8 @@ cudaError_t launch_shape(const CUtensorMap& w, const CUtensorMap& w_sh, const CU
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   });
   if (e != cudaSuccess) return e;
-  return launch_pdl(grouped_mx_gemm_kernel<STAGES, AROWS, EPI, FP4>, dim3(num_sms), dim3(kThreads), C::kSmem, s, w,
-                    w_sh, act, act_small, a);
+  return launch_pdl(grouped_mx_gemm_kernel<STAGES, AROWS, EPI, FP4>, dim3(num_sms), dim3(Roles1<AROWS>::kThreads),
+                    C::kSmem, s, w, w_sh, act, act_small, a);
 }
 
 // CTA-pair launch: clusters of two CTAs with programmatic dependent launch.  The grid is as many pairs as
