@@ -72,12 +72,15 @@ struct Roles1 {
 // rows pass through it 8 at a time), rows 144 B apart (36 words) so that the row-per-lane writes and the
 // line-per-quarter-warp reads are both free of bank conflicts.  8 rows rather than 32 leave the shared
 // memory to one more pipeline stage of the down GEMM.
-// 128-row shape: the epilogue pauses this many ns every 8 h elements (gate-up) or after each staged pass
-// (down).  Its 16 warps share the SM's issue slots with the single MMA-issuing thread and the TMA producer;
-// spreading their work over the item instead of running it in one burst after each handoff took the
-// prefill step from 1.404 to 1.398 ms at 300 ns (800 ns: 1.394 ms against 1.389 ms with the folded row scale
-// of row16_encode32).  A down item leaves about 3 us of slack for its epilogue.
-constexpr int kEpiNapNs = 300;
+// 128-row shape: the epilogue pauses every 8 h elements (gate-up) or after each staged pass (down).  Its 16
+// warps share the SM's issue slots with the single MMA-issuing thread (warp 1, the sub-partition of
+// quadrant 1's warps) and the TMA producer (warp 0, quadrant 0's); spreading their work over the item
+// instead of running it in one burst after each handoff shortens the items.  Measured on the prefill step
+// (A/B on one box): no pause 1.404 ms; 300 ns for every warp 1.398; 400 ns beside the producer and the
+// issuer with 100 ns elsewhere 1.383 (600 / 0 ns: 1.391).  A down item leaves about 3 us of slack for its
+// epilogue.
+constexpr uint32_t kEpiNapNear = 400;  // quadrants 0 and 1
+constexpr uint32_t kEpiNapFar = 100;   // quadrants 2 and 3
 
 constexpr int kStageStride = 36;
 constexpr int kStageRows = 8;
@@ -153,9 +156,10 @@ __device__ __forceinline__ float silu_f(float z) { return __fdividef(z, 1.0f + _
 // column quarter c of the accumulator, already in registers (v0, v1), for row tile `ti` (rows rt) and
 // output tile mt.  Gate-up: SwiGLU with clamp, then the MX requantisation of h; down: the routing-weighted
 // rows, as scaled fp16 (ExpertRows) through the warp's staging buffer stg (EPI) or direct, or as bf16.
-template <int EPI, bool FP4, int NAP = 0>
+template <int EPI, bool FP4>
 __device__ __forceinline__ void epilogue_rows(const GemmArgs& a, const RowTile& rt, int ti, int mt, int q, int c,
-                                              int lane, float* stg, bool active, float (&v0)[32], float (&v1)[32]) {
+                                              int lane, float* stg, bool active, float (&v0)[32], float (&v1)[32],
+                                              uint32_t nap = 0) {
   const int lr = q * 32 + lane;  // token row inside the tile
   if (EPI && !a.gate_up) {
     // scaled fp16 rows through the warp's staging buffer
@@ -185,7 +189,7 @@ __device__ __forceinline__ void epilogue_rows(const GemmArgs& a, const RowTile& 
           if (rr < rt.nrows) reinterpret_cast<uint4*>(ybase + (size_t)rr * a.d)[lane & 7] = val;
         }
         __syncwarp();
-        if (NAP) __nanosleep(NAP);
+        if (nap) __nanosleep(nap);
       }
       if (row_ok)
         *reinterpret_cast<uint16_t*>(a.y16.exp + (size_t)(rt.row0 + lr) * (a.d / 32) + mt * (kN / 32) + 2 * c) =
@@ -205,7 +209,7 @@ __device__ __forceinline__ void epilogue_rows(const GemmArgs& a, const RowTile& 
       const float uc = fminf(fmaxf(v1[j], -L), L);
       h[j] = silu_f(gc) * uc;
       amax = fmaxf(amax, fabsf(h[j]));
-      if (NAP && (j & 7) == 7) __nanosleep(NAP);
+      if (nap && (j & 7) == 7) __nanosleep(nap);
     }
     const int se = FP4 ? mxfp4_block_exp(amax) : mxfp8_block_exp(amax);
     const float mul = exp2_neg_int(se);
@@ -493,9 +497,9 @@ __global__ void __launch_bounds__(Roles1<AROWS>::kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(acc_empty);
-      epilogue_rows<EPI, FP4, AROWS == kBM ? kEpiNapNs : 0>(a, rt, ti, mt, q, c, lane,
+      epilogue_rows<EPI, FP4>(a, rt, ti, mt, q, c, lane,
                               reinterpret_cast<float*>(smem + C::kEpiOff) + (4 * q + c) * kStageFloats, active, v0,
-                              v1);
+                              v1, AROWS == kBM ? (q <= 1 ? kEpiNapNear : kEpiNapFar) : 0u);
     }
   }
 
