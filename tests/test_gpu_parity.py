@@ -222,6 +222,41 @@ def test_expert_ffn_wide_weight_scales():
         layer.close()
 
 
+@pytest.mark.parametrize("case", ["up60", "down60", "rows40"])
+def test_forward_expert_rows_across_the_fp32_range(case):
+    """The weighted expert rows travel from the down GEMM to the combine as fp16 with one power-of-two scale
+    per 32 columns.  Drive them far outside fp16's own range and across a wide range inside one block, then
+    compare the fp32 sums strictly with the oracle: every down scale byte (routed and shared) 60 binades up
+    (rows near 2^60, far above fp16's 65504), 60 down (rows near 2^-60, far below its smallest normal), or
+    each output row of W2 shifted by its own draw from -20..20 binades (columns inside one 32-column block
+    of y then span up to 2^40)."""
+    wl = WORKLOADS["tiny"].with_T(64)
+    inp, ids_ref, wts_ref, _ = oracle.margin_filtered_layer(wl, seed=11)
+    rng = np.random.default_rng(11)
+    for ew in (inp.experts, inp.shared):
+        sc = ew.s2.astype(np.int64)  # [n, d, f / 32]
+        if case == "up60":
+            sc += 60
+        elif case == "down60":
+            sc -= 60
+        else:
+            sc += rng.integers(-20, 21, size=sc.shape[:2])[:, :, None]
+        assert sc.min() >= 1 and sc.max() <= 254
+        ew.s2 = sc.astype(np.uint8)
+    layer = _layer_from(inp)
+    try:
+        y = _strict_layer_parity(wl, inp, ids_ref, wts_ref, layer, what=f"rows {case}")
+        assert torch.isfinite(y.float()).all()
+        y_ref, _, _, _ = oracle.layer(inp.x, ids_ref, wts_ref, inp.experts, inp.shared, wl.swiglu_limit, want_h=True)
+        mag = float(np.sqrt(np.mean(y_ref ** 2)))
+        if case == "up60":
+            assert mag > 2.0 ** 50
+        elif case == "down60":
+            assert mag < 2.0 ** -50
+    finally:
+        layer.close()
+
+
 @pytest.mark.parametrize("name", ["tiny", "wide", "verify8", "verify512"])
 def test_resident_router_matches_per_call_router(name):
     """moe_experts_set_router (weights split once on the handle) gives the per-call router's ids,
