@@ -257,6 +257,24 @@ def test_forward_expert_rows_across_the_fp32_range(case):
         layer.close()
 
 
+@pytest.mark.parametrize("T", [1024, 1025])
+@pytest.mark.parametrize("routing", ["learned", "hash"])
+def test_forward_at_the_dispatch_state_boundary(routing, T):
+    """Up to 1024 rows the routing kernel's last CTA writes the dispatch state (chunk bases, counts, offsets,
+    the tile list); above that the histogram and scan kernels do.  Both sides of the switch, for the cluster
+    router and the hash router, every row against the oracle (d = 1024, f = 512, 16 experts top-4: about 256
+    rows per expert, several 128-row tiles each)."""
+    wl = synth.Workload(f"boundary_{routing}", T, 1024, 512, 16, 4, hash_vocab=4096 if routing == "hash" else 0)
+    inp, ids_ref, wts_ref, _ = oracle.margin_filtered_layer(wl, seed=5)
+    layer = _layer_from(inp)
+    try:
+        _strict_layer_parity(wl, inp, ids_ref, wts_ref, layer, what=f"{routing} T={T}")
+        counts, _, _, _ = oracle.permute(ids_ref, wl.E)
+        assert counts.min() > 128  # every expert group spans more than one 128-row tile
+    finally:
+        layer.close()
+
+
 @pytest.mark.parametrize("name", ["tiny", "wide", "verify8", "verify512"])
 def test_resident_router_matches_per_call_router(name):
     """moe_experts_set_router (weights split once on the handle) gives the per-call router's ids,
